@@ -1,0 +1,475 @@
+"""Benchmark: W8A16 FP8 block-scaled decode GEMM on GB300 (one JSON line).
+
+Headline workload: FFN gate/up, M=16, N=17408, K=5120 (89 MB of E4M3
+weights, [128 x 128] FP32 block scales, BF16 X and Y).  One step is one call of
+the whole path (weight stream, dequant, tensor-core MMA, two-level fold,
+split-K reduction, BF16 store).  Inputs are resident in HBM; the weight
+matrix rotates over enough copies (>= 2x the L2 size) that no step finds its
+weights in L2.  `value` is algorithmic bytes per call (W + scales + X + Y,
+each counted once) / device time per call.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--quick]
+
+Under torchrun each rank runs an independent replica (the GEMM has no
+exchange step); rank 0 prints the line with the max time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "achieved HBM GB/s (and µs/call) of FP8 block-scaled W8A16 GEMM at M=1..32"
+PAGE_BASELINE_GBPS = 342.0   # H100 w8a16_gemv_batch16, gate/up, M=16 (atlas page, WHY table)
+HEAD = dict(M=16, N=17408, K=5120, config_id=1)
+L2_BYTES = 129 * 1000 * 1000
+
+
+def fp8_bytes(M, N, K):
+    nb, kb = -(-N // 128), -(-K // 128)
+    return N * K + nb * kb * 4 + M * K * 2 + M * N * 2
+
+
+def lut3_bytes(M, N, K):
+    return (-(-N // 128)) * (-(-K // 256)) * 16384 + N * (K // 128) * 2 + 16 + M * K * 2 + M * N * 2
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "weight_only_quantized_qgemm_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(name, calls_bytes):
+    """DRAM bytes per launch from a committed ncu summary of the same kernel
+    source, else None."""
+    path = os.path.join(ROOT, "profiles", f"{name}.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except Exception:
+        return None
+    if d.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    t = d.get("dram_bytes_per_launch")
+    if t is None:
+        return None
+    scale = d.get("scale_to_full", 1.0)
+    return float(t) * float(scale)
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_uuid=None):
+        self.rows = []
+        self.proc = None
+        self.uuid = device_uuid
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"]
+        if self.uuid:
+            cmd += ["-i", self.uuid]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self._t = threading.Thread(target=self._read, daemon=True)
+        self._first = threading.Event()
+        self._t.start()
+        self._first.wait(timeout=5.0)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), line.strip()))
+            self._first.set()
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        for _, line in self.rows:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def gpu_uuid(torch, dev):
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return None
+
+
+# ----------------------------------------------------------------- our arm
+def time_calls(torch, stream, fn, steps, warmup):
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            fn(i)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for i in range(steps):
+            fn(i)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps  # ms per call
+
+
+def fp8_case(torch, qg, M, N, K, config_id, copies_min=1):
+    import workloads as wl
+    p = wl.make_fp8_problem(M, N, K, config_id=config_id)
+    copies = max(copies_min, -(-2 * L2_BYTES // (N * K)) + 1)
+    W = [torch.from_numpy(p.W).cuda() for _ in range(copies)]
+    S = torch.from_numpy(p.S).cuda()
+    X = torch.from_numpy(p.X.view(np.int16)).view(torch.bfloat16).cuda()
+    Y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    ws = qg.Workspace()
+    return p, W, S, X, Y, ws, copies
+
+
+def bench_fp8(torch, qg, stream, M, N, K, config_id, steps, warmup):
+    p, W, S, X, Y, ws, copies = fp8_case(torch, qg, M, N, K, config_id)
+    wsbuf = ws.get(qg.workspace_bytes(qg.KIND_FP8_BLOCK, M, N, K))
+    ws_ptr = wsbuf.data_ptr() if wsbuf is not None else None
+    ws_n = wsbuf.numel() if wsbuf is not None else 0
+    lib = qg.lib
+    sptr = stream.cuda_stream
+    xp, yp, sp = X.data_ptr(), Y.data_ptr(), S.data_ptr()
+    wps = [w.data_ptr() for w in W]
+
+    def step(i):
+        r = lib.qgemm_fp8_block(xp, K, wps[i % copies], sp, yp, N, M, N, K, ws_ptr, ws_n, sptr)
+        if r:
+            raise RuntimeError(qg.status_string(r))
+
+    ms = time_calls(torch, stream, step, steps, warmup)
+    st = qg.last_device_status(stream)
+    if st:
+        raise RuntimeError(f"device status {qg.status_string(st)}")
+    return ms, copies, p, (W, S, X, Y, ws)
+
+
+def bench_lut3(torch, qg, stream, M, N, K, steps, warmup):
+    import workloads as wl
+    p = wl.make_lut3_problem(M, N, K, config_id=4)
+    packed = qg.pack_lut3(p.codes)
+    copies = max(1, -(-2 * L2_BYTES // packed.size) + 1)
+    Wq = [torch.from_numpy(packed).cuda() for _ in range(copies)]
+    qm = torch.from_numpy(p.qmap.view(np.int16)).view(torch.float16).cuda()
+    sc = torch.from_numpy(p.scales.view(np.int16)).view(torch.float16).cuda()
+    X = torch.from_numpy(p.X.view(np.int16)).view(torch.float16).cuda()
+    Y = torch.empty((M, N), dtype=torch.float16, device="cuda")
+    ws = qg.Workspace()
+    wsbuf = ws.get(qg.workspace_bytes(qg.KIND_LUT3, M, N, K))
+    ws_ptr = wsbuf.data_ptr() if wsbuf is not None else None
+    ws_n = wsbuf.numel() if wsbuf is not None else 0
+    lib = qg.lib
+    sptr = stream.cuda_stream
+    wps = [w.data_ptr() for w in Wq]
+
+    def step(i):
+        r = lib.qgemm_lut3(X.data_ptr(), K, wps[i % copies], qm.data_ptr(), sc.data_ptr(), Y.data_ptr(), N,
+                           M, N, K, ws_ptr, ws_n, sptr)
+        if r:
+            raise RuntimeError(qg.status_string(r))
+
+    ms = time_calls(torch, stream, step, steps, warmup)
+    st = qg.last_device_status(stream)
+    if st:
+        raise RuntimeError(f"device status {qg.status_string(st)}")
+    return ms, copies
+
+
+def e2e_fp8(torch, qg, stream, state, M, N, K, steps, warmup):
+    """Through the public Python API with host buffers: each step copies X in
+    from pinned host memory and Y back out, inside the timed region."""
+    W, S, X, Y, ws = state
+    copies = len(W)
+    Xh = torch.empty(X.shape, dtype=X.dtype).pin_memory()
+    Xh.copy_(X.cpu())
+    Yh = torch.empty(Y.shape, dtype=Y.dtype).pin_memory()
+
+    def step(i):
+        X.copy_(Xh, non_blocking=True)
+        qg.qgemm_fp8_block(X, W[i % copies], S, Y=Y, workspace=ws, stream=stream)
+        Yh.copy_(Y, non_blocking=True)
+
+    ms = time_calls(torch, stream, step, steps, warmup)
+    return ms, X.numel() * X.element_size(), Y.numel() * Y.element_size()
+
+
+def cpu_baseline(M, N, K, config_id, budget_s=12.0):
+    """The oracle as it stands, on the host cores, over a column sample of the
+    same workload sized to roughly `budget_s` seconds."""
+    import oracle
+    import workloads as wl
+    p = wl.make_fp8_problem(M, N, K, config_id=config_id)
+    nt = oracle.max_threads()
+    cols = 512
+    t0 = time.perf_counter()
+    oracle.qgemm_fp8_block(p.X, p.W[:cols], p.S[: -(-cols // 128)], nthreads=nt)
+    dt = time.perf_counter() - t0
+    n_s = int(min(N, max(128, (budget_s / max(dt, 1e-6)) * cols)) // 128 * 128)
+    t0 = time.perf_counter()
+    oracle.qgemm_fp8_block(p.X, p.W[:n_s], p.S[: -(-n_s // 128)], nthreads=nt)
+    dt = time.perf_counter() - t0
+    gbs = fp8_bytes(M, n_s, K) / dt / 1e9
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": nt, "kind": "oracle",
+            "sample": f"columns 0..{n_s - 1} of {N} (all {M} rows, full K={K}); {dt:.2f} s"}, p
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    import workloads as wl
+    M, N, K, cid = HEAD["M"], HEAD["N"], HEAD["K"], HEAD["config_id"]
+    p = wl.make_fp8_problem(M, N, K, config_id=cid)
+    nt = oracle.max_threads()
+    # each step: a column sample of the workload sized to ~1 s on these cores
+    cols = 512
+    t0 = time.perf_counter()
+    oracle.qgemm_fp8_block(p.X, p.W[:cols], p.S[:cols // 128], nthreads=nt)
+    dt = time.perf_counter() - t0
+    n_s = int(min(N, max(128, (1.0 / max(dt, 1e-6)) * cols)) // 128 * 128)
+    for _ in range(args.warmup):
+        oracle.qgemm_fp8_block(p.X, p.W[:n_s], p.S[:n_s // 128], nthreads=nt)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.qgemm_fp8_block(p.X, p.W[:n_s], p.S[:n_s // 128], nthreads=nt)
+    dt = time.perf_counter() - t0
+    per = dt / args.steps
+    gbs = fp8_bytes(M, n_s, K) / per / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(per * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "fp8_block gate/up M=16 N=17408 K=5120", "M": M, "N": N, "K": K,
+                   "sample_columns": n_s},
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": nt, "kind": "oracle",
+                         "sample": f"columns 0..{n_s - 1} of {N} per step (all {M} rows, full K)"},
+        "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--quick", action="store_true", help="headline only, no secondary configs or CPU baseline")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    from __graft_entry__ import build
+    if rank == 0:
+        build()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    import weight_only_quantized_qgemm_gb300 as qg
+
+    M, N, K, cid = HEAD["M"], HEAD["N"], HEAD["K"], HEAD["config_id"]
+    stream = torch.cuda.Stream()
+    sampler = ClockSampler(gpu_uuid(torch, local))
+
+    # headline: warm up, then the timed region with clocks sampled alongside
+    p, W, S, X, Y, ws, copies = fp8_case(torch, qg, M, N, K, cid)
+    wsbuf = ws.get(qg.workspace_bytes(qg.KIND_FP8_BLOCK, M, N, K))
+    ws_ptr = wsbuf.data_ptr() if wsbuf is not None else None
+    ws_n = wsbuf.numel() if wsbuf is not None else 0
+    lib = qg.lib
+    sptr = stream.cuda_stream
+    xp, yp, sp = X.data_ptr(), Y.data_ptr(), S.data_ptr()
+    wps = [w.data_ptr() for w in W]
+
+    def step(i):
+        r = lib.qgemm_fp8_block(xp, K, wps[i % copies], sp, yp, N, M, N, K, ws_ptr, ws_n, sptr)
+        if r:
+            raise RuntimeError(qg.status_string(r))
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            step(i)
+    torch.cuda.synchronize()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for i in range(args.steps):
+            step(i)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    ms_total = e0.elapsed_time(e1)
+    st = qg.last_device_status(stream)
+    if st:
+        raise RuntimeError(f"device status {qg.status_string(st)}")
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms_total], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+        dist.barrier()
+    ms = ms_total / args.steps
+    per_call_bytes = fp8_bytes(M, N, K)
+    value = per_call_bytes * world / (ms * 1e-3) / 1e9
+    achieved = per_call_bytes / (ms * 1e-3) / 1e9
+
+    e2e_ms, h2d, d2h = e2e_fp8(torch, qg, stream, (W, S, X, Y, ws), M, N, K,
+                               steps=max(200, min(args.steps, 5000)), warmup=args.warmup)
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return 0
+
+    peak, peak_kind = measured_peaks()
+    secondary = {}
+    cpu = None
+    if not args.quick:
+        sec_steps = 2000
+        try:
+            for m in (1, 8):
+                ms2, _, _, _ = bench_fp8(torch, qg, stream, m, N, K, cid, sec_steps, 50)
+                secondary[f"fp8_gateup_M{m}"] = {"us": round(ms2 * 1e3, 3),
+                                                 "GBps": round(fp8_bytes(m, N, K) / (ms2 * 1e-3) / 1e9, 1)}
+            for m in (16, 32):
+                ms2, _, _, _ = bench_fp8(torch, qg, stream, m, 5120, 17408, 2, sec_steps, 50)
+                secondary[f"fp8_down_M{m}"] = {"us": round(ms2 * 1e3, 3),
+                                               "GBps": round(fp8_bytes(m, 5120, 17408) / (ms2 * 1e-3) / 1e9, 1)}
+            for n in (1024, 5120, 6144):
+                for m in (1, 16, 32):
+                    ms2, _, _, _ = bench_fp8(torch, qg, stream, m, n, 5120, 3, sec_steps, 50)
+                    secondary[f"fp8_attn_N{n}_M{m}"] = {
+                        "us": round(ms2 * 1e3, 3), "GBps": round(fp8_bytes(m, n, 5120) / (ms2 * 1e-3) / 1e9, 1)}
+            ms2, _, _, _ = bench_fp8(torch, qg, stream, 1, 256, 512, 0, sec_steps, 50)
+            secondary["fp8_small_M1"] = {"us": round(ms2 * 1e3, 3)}
+            for m in (1, 16):
+                ms3, _ = bench_lut3(torch, qg, stream, m, 28672, 8192, sec_steps, 50)
+                secondary[f"lut3_M{m}"] = {"us": round(ms3 * 1e3, 3),
+                                           "GBps": round(lut3_bytes(m, 28672, 8192) / (ms3 * 1e-3) / 1e9, 1),
+                                           "frac": round(lut3_bytes(m, 28672, 8192) / (ms3 * 1e-3) / 1e9 / peak, 4)}
+        except Exception as e:  # secondary numbers must not hide the headline
+            secondary["error"] = repr(e)[:300]
+        cpu, _ = cpu_baseline(M, N, K, cid)
+
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 6),
+        "us_per_call": round(ms * 1e3, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": round(value / world / PAGE_BASELINE_GBPS, 3),
+        "vs_baseline_ref": "H100 w8a16_gemv_batch16 gate/up M=16, 342 GB/s (atlas m16_tc page, WHY table): context, other hardware",
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": "fp8_block gate/up M=16 N=17408 K=5120",
+                   "M": M, "N": N, "K": K, "weights": "E4M3 [N,K] + FP32 [128x128] block scales",
+                   "arith": "E4M3->BF16 exact dequant, BF16 x BF16 tcgen05 MMA, FP32 two-level fold, BF16 out",
+                   "l2": f"inputs larger than L2: {copies} rotating weight copies ({copies * N * K / 1e6:.0f} MB)",
+                   "parallelism": "replicas" if world > 1 else "1 GPU"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
+                     "bytes_per_launch": per_call_bytes,
+                     "traffic": profiled_traffic("fp8_gateup_m16", per_call_bytes)},
+        "e2e": {"value": round(per_call_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "us_per_step": round(e2e_ms * 1e3, 3)},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+        "secondary": secondary,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,147 @@
+"""Host-side checks of the C ABI (no GPU): the library loads, exports every
+function include/qgemm.h declares, validates arguments before touching the
+device, and packs 3-bit codes bit-exactly like the oracle's independent
+packer."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads as wl
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def qg():
+    from weight_only_quantized_qgemm_gb300 import _build
+    _build.build()
+    import weight_only_quantized_qgemm_gb300 as q
+    return q
+
+
+def _declared_functions():
+    names = []
+    for hdr in os.listdir(os.path.join(ROOT, "include")):
+        if not hdr.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", hdr)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"^[A-Za-z_][\w \*]*?\b(\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for must in ("qgemm_fp8_block", "qgemm_lut3", "pack_lut3", "qg_workspace_bytes",
+                 "qg_last_device_status", "qg_status_string"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(qg):
+    handle = ctypes.CDLL(qg.LIB_PATH)
+    for name in _declared_functions():
+        assert hasattr(handle, name), name
+
+
+def test_status_strings(qg):
+    for code in range(7):
+        assert qg.status_string(code) and qg.status_string(code) != "unknown status"
+    assert qg.status_string(99) == "unknown status"
+    assert qg.lib.qg_version().decode().count(".") == 2
+
+
+FAKE = 0x100000  # never dereferenced: every call below fails validation first
+
+
+@pytest.mark.parametrize("args,expect", [
+    # X, ldx, W, S, Y, ldy, M, N, K
+    ((FAKE, 512, FAKE, FAKE, FAKE, 256, 0, 256, 512), 0),        # M == 0: no-op
+    ((FAKE, 512, FAKE, FAKE, FAKE, 256, 4, 0, 512), 0),          # N == 0: no-op
+    ((None, 512, FAKE, FAKE, FAKE, 256, 4, 256, 512), 1),        # null X
+    ((FAKE, 512, None, FAKE, FAKE, 256, 4, 256, 512), 1),        # null W
+    ((FAKE, 512, FAKE, None, FAKE, 256, 4, 256, 512), 1),        # null scales
+    ((FAKE, 512, FAKE, FAKE, None, 256, 4, 256, 512), 1),        # null Y
+    ((FAKE, 512, FAKE, FAKE, FAKE, 256, -1, 256, 512), 1),       # negative M
+    ((FAKE, 512, FAKE, FAKE, FAKE, 256, 33, 256, 512), 2),       # M > 32
+    ((FAKE, 520, FAKE, FAKE, FAKE, 256, 4, 256, 520), 2),        # K % 16
+    ((FAKE, 256, FAKE, FAKE, FAKE, 256, 4, 256, 512), 1),        # ldx < K
+    ((FAKE, 512, FAKE, FAKE, FAKE, 100, 4, 256, 512), 1),        # ldy < N
+    ((FAKE + 8, 512, FAKE, FAKE, FAKE, 256, 4, 256, 512), 3),    # X not 16-byte aligned
+    ((FAKE, 512, FAKE + 4, FAKE, FAKE, 256, 4, 256, 512), 3),    # W not 16-byte aligned
+    ((FAKE, 516, FAKE, FAKE, FAKE, 256, 4, 256, 512), 3),        # ldx % 8
+])
+def test_fp8_argument_validation(qg, args, expect):
+    X, ldx, W, S, Y, ldy, M, N, K = args
+    assert qg.lib.qgemm_fp8_block(X, ldx, W, S, Y, ldy, M, N, K, None, 0, None) == expect
+
+
+@pytest.mark.parametrize("args,expect", [
+    # X, ldx, Wq, qmap, scales, Y, ldy, M, N, K
+    ((FAKE, 512, FAKE, FAKE, FAKE, FAKE, 256, 0, 256, 512), 0),
+    ((None, 512, FAKE, FAKE, FAKE, FAKE, 256, 4, 256, 512), 1),
+    ((FAKE, 512, FAKE, None, FAKE, FAKE, 256, 4, 256, 512), 1),
+    ((FAKE, 512, FAKE, FAKE, FAKE, FAKE, 256, 40, 256, 512), 2),
+    ((FAKE, 512, FAKE, FAKE, FAKE, FAKE, 256, 4, 256, 448), 2),   # K % 128
+    ((FAKE, 512, FAKE + 8, FAKE, FAKE, FAKE, 256, 4, 256, 512), 3),
+    ((FAKE, 512, FAKE, FAKE + 2, FAKE, FAKE, 256, 4, 256, 512), 3),
+])
+def test_lut3_argument_validation(qg, args, expect):
+    X, ldx, Wq, qm, sc, Y, ldy, M, N, K = args
+    assert qg.lib.qgemm_lut3(X, ldx, Wq, qm, sc, Y, ldy, M, N, K, None, 0, None) == expect
+
+
+def test_dequant_entry_validation(qg):
+    assert qg.lib.qg_dequant_e4m3_bf16(FAKE, FAKE, 0, None) == 0
+    assert qg.lib.qg_dequant_e4m3_bf16(None, FAKE, 4, None) == 1
+    assert qg.lib.qg_dequant_e4m3_bf16(FAKE, FAKE, -1, None) == 1
+    assert qg.lib.qg_dequant_lut3(FAKE, FAKE, FAKE, FAKE, 128, 200, None) == 2
+    assert qg.lib.qg_dequant_lut3(None, FAKE, FAKE, FAKE, 128, 256, None) == 1
+
+
+@pytest.mark.parametrize("N,K", [(128, 256), (256, 1024), (130, 384), (1, 128), (300, 640), (28672 // 64, 8192)])
+def test_pack_matches_oracle_packer(qg, N, K):
+    codes = wl.uniform_codes(1234 + N + K, N * K).reshape(N, K)
+    ours = qg.pack_lut3(codes)
+    ref = oracle.pack_lut3(codes)
+    assert ours.size == qg.lut3_packed_bytes(N, K) == ref.size == oracle.lut3_packed_bytes(N, K)
+    assert np.array_equal(ours, ref)
+    assert np.array_equal(qg.unpack_lut3(ours, N, K), codes)
+    assert np.array_equal(oracle.unpack_lut3(ours, N, K), codes)
+
+
+def test_pack_rejects_wide_codes(qg):
+    codes = np.zeros((128, 256), dtype=np.uint8)
+    codes[5, 17] = 8
+    with pytest.raises(qg.QgemmError) as e:
+        qg.pack_lut3(codes)
+    assert e.value.code == 1
+
+
+def _begin(c, U, G):
+    return c * U // G
+
+
+def _owner(x, U, G):
+    return ((x + 1) * G - 1) // U
+
+
+@pytest.mark.parametrize("U", [1, 7, 8, 40, 152, 153, 320, 5440, 7168, 14336, 99991])
+@pytest.mark.parametrize("G", [1, 2, 7, 148, 152])
+def test_stream_k_partition_rule(U, G):
+    """The kernels split U work units over G CTAs as [c*U/G, (c+1)*U/G) and find
+    a unit's owner as ((x+1)*G-1)/U; the two must agree for every unit."""
+    if G > U:
+        return
+    starts = [_begin(c, U, G) for c in range(G + 1)]
+    assert starts[0] == 0 and starts[-1] == U
+    sizes = np.diff(starts)
+    assert sizes.min() >= 1 and sizes.max() - sizes.min() <= 1
+    xs = np.unique(np.concatenate([np.arange(min(U, 3000)), np.array(starts[:-1]),
+                                   np.array(starts[1:]) - 1]))
+    for x in xs:
+        c = _owner(int(x), U, G)
+        assert starts[c] <= x < starts[c + 1]

@@ -1,0 +1,148 @@
+"""W8A16 FP8 block-scaled GEMM on the GPU against the CPU oracle, through the
+C ABI.  Every element must satisfy the comparison rule (<= 2 BF16 ULP, or
+within the near-zero floor); small shapes are compared in full, the full-size
+configurations in full as well (the oracle runs on all host cores)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+from gpu_util import Fp8Device, cached, grade_fp8, qg, sample_indices, to_bits
+
+pytestmark = pytest.mark.gpu
+
+
+def _problem(M, N, K, cid):
+    return cached(("fp8", M, N, K, cid), lambda: wl.make_fp8_problem(M, N, K, config_id=cid))
+
+
+def _check(p, Y, X_bits=None, ms=None, ns=None):
+    q = qg()
+    assert q.last_device_status() == 0
+    y = to_bits(Y)
+    ok, rep = grade_fp8(p, y, X_bits=X_bits, ms=ms, ns=ns)
+    assert rep.ok, rep
+    assert rep.max_rel_err <= 1e-2, rep
+    return y, rep
+
+
+def test_small_config():
+    """M=1, N=256, K=512 -- the smallest configuration."""
+    p = _problem(1, 256, 512, 0)
+    dev = Fp8Device(p)
+    _check(p, dev.run())
+
+
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 8, 15, 16, 17, 24, 31, 32])
+def test_m_sweep_attention_shape(M):
+    """N=1024, K=5120 (QKV K/V shape): 8 tiles x 40 blocks, split-K over the SMs."""
+    p = _problem(32, 1024, 5120, 3)
+    dev = cached(("fp8dev", 32, 1024, 5120), lambda: Fp8Device(p))
+    Xb = p.X[:M]
+    Y = dev.run(X_bits=Xb)
+    _check(p, Y[:M], X_bits=Xb)
+
+
+@pytest.mark.parametrize("N,K", [(200, 336), (130, 128), (1000, 2064), (128, 16), (77, 4096),
+                                 (256, 144), (3000, 1040)])
+@pytest.mark.parametrize("M", [1, 7, 20])
+def test_ragged_shapes(M, N, K):
+    """N not a multiple of 128 and K not a multiple of 128 (partial blocks)."""
+    p = _problem(M, N, K, 40)
+    _check(p, Fp8Device(p).run())
+
+
+@pytest.mark.parametrize("N", [5120, 6144])
+@pytest.mark.parametrize("M", [1, 5, 16, 32])
+def test_attention_shapes(M, N):
+    p = _problem(32, N, 5120, 3)
+    dev = cached(("fp8dev", 32, N, 5120), lambda: Fp8Device(p))
+    Xb = p.X[:M]
+    _check(p, dev.run(X_bits=Xb)[:M], X_bits=Xb)
+
+
+@pytest.mark.parametrize("M", [16, 8])
+def test_gateup_full(M):
+    """FFN gate/up, N=17408, K=5120 (89 MB of weights), every element."""
+    p = _problem(16, 17408, 5120, 1)
+    dev = cached(("fp8dev", 16, 17408, 5120), lambda: Fp8Device(p))
+    Xb = p.X[:M]
+    _check(p, dev.run(X_bits=Xb), X_bits=Xb)
+
+
+def test_down_full_and_halves():
+    """FFN down, N=5120, K=17408: M=16, M=32 in one call, and M=32 as two
+    contiguous 16-row halves (plain row offsets of X and Y)."""
+    q = qg()
+    p = _problem(32, 5120, 17408, 2)
+    dev = Fp8Device(p)
+    y16, _ = _check(p, dev.run(X_bits=p.X[:16]), X_bits=p.X[:16])
+    y32, _ = _check(p, dev.run())
+    # two halves through pointer offsets into one X / Y pair
+    Xd = torch.from_numpy(p.X.view(np.int16)).view(torch.bfloat16).cuda()
+    Y = torch.empty((32, 5120), dtype=torch.bfloat16, device="cuda")
+    q.qgemm_fp8_block(Xd[:16], dev.W[0], dev.S, Y=Y[:16])
+    q.qgemm_fp8_block(Xd[16:], dev.W[0], dev.S, Y=Y[16:])
+    yh, _ = _check(p, Y)
+    # the first half of the split is the M=16 call, bit for bit
+    assert np.array_equal(yh[:16], y16)
+
+
+def test_deterministic_and_workspace_left_clean():
+    """Same inputs, same bits (the split-K pieces are summed in a fixed order
+    whichever CTA finishes last); the arrival counters are back to zero."""
+    q = qg()
+    p = _problem(16, 5120, 5120, 3)
+    dev = Fp8Device(p)
+    ws = q.Workspace()
+    Xd = torch.from_numpy(p.X[:16].view(np.int16)).view(torch.bfloat16).cuda()
+    outs = []
+    for _ in range(3):
+        outs.append(to_bits(q.qgemm_fp8_block(Xd, dev.W[0], dev.S, workspace=ws)))
+    assert q.last_device_status() == 0
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
+    need = q.workspace_bytes(q.KIND_FP8_BLOCK, 16, 5120, 5120)
+    assert need > 0
+    T = -(-5120 // 128)
+    assert int(ws.buf[:T * 16].count_nonzero()) == 0
+
+
+def test_strided_rows_and_padding_untouched():
+    """ldx > K and ldy > N: padding columns of Y keep their canary."""
+    p = _problem(5, 1024, 5120, 3)
+    dev = Fp8Device(p)
+    Y = dev.run(x_pad=24, y_pad=40)
+    y, _ = _check(p, Y[:, :1024])
+    pad = to_bits(Y[:, 1024:])
+    assert np.all(pad == 0x7FC1)
+
+
+def test_k_zero_and_empty():
+    q = qg()
+    W = torch.zeros((256, 0), dtype=torch.uint8, device="cuda")
+    S = torch.zeros((2, 0), dtype=torch.float32, device="cuda")
+    X = torch.zeros((3, 8), dtype=torch.bfloat16, device="cuda")[:, :0]
+    Y = torch.full((3, 256), 5.0, dtype=torch.bfloat16, device="cuda")
+    assert q.lib.qgemm_fp8_block(X.data_ptr() or 16, 8, W.data_ptr() or 16, S.data_ptr() or 16,
+                                 Y.data_ptr(), 256, 3, 256, 0, None, 0, None) == 0
+    torch.cuda.synchronize()
+    assert float(Y.float().abs().max()) == 0.0
+    # M == 0 leaves Y alone
+    Y.fill_(5.0)
+    assert q.lib.qgemm_fp8_block(16, 8, 16, 16, Y.data_ptr(), 256, 0, 256, 128, None, 0, None) == 0
+    torch.cuda.synchronize()
+    assert float(Y.float().min()) == 5.0
+
+
+def test_extreme_scales_and_codes():
+    """All-448 codes, subnormal codes, zeros, negative zero and tiny/huge block
+    scales in one problem."""
+    M, N, K = 4, 256, 512
+    rng = np.random.default_rng(5)
+    W = rng.choice(np.array([0x7E, 0xFE, 0x01, 0x81, 0x07, 0x00, 0x80, 0x3C, 0xBC], dtype=np.uint8),
+                   size=(N, K))
+    S = np.array([[1e-30, 3e30, 1.0, 2.0 ** -20], [7.0, 1e-3, 4096.0, 0.5]], dtype=np.float32)
+    X = wl.bf16_bits_from_f32(rng.standard_normal((M, K)).astype(np.float32) * 8)
+    p = wl.Fp8Problem(M, N, K, X, W, S)
+    _check(p, Fp8Device(p).run())

@@ -1,0 +1,249 @@
+"""Python binding of libqgemm (weight-only quantized decode GEMMs for GB300).
+
+Argument marshalling only: every step of the GEMM runs in the library's CUDA
+kernels.  PyTorch provides device memory and the current stream.  If the
+compiled library is missing this module raises on import; there is no
+fallback implementation.
+
+The names follow the C ABI in ``include/qgemm.h``:
+
+* :func:`qgemm_fp8_block` -- W8A16 FP8 E4M3 weights with [128 x 128] FP32
+  block scales, BF16 activations and output, two-level FP32 fold.
+* :func:`qgemm_lut3` -- 3-bit learned-LUT weights (see :func:`pack_lut3`),
+  FP16 activations and output.
+* :func:`pack_lut3` / :func:`unpack_lut3` -- offline nibble packer (host).
+* :func:`dequant_e4m3_bf16` / :func:`dequant_lut3` -- the kernels' own
+  dequantisers, exposed for code-by-code checks.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+__all__ = [
+    "QgemmError", "LIB_PATH", "lib", "status_string", "workspace_bytes", "Workspace",
+    "qgemm_fp8_block", "qgemm_lut3", "pack_lut3", "unpack_lut3", "lut3_packed_bytes",
+    "dequant_e4m3_bf16", "dequant_lut3", "last_device_status", "set_wait_timeout_ns",
+    "set_fault_injection", "KIND_FP8_BLOCK", "KIND_LUT3", "STATUS",
+]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libqgemm.so")
+
+KIND_FP8_BLOCK = 0
+KIND_LUT3 = 1
+STATUS = {
+    0: "QG_OK", 1: "QG_ERR_INVALID_ARG", 2: "QG_ERR_UNSUPPORTED_SHAPE", 3: "QG_ERR_MISALIGNED",
+    4: "QG_ERR_CUDA", 5: "QG_ERR_TIMEOUT", 6: "QG_ERR_WORKSPACE",
+}
+
+
+class QgemmError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {STATUS.get(code, code)} ({status_string(code)})")
+
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"libqgemm.so not found at {LIB_PATH}; build it first with "
+        "`python -m weight_only_quantized_qgemm_gb300._build` (needs nvcc)")
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_L = ctypes.c_int64
+_S = ctypes.c_size_t
+
+lib = ctypes.CDLL(LIB_PATH)
+_SIGS = {
+    "qg_workspace_bytes": (_S, [_I, _I, _I, _I]),
+    "qgemm_fp8_block": (_I, [_P, _L, _P, _P, _P, _L, _I, _I, _I, _P, _S, _P]),
+    "qgemm_lut3": (_I, [_P, _L, _P, _P, _P, _P, _L, _I, _I, _I, _P, _S, _P]),
+    "qg_lut3_packed_bytes": (_S, [_I, _I]),
+    "pack_lut3": (_I, [_P, _P, _I, _I]),
+    "unpack_lut3": (_I, [_P, _P, _I, _I]),
+    "qg_dequant_e4m3_bf16": (_I, [_P, _P, _L, _P]),
+    "qg_dequant_lut3": (_I, [_P, _P, _P, _P, _I, _I, _P]),
+    "qg_last_device_status": (_I, [_P]),
+    "qg_set_wait_timeout_ns": (None, [ctypes.c_uint64]),
+    "qg_set_fault_injection": (None, [_I]),
+    "qg_status_string": (ctypes.c_char_p, [_I]),
+    "qg_version": (ctypes.c_char_p, []),
+}
+for _name, (_res, _args) in _SIGS.items():
+    _fn = getattr(lib, _name)
+    _fn.restype = _res
+    _fn.argtypes = _args
+
+
+def status_string(code: int) -> str:
+    return lib.qg_status_string(int(code)).decode()
+
+
+def _check(code: int, where: str) -> None:
+    if code != 0:
+        raise QgemmError(code, where)
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _stream_ptr(stream) -> int:
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def workspace_bytes(kind: int, M: int, N: int, K: int) -> int:
+    """Device workspace a call needs on the current device (may be 0)."""
+    return int(lib.qg_workspace_bytes(kind, M, N, K))
+
+
+class Workspace:
+    """A zero-filled device byte buffer that grows on demand.  Calls leave it
+    zero-filled again, so one buffer serves any sequence of calls on one
+    stream."""
+
+    def __init__(self, device=None):
+        self.device = device
+        self.buf = None
+
+    def get(self, nbytes: int):
+        torch = _torch()
+        if nbytes == 0:
+            return None
+        if self.buf is None or self.buf.numel() < nbytes:
+            self.buf = torch.zeros(max(nbytes, 1 << 20), dtype=torch.uint8,
+                                   device=self.device or torch.cuda.current_device())
+        return self.buf
+
+    def reset(self):
+        if self.buf is not None:
+            self.buf.zero_()
+
+
+_default_ws = {}
+
+
+def _workspace_for(kind, M, N, K, workspace, device):
+    need = workspace_bytes(kind, M, N, K)
+    if need == 0:
+        return None, 0
+    if workspace is None:
+        workspace = _default_ws.setdefault(device, Workspace(device))
+    buf = workspace.get(need) if isinstance(workspace, Workspace) else workspace
+    return buf.data_ptr(), buf.numel() * buf.element_size()
+
+
+def _ld(t) -> int:
+    if t.dim() != 2 or t.stride(1) != 1:
+        raise ValueError("expected a 2-D tensor with unit stride in its last dimension")
+    return t.stride(0)
+
+
+def qgemm_fp8_block(X, W, W_scale, Y=None, workspace=None, stream=None):
+    """Y[M, N] = X[M, K] . dequant(W)[N, K]^T (BF16 out).
+
+    X: bf16 CUDA [M, K] (row stride a multiple of 8); W: uint8 (E4M3 codes) or
+    float8_e4m3fn [N, K] contiguous; W_scale: float32 [ceil(N/128), ceil(K/128)]
+    contiguous.  Y (optional): bf16 [M, N] with unit column stride.
+    """
+    torch = _torch()
+    if X.dtype != torch.bfloat16:
+        raise TypeError("X must be bfloat16")
+    if W.dtype not in (torch.uint8, torch.float8_e4m3fn):
+        raise TypeError("W must hold E4M3 codes (uint8 or float8_e4m3fn)")
+    if W_scale.dtype != torch.float32 or not W_scale.is_contiguous() or not W.is_contiguous():
+        raise TypeError("W must be contiguous and W_scale contiguous float32")
+    M, K = X.shape
+    N = W.shape[0]
+    if W.shape[1] != K or tuple(W_scale.shape) != (-(-N // 128), -(-K // 128)):
+        raise ValueError("shape mismatch between X, W and W_scale")
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
+    ws, wsb = _workspace_for(KIND_FP8_BLOCK, M, N, K, workspace, X.device)
+    _check(lib.qgemm_fp8_block(X.data_ptr(), _ld(X), W.data_ptr(), W_scale.data_ptr(), Y.data_ptr(),
+                               _ld(Y), M, N, K, ws, wsb, _stream_ptr(stream)), "qgemm_fp8_block")
+    return Y
+
+
+def qgemm_lut3(X, Wq, qmap, scales, N: int, Y=None, workspace=None, stream=None):
+    """Y[M, N] = X[M, K] . dequant(Wq)^T with the 3-bit learned-LUT format (FP16 out).
+
+    X: fp16 CUDA [M, K]; Wq: the packed bytes from :func:`pack_lut3` on the
+    device; qmap: fp16 [8]; scales: fp16 [N, K/128] contiguous.
+    """
+    torch = _torch()
+    if X.dtype != torch.float16 or qmap.dtype != torch.float16 or scales.dtype != torch.float16:
+        raise TypeError("X, qmap and scales must be float16")
+    M, K = X.shape
+    if tuple(scales.shape) != (N, K // 128) or not scales.is_contiguous():
+        raise ValueError("scales must be a contiguous [N, K/128] tensor")
+    if Wq.numel() * Wq.element_size() < lut3_packed_bytes(N, K):
+        raise ValueError("packed weights are smaller than pack_lut3 produces for this shape")
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.float16, device=X.device)
+    ws, wsb = _workspace_for(KIND_LUT3, M, N, K, workspace, X.device)
+    _check(lib.qgemm_lut3(X.data_ptr(), _ld(X), Wq.data_ptr(), qmap.data_ptr(), scales.data_ptr(),
+                          Y.data_ptr(), _ld(Y), M, N, K, ws, wsb, _stream_ptr(stream)), "qgemm_lut3")
+    return Y
+
+
+def lut3_packed_bytes(N: int, K: int) -> int:
+    return int(lib.qg_lut3_packed_bytes(N, K))
+
+
+def pack_lut3(codes: np.ndarray) -> np.ndarray:
+    """Pack an [N, K] uint8 matrix of 3-bit codes (host) into the kernel layout."""
+    c = np.ascontiguousarray(codes, dtype=np.uint8)
+    N, K = c.shape
+    out = np.empty(lut3_packed_bytes(N, K), dtype=np.uint8)
+    _check(lib.pack_lut3(c.ctypes.data, out.ctypes.data, N, K), "pack_lut3")
+    return out
+
+
+def unpack_lut3(packed: np.ndarray, N: int, K: int) -> np.ndarray:
+    p = np.ascontiguousarray(packed, dtype=np.uint8)
+    if p.size < lut3_packed_bytes(N, K):
+        raise ValueError("packed buffer too small")
+    out = np.empty((N, K), dtype=np.uint8)
+    _check(lib.unpack_lut3(p.ctypes.data, out.ctypes.data, N, K), "unpack_lut3")
+    return out
+
+
+def dequant_e4m3_bf16(codes, out=None, stream=None):
+    """E4M3 codes (uint8 CUDA tensor) -> BF16, with the FP8 GEMM's own conversion."""
+    torch = _torch()
+    if out is None:
+        out = torch.empty(codes.shape, dtype=torch.bfloat16, device=codes.device)
+    _check(lib.qg_dequant_e4m3_bf16(codes.data_ptr(), out.data_ptr(), codes.numel(), _stream_ptr(stream)),
+           "qg_dequant_e4m3_bf16")
+    return out
+
+
+def dequant_lut3(Wq, qmap, scales, N: int, K: int, out=None, stream=None):
+    """Packed LUT3 weights -> FP16 [N, K], with the LUT3 GEMM's own dequantiser."""
+    torch = _torch()
+    if out is None:
+        out = torch.empty((N, K), dtype=torch.float16, device=Wq.device)
+    _check(lib.qg_dequant_lut3(Wq.data_ptr(), qmap.data_ptr(), scales.data_ptr(), out.data_ptr(), N, K,
+                               _stream_ptr(stream)), "qg_dequant_lut3")
+    return out
+
+
+def last_device_status(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the kernels' status code."""
+    return int(lib.qg_last_device_status(_stream_ptr(stream)))
+
+
+def set_wait_timeout_ns(ns: int) -> None:
+    lib.qg_set_wait_timeout_ns(int(ns))
+
+
+def set_fault_injection(unit: int) -> None:
+    lib.qg_set_fault_injection(int(unit))

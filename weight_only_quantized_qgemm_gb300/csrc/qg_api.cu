@@ -1,0 +1,411 @@
+// C ABI of libqgemm: argument validation, the per-shape dispatch table,
+// tensor-map encoding, the device status word, the code-by-code dequant
+// kernels and the offline LUT3 packer.  See include/qgemm.h for the contract.
+#include <atomic>
+#include <cstring>
+#include <mutex>
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "../../include/qgemm.h"
+#include "qg_device.cuh"
+#include "qg_internal.h"
+
+namespace qg {
+
+__device__ uint32_t g_status_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::atomic<uint64_t> g_timeout_ns{1000000000ull};
+std::atomic<int> g_fault_unit{-1};
+
+struct DeviceInfo {
+    std::once_flag once;
+    int sms = 0;
+    uint32_t* status = nullptr;
+    cudaError_t err = cudaSuccess;
+};
+DeviceInfo g_dev[kMaxDevices];
+
+// Per-device setup: SM count and the device address of the status word.
+DeviceInfo* device_info() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    DeviceInfo* d = &g_dev[dev];
+    std::call_once(d->once, [d, dev]() {
+        d->err = cudaDeviceGetAttribute(&d->sms, cudaDevAttrMultiProcessorCount, dev);
+        if (d->err == cudaSuccess)
+            d->err = cudaGetSymbolAddress(reinterpret_cast<void**>(&d->status), g_status_word);
+    });
+    return d->err == cudaSuccess ? d : nullptr;
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    std::call_once(once, []() {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// 2-D row-major tensor map: `rows` x `cols` elements, row stride `ld_bytes`,
+// box `box_cols` x `box_rows`, 128-byte swizzle, out-of-range reads as zero.
+bool make_tmap(CUtensorMap* m, const void* ptr, CUtensorMapDataType dt, uint64_t cols, uint64_t rows,
+               uint64_t ld_bytes, uint32_t box_cols, uint32_t box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {ld_bytes};
+    const cuuint32_t box[2] = {box_cols, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+LaunchCtl launch_ctl(const DeviceInfo* d) {
+    LaunchCtl c;
+    c.timeout_ns = g_timeout_ns.load();
+    c.fault_unit = g_fault_unit.load();
+    c.status = d->status;
+    c.num_sms = d->sms;
+    return c;
+}
+
+// ----------------------------------------------------------------- dispatch
+// Per-(kind, M, N, K) choice of MMA width and grid.  The MMA N side is 16 for
+// M <= 16 and 32 above (one weight pass for every M <= 32).  The grid is one
+// CTA per SM, or one per work unit when there are fewer units than SMs.
+Schedule choose_schedule(int kind, int M, int N, int K, int sms) {
+    Schedule s;
+    s.nmma = M <= 16 ? 16 : 32;
+    s.T = (N + 127) / 128;
+    s.KU = kind == QG_KIND_FP8_BLOCK ? (K + 127) / 128 : (K + 255) / 256;
+    s.U = static_cast<long long>(s.T) * s.KU;
+    s.G = static_cast<int>(s.U < sms ? s.U : sms);
+    if (s.G < 1) s.G = 1;
+    return s;
+}
+
+// True when some tile's units are spread over more than one CTA.
+bool schedule_splits(const Schedule& s) {
+    for (int c = 0; c <= s.G; ++c) {
+        const long long b = static_cast<long long>(c) * s.U / s.G;
+        if (b % s.KU != 0) return true;
+    }
+    return false;
+}
+
+}  // namespace
+
+size_t workspace_bytes(const Schedule& s) {
+    if (!schedule_splits(s)) return 0;
+    const size_t cnt = (static_cast<size_t>(s.T) * 4 * sizeof(uint32_t) + 255) & ~static_cast<size_t>(255);
+    return cnt + static_cast<size_t>(s.G) * 2 * s.nmma * 128 * sizeof(float);
+}
+
+uint32_t* device_status_ptr() {
+    DeviceInfo* d = device_info();
+    return d ? d->status : nullptr;
+}
+
+// ----------------------------------------------------------------- small kernels
+namespace {
+
+__global__ void dequant_e4m3_kernel(const uint8_t* __restrict__ codes, uint32_t* __restrict__ out, int64_t n) {
+    const int64_t nq = (n + 3) / 4;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < nq;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        uint32_t r = 0;
+        for (int b = 0; b < 4; ++b)
+            if (4 * i + b < n) r |= static_cast<uint32_t>(codes[4 * i + b]) << (8 * b);
+        uint32_t lo, hi;
+        e4m3x4_to_bf16(r, lo, hi);
+        const uint32_t v[4] = {lo & 0xFFFFu, lo >> 16, hi & 0xFFFFu, hi >> 16};
+        uint16_t* o = reinterpret_cast<uint16_t*>(out);
+        for (int b = 0; b < 4; ++b)
+            if (4 * i + b < n) o[4 * i + b] = static_cast<uint16_t>(v[b]);
+    }
+}
+
+// One thread per (row, 8-code word) of the packed LUT3 layout.
+__global__ void dequant_lut3_kernel(const uint8_t* __restrict__ Wq, const uint4* __restrict__ qmap,
+                                    const uint16_t* __restrict__ scales, uint16_t* __restrict__ D, int N, int K) {
+    const int KT = (K + 255) / 256;
+    const int words_per_row = KT * 32;
+    const int64_t total = static_cast<int64_t>(N) * words_per_row;
+    const uint4 qm = __ldg(qmap);
+    const int G128 = K / 128;
+    for (int64_t t = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; t < total;
+         t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int n = static_cast<int>(t / words_per_row);
+        const int wi = static_cast<int>(t % words_per_row);
+        const int k0 = wi * 8;
+        const int tk = k0 / 256, qq = (k0 % 256) / 32, w = (k0 % 32) / 8;
+        const size_t off = (static_cast<size_t>(n / 128) * KT + tk) * 16384 +
+                           (static_cast<size_t>(qq) * 128 + (n % 128)) * 16 + w * 4;
+        const uint32_t word = *reinterpret_cast<const uint32_t*>(Wq + off);
+        const int g = k0 / 128;
+        const uint32_t sc = g < G128 ? scales[static_cast<int64_t>(n) * G128 + g] : 0u;
+        const uint32_t sc2 = sc | (sc << 16);
+        const LutPlanes tp = lut_planes(f16x2_mul(qm.x, sc2), f16x2_mul(qm.y, sc2), f16x2_mul(qm.z, sc2),
+                                        f16x2_mul(qm.w, sc2));
+        uint32_t o[4];
+        lut3x8_to_f16(word, tp, o);
+        for (int e = 0; e < 8; ++e) {
+            if (k0 + e < K) {
+                const uint32_t pair = o[e >> 1];
+                D[static_cast<int64_t>(n) * K + k0 + e] = static_cast<uint16_t>((e & 1) ? (pair >> 16) : (pair & 0xFFFFu));
+            }
+        }
+    }
+}
+
+__global__ void zero_rows_kernel(uint16_t* Y, int64_t ldy, int M, int N) {
+    const int64_t total = static_cast<int64_t>(M) * N;
+    for (int64_t t = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; t < total;
+         t += static_cast<int64_t>(gridDim.x) * blockDim.x)
+        Y[(t / N) * ldy + (t % N)] = 0;
+}
+
+int grid_for(int64_t work, int threads) {
+    int64_t g = (work + threads - 1) / threads;
+    if (g > 4096) g = 4096;
+    if (g < 1) g = 1;
+    return static_cast<int>(g);
+}
+
+}  // namespace
+
+cudaError_t launch_dequant_e4m3(const uint8_t* codes, void* out, int64_t n, cudaStream_t st) {
+    dequant_e4m3_kernel<<<grid_for((n + 3) / 4, 256), 256, 0, st>>>(codes, static_cast<uint32_t*>(out), n);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dequant_lut3(const void* Wq, const void* qmap, const void* scales, void* D, int N, int K,
+                                cudaStream_t st) {
+    const int64_t work = static_cast<int64_t>(N) * ((K + 255) / 256) * 32;
+    dequant_lut3_kernel<<<grid_for(work, 256), 256, 0, st>>>(static_cast<const uint8_t*>(Wq),
+                                                             static_cast<const uint4*>(qmap),
+                                                             static_cast<const uint16_t*>(scales),
+                                                             static_cast<uint16_t*>(D), N, K);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_zero_rows(void* Y, int64_t ldy, int M, int N, cudaStream_t st) {
+    zero_rows_kernel<<<grid_for(static_cast<int64_t>(M) * N, 256), 256, 0, st>>>(static_cast<uint16_t*>(Y), ldy,
+                                                                               M, N);
+    return cudaGetLastError();
+}
+
+}  // namespace qg
+
+// =================================================================== C ABI
+using namespace qg;
+
+extern "C" {
+
+size_t qg_workspace_bytes(int kind, int M, int N, int K) {
+    if (M < 1 || N < 1 || K < 1 || M > 32) return 0;
+    if (kind != QG_KIND_FP8_BLOCK && kind != QG_KIND_LUT3) return 0;
+    DeviceInfo* d = device_info();
+    if (!d) return 0;
+    return workspace_bytes(choose_schedule(kind, M, N, K, d->sms));
+}
+
+qg_status qgemm_fp8_block(const void* X, int64_t ldx, const uint8_t* W, const float* W_scale, void* Y, int64_t ldy,
+                          int M, int N, int K, void* workspace, size_t workspace_bytes_, cudaStream_t stream) {
+    if (M < 0 || N < 0 || K < 0) return QG_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return QG_OK;
+    if (!X || !W || !W_scale || !Y) return QG_ERR_INVALID_ARG;
+    if (M > 32 || K % 16 != 0) return QG_ERR_UNSUPPORTED_SHAPE;
+    if (ldx < K || ldy < N) return QG_ERR_INVALID_ARG;
+    if (!aligned16(X) || !aligned16(W) || (ldx % 8) != 0) return QG_ERR_MISALIGNED;
+    if ((reinterpret_cast<uintptr_t>(W_scale) & 3u) != 0 || (reinterpret_cast<uintptr_t>(Y) & 1u) != 0)
+        return QG_ERR_MISALIGNED;
+    DeviceInfo* d = device_info();
+    if (!d) return QG_ERR_CUDA;
+    if (K == 0) return launch_zero_rows(Y, ldy, M, N, stream) == cudaSuccess ? QG_OK : QG_ERR_CUDA;
+    const Schedule s = choose_schedule(QG_KIND_FP8_BLOCK, M, N, K, d->sms);
+    const size_t need = workspace_bytes(s);
+    if (need > 0 && (!workspace || workspace_bytes_ < need || (reinterpret_cast<uintptr_t>(workspace) & 255u)))
+        return QG_ERR_WORKSPACE;
+    CUtensorMap tmW, tmX;
+    if (!make_tmap(&tmW, W, CU_TENSOR_MAP_DATA_TYPE_UINT8, static_cast<uint64_t>(K), static_cast<uint64_t>(N),
+                   static_cast<uint64_t>(K), 128, 128))
+        return QG_ERR_CUDA;
+    if (!make_tmap(&tmX, X, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<uint64_t>(K), static_cast<uint64_t>(M),
+                   static_cast<uint64_t>(ldx) * 2, 64, static_cast<uint32_t>(s.nmma)))
+        return QG_ERR_CUDA;
+    Fp8Args a;
+    a.X = X;
+    a.ldx = ldx;
+    a.W = W;
+    a.S = W_scale;
+    a.lds = (K + 127) / 128;
+    a.Y = Y;
+    a.ldy = ldy;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.ws = need > 0 ? workspace : nullptr;
+    return launch_fp8(a, s, tmW, tmX, launch_ctl(d), stream) == cudaSuccess ? QG_OK : QG_ERR_CUDA;
+}
+
+qg_status qgemm_lut3(const void* X, int64_t ldx, const void* Wq, const void* qmap, const void* scales, void* Y,
+                     int64_t ldy, int M, int N, int K, void* workspace, size_t workspace_bytes_,
+                     cudaStream_t stream) {
+    if (M < 0 || N < 0 || K < 0) return QG_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return QG_OK;
+    if (!X || !Wq || !qmap || !scales || !Y) return QG_ERR_INVALID_ARG;
+    if (M > 32 || K % 128 != 0) return QG_ERR_UNSUPPORTED_SHAPE;
+    if (ldx < K || ldy < N) return QG_ERR_INVALID_ARG;
+    if (!aligned16(X) || !aligned16(Wq) || !aligned16(qmap) || (ldx % 8) != 0) return QG_ERR_MISALIGNED;
+    if ((reinterpret_cast<uintptr_t>(scales) & 1u) != 0 || (reinterpret_cast<uintptr_t>(Y) & 1u) != 0)
+        return QG_ERR_MISALIGNED;
+    DeviceInfo* d = device_info();
+    if (!d) return QG_ERR_CUDA;
+    if (K == 0) return launch_zero_rows(Y, ldy, M, N, stream) == cudaSuccess ? QG_OK : QG_ERR_CUDA;
+    const Schedule s = choose_schedule(QG_KIND_LUT3, M, N, K, d->sms);
+    const size_t need = workspace_bytes(s);
+    if (need > 0 && (!workspace || workspace_bytes_ < need || (reinterpret_cast<uintptr_t>(workspace) & 255u)))
+        return QG_ERR_WORKSPACE;
+    CUtensorMap tmX;
+    if (!make_tmap(&tmX, X, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, static_cast<uint64_t>(K), static_cast<uint64_t>(M),
+                   static_cast<uint64_t>(ldx) * 2, 64, static_cast<uint32_t>(s.nmma)))
+        return QG_ERR_CUDA;
+    Lut3Args a;
+    a.X = X;
+    a.ldx = ldx;
+    a.Wq = Wq;
+    a.qmap = qmap;
+    a.scales = scales;
+    a.ldsc = K / 128;
+    a.Y = Y;
+    a.ldy = ldy;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.ws = need > 0 ? workspace : nullptr;
+    return launch_lut3(a, s, tmX, launch_ctl(d), stream) == cudaSuccess ? QG_OK : QG_ERR_CUDA;
+}
+
+size_t qg_lut3_packed_bytes(int N, int K) {
+    if (N < 0 || K < 0) return 0;
+    return static_cast<size_t>((N + 127) / 128) * static_cast<size_t>((K + 255) / 256) * 16384u;
+}
+
+qg_status pack_lut3(const uint8_t* codes, void* packed, int N, int K) {
+    if (N < 0 || K < 0) return QG_ERR_INVALID_ARG;
+    if (N == 0 || K == 0) return QG_OK;
+    if (!codes || !packed) return QG_ERR_INVALID_ARG;
+    const int KT = (K + 255) / 256;
+    const size_t bytes = qg_lut3_packed_bytes(N, K);
+    uint8_t* out = static_cast<uint8_t*>(packed);
+    std::memset(out, 0, bytes);
+    for (int n = 0; n < N; ++n) {
+        const uint8_t* crow = codes + static_cast<size_t>(n) * K;
+        const size_t tile_row = static_cast<size_t>(n / 128) * KT;
+        const int r = n % 128;
+        for (int k = 0; k < K; k += 8) {
+            uint32_t word = 0;
+            for (int i = 0; i < 8 && k + i < K; ++i) {
+                const uint8_t c = crow[k + i];
+                if (c > 7) return QG_ERR_INVALID_ARG;
+                word |= static_cast<uint32_t>(c) << (4 * i);
+            }
+            const int tk = k / 256, q = (k % 256) / 32, w = (k % 32) / 8;
+            const size_t off = (tile_row + tk) * 16384 + (static_cast<size_t>(q) * 128 + r) * 16 + w * 4;
+            out[off + 0] = static_cast<uint8_t>(word);
+            out[off + 1] = static_cast<uint8_t>(word >> 8);
+            out[off + 2] = static_cast<uint8_t>(word >> 16);
+            out[off + 3] = static_cast<uint8_t>(word >> 24);
+        }
+    }
+    return QG_OK;
+}
+
+qg_status unpack_lut3(const void* packed, uint8_t* codes, int N, int K) {
+    if (N < 0 || K < 0) return QG_ERR_INVALID_ARG;
+    if (N == 0 || K == 0) return QG_OK;
+    if (!codes || !packed) return QG_ERR_INVALID_ARG;
+    const int KT = (K + 255) / 256;
+    const uint8_t* in = static_cast<const uint8_t*>(packed);
+    for (int n = 0; n < N; ++n) {
+        const size_t tile_row = static_cast<size_t>(n / 128) * KT;
+        const int r = n % 128;
+        for (int k = 0; k < K; ++k) {
+            const int tk = k / 256, q = (k % 256) / 32, w = (k % 32) / 8, i = k % 8;
+            const size_t off = (tile_row + tk) * 16384 + (static_cast<size_t>(q) * 128 + r) * 16 + w * 4 + i / 2;
+            codes[static_cast<size_t>(n) * K + k] = static_cast<uint8_t>((in[off] >> (4 * (i % 2))) & 15u);
+        }
+    }
+    return QG_OK;
+}
+
+qg_status qg_dequant_e4m3_bf16(const uint8_t* codes, void* out_bf16, int64_t n, cudaStream_t stream) {
+    if (n < 0) return QG_ERR_INVALID_ARG;
+    if (n == 0) return QG_OK;
+    if (!codes || !out_bf16) return QG_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(out_bf16) & 1u) != 0) return QG_ERR_MISALIGNED;
+    return launch_dequant_e4m3(codes, out_bf16, n, stream) == cudaSuccess ? QG_OK : QG_ERR_CUDA;
+}
+
+qg_status qg_dequant_lut3(const void* Wq, const void* qmap, const void* scales, void* D, int N, int K,
+                          cudaStream_t stream) {
+    if (N < 0 || K < 0) return QG_ERR_INVALID_ARG;
+    if (N == 0 || K == 0) return QG_OK;
+    if (!Wq || !qmap || !scales || !D) return QG_ERR_INVALID_ARG;
+    if (K % 128 != 0) return QG_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned16(Wq) || !aligned16(qmap) || (reinterpret_cast<uintptr_t>(scales) & 1u) ||
+        (reinterpret_cast<uintptr_t>(D) & 1u))
+        return QG_ERR_MISALIGNED;
+    return launch_dequant_lut3(Wq, qmap, scales, D, N, K, stream) == cudaSuccess ? QG_OK : QG_ERR_CUDA;
+}
+
+qg_status qg_last_device_status(cudaStream_t stream) {
+    DeviceInfo* d = device_info();
+    if (!d) return QG_ERR_CUDA;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return QG_ERR_CUDA;
+    uint32_t word = 0;
+    if (cudaMemcpy(&word, d->status, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return QG_ERR_CUDA;
+    if (word != 0 && cudaMemset(d->status, 0, sizeof(word)) != cudaSuccess) return QG_ERR_CUDA;
+    if (word & kDevTimeout) return QG_ERR_TIMEOUT;
+    return word ? QG_ERR_CUDA : QG_OK;
+}
+
+void qg_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns < 1000 ? 1000 : ns); }
+
+void qg_set_fault_injection(int unit) { g_fault_unit.store(unit < 0 ? -1 : unit); }
+
+const char* qg_status_string(qg_status s) {
+    switch (s) {
+        case QG_OK: return "ok";
+        case QG_ERR_INVALID_ARG: return "invalid argument";
+        case QG_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+        case QG_ERR_MISALIGNED: return "misaligned pointer or stride";
+        case QG_ERR_CUDA: return "CUDA error";
+        case QG_ERR_TIMEOUT: return "in-kernel wait timed out";
+        case QG_ERR_WORKSPACE: return "workspace missing or too small";
+    }
+    return "unknown status";
+}
+
+const char* qg_version(void) { return "0.1.0"; }
+
+}  // extern "C"

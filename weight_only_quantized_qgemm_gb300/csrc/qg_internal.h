@@ -1,0 +1,72 @@
+// Internal interface between the C ABI (qg_api.cu) and the kernel translation
+// units.  Not installed; not part of the public header.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace qg {
+
+// Work decomposition shared by both GEMM kernels.  The output is cut into
+// T tiles of 128 weight rows; each tile's K range into KU units.  The
+// T * KU units, tile-major, are split evenly over G CTAs (CTA c owns units
+// [c*U/G, (c+1)*U/G)).  A tile whose units are spread over several CTAs is
+// finished by the last of them to arrive (split-K / stream-K).
+struct Schedule {
+    int T = 0;        // tiles
+    int KU = 0;       // units per tile
+    long long U = 0;  // T * KU
+    int G = 0;        // CTAs
+    int nmma = 16;    // MMA N (16 or 32)
+};
+
+// Workspace layout for a schedule: per-tile counters, then per-CTA partials.
+size_t workspace_bytes(const Schedule& s);
+
+struct Fp8Args {
+    const void* X;
+    int64_t ldx;
+    const uint8_t* W;
+    const float* S;
+    int64_t lds;
+    void* Y;
+    int64_t ldy;
+    int M, N, K;
+    void* ws;
+};
+
+struct Lut3Args {
+    const void* X;
+    int64_t ldx;
+    const void* Wq;
+    const void* qmap;
+    const void* scales;
+    int64_t ldsc;
+    void* Y;
+    int64_t ldy;
+    int M, N, K;
+    void* ws;
+};
+
+struct LaunchCtl {
+    uint64_t timeout_ns;
+    int fault_unit;
+    uint32_t* status;    // device status word
+    int num_sms;
+};
+
+cudaError_t launch_fp8(const Fp8Args& a, const Schedule& s, const CUtensorMap& tmW,
+                       const CUtensorMap& tmX, const LaunchCtl& c, cudaStream_t st);
+cudaError_t launch_lut3(const Lut3Args& a, const Schedule& s, const CUtensorMap& tmX,
+                        const LaunchCtl& c, cudaStream_t st);
+
+cudaError_t launch_dequant_e4m3(const uint8_t* codes, void* out, int64_t n, cudaStream_t st);
+cudaError_t launch_dequant_lut3(const void* Wq, const void* qmap, const void* scales, void* D,
+                                int N, int K, cudaStream_t st);
+cudaError_t launch_zero_rows(void* Y, int64_t ldy, int M, int N, cudaStream_t st);
+
+uint32_t* device_status_ptr();
+
+}  // namespace qg
