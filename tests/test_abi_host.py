@@ -17,8 +17,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 @pytest.fixture(scope="module")
 def qg():
-    from weight_only_quantized_qgemm_gb300 import _build
-    _build.build()
+    import __graft_entry__
+    __graft_entry__.build_library()
     import weight_only_quantized_qgemm_gb300 as q
     return q
 

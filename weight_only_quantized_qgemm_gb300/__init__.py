@@ -49,7 +49,7 @@ class QgemmError(RuntimeError):
 if not os.path.exists(LIB_PATH):
     raise ImportError(
         f"libqgemm.so not found at {LIB_PATH}; build it first with "
-        "`python -m weight_only_quantized_qgemm_gb300._build` (needs nvcc)")
+        "`python -c 'import __graft_entry__ as g; g.build()'` from the repository root (needs nvcc)")
 
 _P = ctypes.c_void_p
 _I = ctypes.c_int

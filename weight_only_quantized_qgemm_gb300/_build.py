@@ -71,6 +71,6 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
     return LIB
 
 
-if __name__ == "__main__":
+if __name__ == "__main__":  # python weight_only_quantized_qgemm_gb300/_build.py [--force]
     build(force="--force" in sys.argv, verbose=True, ptxas_info="--ptxas-info" in sys.argv)
     print(LIB)
