@@ -15,7 +15,7 @@ def _timeout_then_recover(run, grade, ws):
     q = qg()
     assert q.last_device_status() == 0
     q.set_wait_timeout_ns(20_000_000)      # 20 ms
-    q.set_fault_injection(1)               # CTA 0 never loads its second unit
+    q.set_fault_injection(0)               # CTA 0 never loads its first unit
     try:
         run(ws)
         assert q.last_device_status() == 5  # QG_ERR_TIMEOUT

@@ -264,13 +264,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (m >= p.M) break;
                         float acc = 0.0f;
                         for (int c2 = cf; c2 <= cl; ++c2) {
-                            float part;
-                            if (c2 == cta) {
-                                part = outer[m];
-                            } else {
-                                const int w2 = (tile == static_cast<int>(unit_begin(c2, p.U, p.G) / p.KB)) ? 0 : 1;
-                                part = __ldcg(p.part + ((static_cast<size_t>(c2) * 2 + w2) * NMMA + m) * 128 + row);
-                            }
+                            const int w2 = (tile == static_cast<int>(unit_begin(c2, p.U, p.G) / p.KB)) ? 0 : 1;
+                            float* slot = p.part + ((static_cast<size_t>(c2) * 2 + w2) * NMMA + m) * 128 + row;
+                            const float part = (c2 == cta) ? outer[m] : __ldcg(slot);
+                            __stcg(slot, 0.0f);   // every call leaves the workspace zero-filled
                             acc = __fadd_rn(acc, part);
                         }
                         if (n < p.N) p.Y[static_cast<int64_t>(m) * p.ldy + n] = __float2bfloat16_rn(acc);
