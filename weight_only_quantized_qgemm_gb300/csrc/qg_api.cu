@@ -95,7 +95,7 @@ Schedule choose_schedule(int kind, int M, int N, int K, int sms) {
     Schedule s;
     s.nmma = M <= 16 ? 16 : 32;
     s.T = (N + 127) / 128;
-    s.KU = kind == QG_KIND_FP8_BLOCK ? (K + 127) / 128 : (K + 255) / 256;
+    s.KU = (K + 127) / 128;   // one unit = 128 rows x one 128-wide K block
     s.U = static_cast<long long>(s.T) * s.KU;
     s.G = static_cast<int>(s.U < sms ? s.U : sms);
     if (s.G < 1) s.G = 1;

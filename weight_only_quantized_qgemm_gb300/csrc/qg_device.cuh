@@ -231,13 +231,6 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     return d;
 }
 
-// f = c ? (b & ~a) : a
-__device__ __forceinline__ uint32_t lop3_sel_sign(uint32_t a, uint32_t b, uint32_t c) {
-    uint32_t d;
-    asm("lop3.b32 %0, %1, %2, %3, 0x58;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-    return d;
-}
-
 __device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
     uint32_t d;
     asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
@@ -252,19 +245,23 @@ __device__ __forceinline__ uint32_t f16x2_mul(uint32_t a, uint32_t b) {
 
 // Four E4M3 codes r = [c3 c2 c1 c0] (c0 = lowest K) -> lo = BF16x2 {c0, c1},
 // hi = BF16x2 {c2, c3}; exact for every finite code, subnormals included.
-// Each code's 7 magnitude bits are placed under the BF16 exponent/mantissa
-// boundary (value 2^-120 times the E4M3 value, a BF16 subnormal when the
-// E4M3 exponent field is 0), the sign is moved to bit 15 with a byte-permute
-// that replicates it, and one BF16 multiply by 2^120 restores the scale.
+// A byte permute builds, per output pair, [c1 | sgn(c0) x 8 | c0 | 0]; an
+// arithmetic shift right by 4 then leaves each code's 7 magnitude bits under
+// the BF16 exponent/mantissa boundary with its sign replicated above them, and
+// a mask keeps the sign bit and the magnitude.  The result is 2^-120 times the
+// E4M3 value (a BF16 subnormal when the E4M3 exponent field is 0); one BF16
+// multiply by 2^120 restores the scale exactly.
+__device__ __forceinline__ uint32_t shr_s32(uint32_t v, int n) {
+    return static_cast<uint32_t>(static_cast<int32_t>(v) >> n);
+}
+
 __device__ __forceinline__ void e4m3x4_to_bf16(uint32_t r, uint32_t& lo, uint32_t& hi) {
     constexpr uint32_t kTwo120 = 0x7B807B80u;  // BF16x2 {2^120, 2^120}
-    constexpr uint32_t kSignPos = 0x88008800u; // bits 11 and 15 of each half
-    const uint32_t m0 = prmt(r, 0u, 0x4140u) << 4;   // [0 c1 0 c0] << 4
-    const uint32_t s0 = prmt(r, 0u, 0x9484u);        // [sgn(c1) 0 sgn(c0) 0]
-    const uint32_t m1 = prmt(r, 0u, 0x4342u) << 4;   // [0 c3 0 c2] << 4
-    const uint32_t s1 = prmt(r, 0u, 0xB4A4u);        // [sgn(c3) 0 sgn(c2) 0]
-    lo = bf16x2_mul(lop3_sel_sign(m0, s0, kSignPos), kTwo120);
-    hi = bf16x2_mul(lop3_sel_sign(m1, s1, kSignPos), kTwo120);
+    constexpr uint32_t kKeep = 0x87F087F0u;    // sign + 7 magnitude bits per half
+    const uint32_t p0 = prmt(r, 0u, 0x1804u);  // [c1 | sgn(c0) | c0 | 0]
+    const uint32_t p1 = prmt(r, 0u, 0x3A24u);  // [c3 | sgn(c2) | c2 | 0]
+    lo = bf16x2_mul(shr_s32(p0, 4) & kKeep, kTwo120);
+    hi = bf16x2_mul(shr_s32(p1, 4) & kKeep, kTwo120);
 }
 
 // Byte planes of an 8-entry FP16 table e[0..7] given as four FP16x2 words

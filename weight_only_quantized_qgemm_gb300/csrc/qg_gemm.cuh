@@ -1,0 +1,487 @@
+// The weight-only decode GEMM pipeline for sm_103a, shared by both weight
+// formats (a format supplies the weight copy, the register dequantiser and
+// the per-block scale of the fold).
+//
+//   Y[m, n] = out( sum_kb  fold_scale(n, kb) * ( sum_{k in kb} x[m,k] * deq(W)[n,k] ) )
+//
+// Swap-AB: a 128-row slice of W is the MMA's M side (TMEM lanes), the M <= 32
+// activation rows are the MMA's narrow N side (16 or 32).  A work unit is one
+// 128-row tile x one 128-wide K block; its MMAs accumulate into a TMEM
+// accumulator of its own, which the fold warps multiply by the block scale
+// and add into FP32 registers (the two-level fold of the FP8 format; the LUT
+// format's scale is inside the weights and its fold scale is 1).
+//
+// One persistent CTA per SM, 512 threads (16 warps; registers are granted in
+// 4-warp steps, so a 17th warp would cut every thread to 96 registers):
+//   warp 0        weight producer: one copy per unit (evict-first L2 hint) into
+//                 a deep ring.  A weight stage is released as soon as the
+//                 dequant warps hold it in registers, so nearly the whole ring
+//                 (up to ~176 KB per SM) is in flight against HBM latency.
+//   warp 15       X producer: the unit's 128-wide X slice (two 64-element TMA
+//                 boxes, 128-byte swizzle) into a smaller ring; a slice is held
+//                 until the unit's MMAs complete.
+//   warps 1,14    MMA issuers, unit i taken by issuer i % 2: 8 tcgen05.mma
+//                 kind::f16 (M=128, N=16|32, K=16), A from TMEM, B (X) from
+//                 shared memory, then one tcgen05.commit.  A single thread
+//                 gets an MMA accepted only every ~55-120 cycles, while the
+//                 tensor core takes one every ~30 at this shape, so two issuers
+//                 keep it ahead of the memory stream.
+//   warps 2-5     fold / epilogue, one per TMEM lane quadrant.
+//   warps 6-13    dequant, two groups of four warps taking alternate units:
+//                 shared memory -> registers -> exact BF16/FP16 -> tcgen05.st
+//                 into a 4-deep A ring in TMEM.
+// The per-unit commit (accumulator ready) also frees the unit's A buffer and,
+// through the dequant group that next reuses that buffer, its X slice.
+//
+// Work units are split evenly over the CTAs in tile-major order (stream-K);
+// a tile shared by several CTAs is summed, in ascending K order of its
+// pieces, by whichever CTA finishes its piece last (an atomic arrival
+// counter; nobody spins on another CTA).  Every wait is bounded: a wait that
+// runs out records a timeout in the status word, the CTA drains its own
+// copies and MMAs, frees its TMEM and returns.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "qg_device.cuh"
+#include "qg_internal.h"
+
+namespace qg {
+namespace gemm {
+
+constexpr int kThreads = 512;
+constexpr int kWarpFold0 = 2;
+constexpr int kWarpDeq0 = 6;
+constexpr int kWarpMma2 = 14;
+constexpr int kWarpXProd = 15;
+constexpr int kIssuers = 2;
+constexpr int kNA = 4;            // A buffers in TMEM (64 columns each) = accumulators
+constexpr int kTmemCols = 512;
+constexpr int kDCol0 = kNA * 64;  // accumulators at columns 256 + 32 a
+
+struct Params {
+    // weights
+    const uint8_t* Wq;            // packed LUT3 weights (bulk copies)
+    const uint4* qmap;            // LUT3 map
+    const uint16_t* lut_scales;   // LUT3 per-(row, group) FP16 scales
+    int64_t ld_lut_scales;
+    int KT;                       // LUT3: 256-wide packed blocks per tile row
+    const float* S;               // FP8 block scales
+    int64_t lds;
+    // output and shape
+    void* Y;
+    int64_t ldy;
+    int M, N, K;
+    int KB;                       // units (128-wide K blocks) per tile
+    long long U;                  // total units
+    int G;                        // CTAs
+    uint32_t* cnt;                // per (tile, quadrant) arrival counters
+    float* part;                  // [G][2][128][NMMA] partial sums
+    uint64_t timeout_ns;
+    int fault_unit;
+    uint32_t* status;
+};
+
+template <int NMMA, int WBYTES>
+struct Layout {
+    static constexpr int kXSlot = NMMA * 256;             // two 64-element X boxes
+    static constexpr int kXBox = NMMA * 128;
+    static constexpr int kXStages = 8;
+    static constexpr int kWBudget = 212992 - kXStages * kXSlot;   // 208 KB in all
+    static constexpr int kWStages = (kWBudget / WBYTES) < 24 ? (kWBudget / WBYTES) : 24;
+    static constexpr int kXOff = kWStages * WBYTES;
+    static constexpr int kBarOff = kXOff + kXStages * kXSlot;
+    static constexpr int kNumBars = 2 * kWStages + 2 * kXStages + 3 * kNA;
+    static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+    static constexpr int kSmemBytes = kMiscOff + 64 + 1024;  // + alignment slack
+    static_assert(WBYTES % 1024 == 0 && kXSlot % 1024 == 0, "keep the 1024-byte swizzle alignment");
+    static_assert(kXStages >= 2 * kNA, "X slices are held until the unit kNA later is dequantised");
+    static_assert(kWStages >= 8, "the weight ring must cover HBM latency");
+    static_assert(kSmemBytes <= 232448, "shared memory");
+};
+
+__device__ __forceinline__ int unit_owner(long long x, long long U, int G) {
+    return static_cast<int>(((x + 1) * G - 1) / U);
+}
+
+__device__ __forceinline__ long long unit_begin(int c, long long U, int G) {
+    return static_cast<long long>(c) * U / G;
+}
+
+// (tile, K block) of a running unit index, advanced without divisions (a 64-bit
+// division costs hundreds of cycles and used to dominate the per-unit loops).
+struct Cursor {
+    int tile, kb;
+    __device__ Cursor(long long u, int KB) : tile(static_cast<int>(u / KB)), kb(static_cast<int>(u % KB)) {}
+    __device__ void step(int KB) {
+        if (++kb == KB) {
+            kb = 0;
+            ++tile;
+        }
+    }
+    __device__ void step(int n, int KB) {
+        kb += n;
+        while (kb >= KB) {
+            kb -= KB;
+            ++tile;
+        }
+    }
+};
+
+// Warp-uniform bounded wait: every lane polls, the warp agrees on the outcome.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const WaitCtl& c) {
+    const bool ok = wait_bounded(bar, parity, c);
+    return __all_sync(0xffffffffu, ok);
+}
+
+// Wait used only while draining before exit: ignores the abort flag.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64_t timeout_ns) {
+    const uint64_t t0 = globaltimer();
+    for (uint32_t it = 0; it < (1u << 24); ++it) {
+        if (mbar_try_wait(bar, parity)) return;
+        if (globaltimer() - t0 > timeout_ns) return;
+    }
+}
+
+template <int NMMA, class F>
+__global__ void __launch_bounds__(kThreads, 1)
+    qgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                 const Params p) {
+    using L = Layout<NMMA, F::kWBytes>;
+    constexpr int kWStages = L::kWStages;
+    constexpr int kXStages = L::kXStages;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* gbase = smem_raw + (base - raw);
+
+    const uint32_t bar0 = base + L::kBarOff;
+    auto wfull = [&](int s) { return bar0 + 8u * s; };
+    auto wempty = [&](int s) { return bar0 + 8u * (kWStages + s); };
+    auto xfull = [&](int s) { return bar0 + 8u * (2 * kWStages + s); };
+    auto xempty = [&](int s) { return bar0 + 8u * (2 * kWStages + kXStages + s); };
+    constexpr int kBarA = 2 * kWStages + 2 * kXStages;
+    auto afull = [&](int a) { return bar0 + 8u * (kBarA + a); };
+    auto dfull = [&](int a) { return bar0 + 8u * (kBarA + kNA + a); };
+    auto dempty = [&](int a) { return bar0 + 8u * (kBarA + 2 * kNA + a); };
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + L::kMiscOff);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + L::kMiscOff + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int cta = blockIdx.x;
+    const long long u0 = unit_begin(cta, p.U, p.G);
+    const long long u1 = unit_begin(cta + 1, p.U, p.G);
+    const int nunits = static_cast<int>(u1 - u0);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kWStages; ++s) {
+            mbar_init(wfull(s), 1);
+            mbar_init(wempty(s), 4);   // the four warps of the dequant group that read it
+        }
+        for (int s = 0; s < kXStages; ++s) {
+            mbar_init(xfull(s), 1);
+            mbar_init(xempty(s), 4);   // the dequant group that saw the unit's MMAs complete
+        }
+        for (int a = 0; a < kNA; ++a) {
+            mbar_init(afull(a), 4);
+            mbar_init(dfull(a), 1);
+            mbar_init(dempty(a), 4);
+        }
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    __syncwarp();
+    if (warp == 0) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const WaitCtl wc{p.timeout_ns, p.status, abort_flag};
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ weight producer
+        if (lane == 0) {
+            if (F::kUsesTensorMapW) prefetch_tmap(&tmW);
+            const uint64_t pol_w = policy_evict_first();
+            int issued = 0;
+            Cursor cur(u0, p.KB);
+            for (int i = 0; i < nunits; ++i, cur.step(p.KB)) {
+                const int s = i % kWStages;
+                if (i >= kWStages && !wait_bounded(wempty(s), ((i / kWStages) - 1) & 1, wc)) break;
+                if (cta == 0 && i == p.fault_unit) continue;   // failure-path test hook
+                mbar_arrive_expect_tx(wfull(s), F::kWBytes);
+                F::load_w(base + s * F::kWBytes, &tmW, p, wfull(s), cur.tile, cur.kb, pol_w);
+                issued = i + 1;
+            }
+            // Every copy this thread started must land before the CTA can exit.
+            for (int i = issued - kWStages < 0 ? 0 : issued - kWStages; i < issued; ++i) {
+                if (cta == 0 && i == p.fault_unit) continue;
+                drain_wait(wfull(i % kWStages), (i / kWStages) & 1, p.timeout_ns);
+            }
+        }
+    } else if (warp == kWarpXProd) {
+        // ------------------------------------------------------------ X producer
+        if (lane == 0) {
+            prefetch_tmap(&tmX);
+            const uint64_t pol_x = policy_evict_last();
+            int issued = 0;
+            Cursor cur(u0, p.KB);
+            for (int i = 0; i < nunits; ++i, cur.step(p.KB)) {
+                const int s = i % kXStages;
+                if (i >= kXStages && !wait_bounded(xempty(s), ((i / kXStages) - 1) & 1, wc)) break;
+                const uint32_t st = base + L::kXOff + s * L::kXSlot;
+                mbar_arrive_expect_tx(xfull(s), L::kXSlot);
+                tma_load_2d(st, &tmX, xfull(s), cur.kb * 128, 0, pol_x);
+                tma_load_2d(st + L::kXBox, &tmX, xfull(s), cur.kb * 128 + 64, 0, pol_x);
+                issued = i + 1;
+            }
+            for (int i = issued - kXStages < 0 ? 0 : issued - kXStages; i < issued; ++i)
+                drain_wait(xfull(i % kXStages), (i / kXStages) & 1, p.timeout_ns);
+        }
+    } else if (warp == 1 || warp == kWarpMma2) {
+        // ------------------------------------------------------------ MMA issuers
+        if (lane == 0) {
+            const int first = warp == 1 ? 0 : 1;
+            constexpr uint32_t idesc = idesc_f16(NMMA, F::kBf16);
+            const uint64_t desc0 = smem_desc_sw128(base + L::kXOff);
+            int last = -1;
+            for (int i = first; i < nunits; i += kIssuers) {
+                const int s = i % kXStages;
+                const int a = i % kNA;
+                if (!wait_bounded(xfull(s), (i / kXStages) & 1, wc)) break;
+                if (!wait_bounded(afull(a), (i / kNA) & 1, wc)) break;
+                if (i >= kNA && !wait_bounded(dempty(a), ((i / kNA) - 1) & 1, wc)) break;
+                tc_fence_after();
+                // the descriptor's start-address field counts 16-byte units
+                const uint64_t xd = desc0 + static_cast<uint64_t>((s * L::kXSlot) >> 4);
+                const uint32_t dt = tmem + kDCol0 + a * 32;
+                const uint32_t at = tmem + a * 64;
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    mma_ts_f16(dt, at + j * 8, xd + (((j >> 2) * L::kXBox + (j & 3) * 32) >> 4), idesc,
+                               j > 0 ? 1u : 0u);
+                tc_commit(dfull(a));
+                last = i;
+            }
+            if (last >= 0) drain_wait(dfull(last % kNA), (last / kNA) & 1, p.timeout_ns);
+        }
+    } else if (warp < kWarpDeq0) {
+        // ------------------------------------------------------------ fold / epilogue
+        const int q = warp & 3;
+        const int row = q * 32 + lane;
+        const uint32_t tl = tmem + (static_cast<uint32_t>(q * 32) << 16);
+        const int first_tile = static_cast<int>(u0 / p.KB);
+        float outer[NMMA];
+#pragma unroll
+        for (int m = 0; m < NMMA; ++m) outer[m] = 0.0f;
+        // Block scales, 32 units per batch: lane l holds the scale of unit
+        // 32 b + l of the current batch and of the next one, which is fetched a
+        // whole batch ahead, so the per-unit value is a register shuffle and the
+        // load latency never meets the fold.
+        auto batch_scale = [&](int b) -> float {
+            if (!F::kHasFoldScale) return 1.0f;
+            const int i = 32 * b + lane;
+            if (i >= nunits) return 0.0f;
+            Cursor c(u0 + i, p.KB);
+            return __ldg(F::fold_scale_ptr(p, c.tile, c.kb));
+        };
+        float sc_cur = batch_scale(0);
+        float sc_next = batch_scale(1);
+        Cursor cur(u0, p.KB);
+        for (int i = 0; i < nunits; ++i, cur.step(p.KB)) {
+            const long long u = u0 + i;
+            const int tile = cur.tile;
+            const int kb = cur.kb;
+            const int a = i % kNA;
+            if ((i & 31) == 0 && i > 0) {
+                sc_cur = sc_next;
+                sc_next = batch_scale((i >> 5) + 1);
+            }
+            const float sc = __shfl_sync(0xffffffffu, sc_cur, i & 31);
+            if (!warp_wait(dfull(a), (i / kNA) & 1, wc)) break;
+            tc_fence_after();
+            uint32_t v0[16], v1[16];
+            tmem_ld_x16(tl + kDCol0 + a * 32, v0);
+            if constexpr (NMMA == 32) tmem_ld_x16(tl + kDCol0 + a * 32 + 16, v1);
+            tmem_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(dempty(a));
+#pragma unroll
+            for (int m = 0; m < 16; ++m) outer[m] = F::fold(outer[m], __uint_as_float(v0[m]), sc);
+            if constexpr (NMMA == 32) {
+#pragma unroll
+                for (int m = 0; m < 16; ++m) outer[16 + m] = F::fold(outer[16 + m], __uint_as_float(v1[m]), sc);
+            }
+
+            if (kb != p.KB - 1 && u != u1 - 1) continue;
+            // ---- end of this CTA's piece of `tile`
+            const int n = tile * 128 + row;
+            const bool whole = (kb == p.KB - 1) && (u - kb >= u0);
+            if (whole) {
+                if (n < p.N) {
+#pragma unroll
+                    for (int m = 0; m < NMMA; ++m)
+                        if (m < p.M) F::store(p.Y, static_cast<int64_t>(m) * p.ldy + n, outer[m]);
+                }
+            } else {
+                // Partial sums are stored row-major per thread ([slot][row][m]) so
+                // that a whole row moves with independent 16-byte accesses.
+                const int which = (tile == first_tile) ? 0 : 1;
+                float4* mine = reinterpret_cast<float4*>(p.part) +
+                               ((static_cast<size_t>(cta) * 2 + which) * 128 + row) * (NMMA / 4);
+#pragma unroll
+                for (int m4 = 0; m4 < NMMA / 4; ++m4)
+                    __stcg(mine + m4, make_float4(outer[4 * m4], outer[4 * m4 + 1], outer[4 * m4 + 2], outer[4 * m4 + 3]));
+                __threadfence();
+                __syncwarp();
+                uint32_t prev = 0;
+                if (lane == 0) prev = atomicAdd(p.cnt + tile * 4 + q, 1u);
+                prev = __shfl_sync(0xffffffffu, prev, 0);
+                const long long t0 = static_cast<long long>(tile) * p.KB;
+                const int cf = unit_owner(t0, p.U, p.G);
+                const int cl = unit_owner(t0 + p.KB - 1, p.U, p.G);
+                if (static_cast<int>(prev) == cl - cf) {
+                    // Last piece to arrive: sum all pieces in ascending K order.
+                    // A contributor's piece sits in its slot 0 when the tile is its
+                    // first tile: true for every contributor after the first (their
+                    // ranges start inside the tile), and for the first one only
+                    // when its range starts exactly at the tile.
+                    __threadfence();
+                    const int w_first = unit_begin(cf, p.U, p.G) == t0 ? 0 : 1;
+                    float acc[NMMA];
+#pragma unroll
+                    for (int m = 0; m < NMMA; ++m) acc[m] = 0.0f;
+                    for (int c2 = cf; c2 <= cl; ++c2) {
+                        float4* slot = reinterpret_cast<float4*>(p.part) +
+                                       ((static_cast<size_t>(c2) * 2 + (c2 == cf ? w_first : 0)) * 128 + row) * (NMMA / 4);
+                        float4 piece[NMMA / 4];
+#pragma unroll
+                        for (int m4 = 0; m4 < NMMA / 4; ++m4)
+                            piece[m4] = c2 == cta ? make_float4(outer[4 * m4], outer[4 * m4 + 1], outer[4 * m4 + 2],
+                                                                outer[4 * m4 + 3])
+                                                  : __ldcg(slot + m4);
+#pragma unroll
+                        for (int m4 = 0; m4 < NMMA / 4; ++m4) {
+                            acc[4 * m4 + 0] = __fadd_rn(acc[4 * m4 + 0], piece[m4].x);
+                            acc[4 * m4 + 1] = __fadd_rn(acc[4 * m4 + 1], piece[m4].y);
+                            acc[4 * m4 + 2] = __fadd_rn(acc[4 * m4 + 2], piece[m4].z);
+                            acc[4 * m4 + 3] = __fadd_rn(acc[4 * m4 + 3], piece[m4].w);
+                            __stcg(slot + m4, make_float4(0.0f, 0.0f, 0.0f, 0.0f));   // leave the workspace zero-filled
+                        }
+                    }
+                    if (n < p.N) {
+#pragma unroll
+                        for (int m = 0; m < NMMA; ++m)
+                            if (m < p.M) F::store(p.Y, static_cast<int64_t>(m) * p.ldy + n, acc[m]);
+                    }
+                    if (lane == 0) p.cnt[tile * 4 + q] = 0u;   // leave the workspace clean
+                }
+            }
+#pragma unroll
+            for (int m = 0; m < NMMA; ++m) outer[m] = 0.0f;
+        }
+    } else {
+        // ------------------------------------------------------------ dequant
+        const int q = warp & 3;
+        const int grp = (warp - kWarpDeq0) >> 2;   // takes units i with i % 2 == grp
+        const int row = q * 32 + lane;
+        const uint32_t tl = tmem + (static_cast<uint32_t>(q * 32) << 16);
+        typename F::Deq dq(p, u0, grp, nunits, row);
+        // one unit of this group; false when a wait gave up
+        auto unit = [&](int i, int slot) -> bool {
+            const int s = i % kWStages;
+            const int a = i % kNA;
+            dq.prepare(p, u0, i, nunits, row, slot);
+            if (!warp_wait(wfull(s), (i / kWStages) & 1, wc)) return false;
+            dq.load(gbase + s * F::kWBytes, row);
+            // the weight stage can be refilled once every lane holds its row
+            dq.settle();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(wempty(s));
+            if (i >= kNA) {
+                // unit i - kNA (this group's) is fully consumed once its MMAs are
+                // done: its A buffer is ours again and its X slice can be refilled
+                if (!warp_wait(dfull(a), ((i - kNA) / kNA) & 1, wc)) return false;
+                if (lane == 0) mbar_arrive(xempty((i - kNA) % kXStages));
+            }
+            __syncwarp();
+            tc_fence_after();
+#pragma unroll
+            for (int hlf = 0; hlf < 2; ++hlf) {
+                uint32_t o[32];
+                dq.convert(hlf, o);
+                tmem_st_x32(tl + a * 64 + hlf * 32, o);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(afull(a));
+            return true;
+        };
+        // unrolled by the dequantiser's look-ahead so that any per-unit value it
+        // prefetches lives in a fixed register slot (no moves that would wait)
+        constexpr int kAhead = F::Deq::kAhead;
+        bool ok = true;
+        for (int i0 = grp; i0 < nunits && ok; i0 += 2 * kAhead) {
+#pragma unroll
+            for (int j = 0; j < kAhead; ++j) {
+                const int i = i0 + 2 * j;
+                if (i < nunits && ok) ok = unit(i, j);
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+template <int NMMA, class F>
+cudaError_t launch(const Params& prm, const Schedule& s, const CUtensorMap& tmW, const CUtensorMap& tmX,
+                   cudaStream_t st) {
+    using L = Layout<NMMA, F::kWBytes>;
+    static int configured_device = -1;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (configured_device != dev) {
+        e = cudaFuncSetAttribute(qgemm_kernel<NMMA, F>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 L::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        configured_device = dev;
+    }
+    qgemm_kernel<NMMA, F><<<s.G, kThreads, L::kSmemBytes, st>>>(tmW, tmX, prm);
+    return cudaGetLastError();
+}
+
+// Common parameter block for a schedule and workspace.
+inline Params base_params(const Schedule& s, void* Y, int64_t ldy, int M, int N, int K, void* ws,
+                          const LaunchCtl& c) {
+    Params p{};
+    p.Y = Y;
+    p.ldy = ldy;
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.KB = s.KU;
+    p.U = s.U;
+    p.G = s.G;
+    uint8_t* w = static_cast<uint8_t*>(ws);
+    const size_t cnt_bytes = (static_cast<size_t>(s.T) * 4 * sizeof(uint32_t) + 255) & ~static_cast<size_t>(255);
+    p.cnt = reinterpret_cast<uint32_t*>(w);
+    p.part = w ? reinterpret_cast<float*>(w + cnt_bytes) : nullptr;
+    p.timeout_ns = c.timeout_ns;
+    p.fault_unit = c.fault_unit;
+    p.status = c.status;
+    return p;
+}
+
+}  // namespace gemm
+}  // namespace qg
