@@ -95,6 +95,34 @@ qg_status qgemm_fp8_block(const void *X, int64_t ldx,
                           struct CUstream_st *stream);
 
 /*
+ * The W8A16 FP8 block-scaled GEMM for callers that cannot allocate device
+ * memory -- for example a plug-in running inside a host framework that owns
+ * all device memory and hands it no allocator, or code that must not allocate
+ * while it serves requests.  (The paper has no counterpart of this entry
+ * point; it is an addition of this library.)
+ *
+ * Arguments and results are those of qgemm_fp8_block without the workspace:
+ * the split-K scratch is a fixed 8 MiB array inside the library, which every
+ * GPU that loads the library holds until the process exits.  The call
+ * allocates nothing.
+ *  - A shape whose scratch need (qg_workspace_bytes) exceeds 8 MiB returns
+ *    QG_ERR_WORKSPACE before anything is enqueued.
+ *  - The first call on a device looks up the array's device address (one
+ *    runtime query, with that device current); make that first call before
+ *    any stream capture.
+ *  - Every call on a device shares the one array, which keeps the previous
+ *    call's contents; each call clears the part it uses on `stream` first.
+ *    Calls whose execution overlaps on the GPU (different streams, or
+ *    concurrent host threads) race on the array and give wrong results:
+ *    serialise them.
+ */
+qg_status qgemm_fp8_block_noalloc(const void *X, int64_t ldx,
+                                  const uint8_t *W, const float *W_scale,
+                                  void *Y, int64_t ldy,
+                                  int M, int N, int K,
+                                  struct CUstream_st *stream);
+
+/*
  * W3A16 learned-LUT GEMM.
  *   X        device, FP16 [M, ldx], 16-byte aligned, ldx >= K, ldx % 8 == 0
  *   Wq       device, pack_lut3() output for an [N, K] code matrix
