@@ -204,6 +204,17 @@ void qg_set_wait_timeout_ns(uint64_t ns);
  */
 void qg_set_fault_injection(int unit);
 
+/*
+ * Overlap of consecutive GEMMs on a stream (off by default).  When enabled,
+ * the GEMM kernels are launched with programmatic stream serialization: a
+ * GEMM may start, and begin streaming its W and scales, while the kernel
+ * before it on the stream is still finishing; it waits for that kernel before
+ * it reads X or touches Y and the workspace.  Enable it only when W and the
+ * scales are not written by the work immediately preceding the GEMM on the
+ * same stream (true for model weights in decode).  Applies to later launches.
+ */
+void qg_set_weight_prefetch_overlap(int enable);
+
 /* Short English description of a status code (static storage). */
 const char *qg_status_string(qg_status status);
 

@@ -161,3 +161,32 @@ def test_extreme_scales_and_codes():
     X = wl.bf16_bits_from_f32(rng.standard_normal((M, K)).astype(np.float32) * 8)
     p = wl.Fp8Problem(M, N, K, X, W, S)
     _check(p, Fp8Device(p).run())
+
+
+def test_overlapped_launches_chain_and_share_workspace():
+    """With programmatic overlap on, a GEMM whose X is the previous GEMM's Y
+    still reads the finished Y, and calls sharing one workspace stay exact."""
+    q = qg()
+    pa = _problem(16, 5120, 5120, 42)
+    pb = _problem(16, 1024, 5120, 43)
+    da, db = Fp8Device(pa), Fp8Device(pb)
+    Xa = torch.from_numpy(pa.X.view(np.int16)).view(torch.bfloat16).cuda()
+    ws = q.Workspace()
+    q.set_weight_prefetch_overlap(True)
+    try:
+        outs = []
+        for _ in range(3):
+            Ya = q.qgemm_fp8_block(Xa, da.W[0], da.S, workspace=ws)
+            Yb = q.qgemm_fp8_block(Ya, db.W[0], db.S, workspace=ws)
+            outs.append((to_bits(Ya), to_bits(Yb)))
+        assert q.last_device_status() == 0
+    finally:
+        q.set_weight_prefetch_overlap(False)
+    ya, yb = outs[0]
+    ok, rep = grade_fp8(pa, ya)
+    assert rep.ok, rep
+    ok, rep = grade_fp8(pb, yb, X_bits=ya)
+    assert rep.ok, rep
+    for a2, b2 in outs[1:]:
+        assert np.array_equal(a2, ya) and np.array_equal(b2, yb)
+    assert int(ws.buf.count_nonzero()) == 0

@@ -26,7 +26,7 @@ __all__ = [
     "QgemmError", "LIB_PATH", "lib", "status_string", "workspace_bytes", "Workspace",
     "qgemm_fp8_block", "qgemm_lut3", "pack_lut3", "unpack_lut3", "lut3_packed_bytes",
     "dequant_e4m3_bf16", "dequant_lut3", "last_device_status", "set_wait_timeout_ns",
-    "set_fault_injection", "KIND_FP8_BLOCK", "KIND_LUT3", "STATUS",
+    "set_fault_injection", "set_weight_prefetch_overlap", "KIND_FP8_BLOCK", "KIND_LUT3", "STATUS",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -69,6 +69,7 @@ _SIGS = {
     "qg_last_device_status": (_I, [_P]),
     "qg_set_wait_timeout_ns": (None, [ctypes.c_uint64]),
     "qg_set_fault_injection": (None, [_I]),
+    "qg_set_weight_prefetch_overlap": (None, [_I]),
     "qg_status_string": (ctypes.c_char_p, [_I]),
     "qg_version": (ctypes.c_char_p, []),
 }
@@ -247,3 +248,9 @@ def set_wait_timeout_ns(ns: int) -> None:
 
 def set_fault_injection(unit: int) -> None:
     lib.qg_set_fault_injection(int(unit))
+
+
+def set_weight_prefetch_overlap(enable: bool) -> None:
+    """Let consecutive GEMMs on a stream overlap (weights stream early); see
+    include/qgemm.h for the condition under which this is safe."""
+    lib.qg_set_weight_prefetch_overlap(1 if enable else 0)

@@ -21,6 +21,7 @@ namespace {
 constexpr int kMaxDevices = 64;
 std::atomic<uint64_t> g_timeout_ns{1000000000ull};
 std::atomic<int> g_fault_unit{-1};
+std::atomic<int> g_overlap{0};
 
 struct DeviceInfo {
     std::once_flag once;
@@ -84,21 +85,29 @@ LaunchCtl launch_ctl(const DeviceInfo* d) {
     c.fault_unit = g_fault_unit.load();
     c.status = d->status;
     c.num_sms = d->sms;
+    c.overlap = g_overlap.load() != 0;
     return c;
 }
 
 // ----------------------------------------------------------------- dispatch
 // Per-(kind, M, N, K) choice of MMA width and grid.  The MMA N side is 16 for
 // M <= 16 and 32 above (one weight pass for every M <= 32).  The grid is one
-// CTA per SM, or one per work unit when there are fewer units than SMs.
+// CTA per SM, capped so that a 128-row tile is split over at most
+// kMaxPiecesPerTile CTAs: the CTA finishing a tile sums the other pieces one
+// after another, so small-N shapes run faster on fewer, longer CTAs.
+constexpr int kMaxPiecesPerTile = 4;
+
 Schedule choose_schedule(int kind, int M, int N, int K, int sms) {
+    (void)kind;
     Schedule s;
     s.nmma = M <= 16 ? 16 : 32;
     s.T = (N + 127) / 128;
     s.KU = (K + 127) / 128;   // one unit = 128 rows x one 128-wide K block
     s.U = static_cast<long long>(s.T) * s.KU;
-    s.G = static_cast<int>(s.U < sms ? s.U : sms);
-    if (s.G < 1) s.G = 1;
+    long long g = sms;
+    if (g > s.U) g = s.U;
+    if (g > static_cast<long long>(kMaxPiecesPerTile) * s.T) g = static_cast<long long>(kMaxPiecesPerTile) * s.T;
+    s.G = static_cast<int>(g < 1 ? 1 : g);
     return s;
 }
 
@@ -392,6 +401,8 @@ qg_status qg_last_device_status(cudaStream_t stream) {
 void qg_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns < 1000 ? 1000 : ns); }
 
 void qg_set_fault_injection(int unit) { g_fault_unit.store(unit < 0 ? -1 : unit); }
+
+void qg_set_weight_prefetch_overlap(int enable) { g_overlap.store(enable ? 1 : 0); }
 
 const char* qg_status_string(qg_status s) {
     switch (s) {

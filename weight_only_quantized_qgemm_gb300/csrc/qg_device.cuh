@@ -93,6 +93,17 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// Programmatic dependent launch: wait for the preceding grid on the stream
+// (and its memory) / let the next grid be scheduled.  Both are no-ops for a
+// grid launched without the programmatic-serialization attribute.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dependents_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Release/acquire fence at GPU scope (lighter than a sequentially consistent one).
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
 // ----------------------------------------------------------------- TMA
 __device__ __forceinline__ uint64_t policy_evict_first() {
     uint64_t p;

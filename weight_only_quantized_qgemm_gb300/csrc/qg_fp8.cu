@@ -73,8 +73,8 @@ cudaError_t launch_fp8(const Fp8Args& a, const Schedule& s, const CUtensorMap& t
     gemm::Params p = gemm::base_params(s, a.Y, a.ldy, a.M, a.N, a.K, a.ws, c);
     p.S = a.S;
     p.lds = a.lds;
-    if (s.nmma == 16) return gemm::launch<16, Fp8Fmt>(p, s, tmW, tmX, st);
-    return gemm::launch<32, Fp8Fmt>(p, s, tmW, tmX, st);
+    if (s.nmma == 16) return gemm::launch<16, Fp8Fmt>(p, s, tmW, tmX, c.overlap, st);
+    return gemm::launch<32, Fp8Fmt>(p, s, tmW, tmX, c.overlap, st);
 }
 
 }  // namespace qg

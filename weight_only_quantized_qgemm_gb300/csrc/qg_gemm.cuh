@@ -199,6 +199,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const WaitCtl wc{p.timeout_ns, p.status, abort_flag};
+    // The next grid on the stream may be scheduled now; its CTAs start as ours
+    // exit, and only its weight stream runs before it waits for this grid.
+    grid_dependents_launch();
 
     if (warp == 0) {
         // ------------------------------------------------------------ weight producer
@@ -225,6 +228,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ X producer
         if (lane == 0) {
             prefetch_tmap(&tmX);
+            // X may be the output of the preceding grid on the stream
+            grid_dependency_wait();
             const uint64_t pol_x = policy_evict_last();
             int issued = 0;
             Cursor cur(u0, p.KB);
@@ -273,6 +278,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row = q * 32 + lane;
         const uint32_t tl = tmem + (static_cast<uint32_t>(q * 32) << 16);
         const int first_tile = static_cast<int>(u0 / p.KB);
+        // Y and the workspace may still be in use by the preceding grid
+        grid_dependency_wait();
         float outer[NMMA];
 #pragma unroll
         for (int m = 0; m < NMMA; ++m) outer[m] = 0.0f;
@@ -335,7 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int m4 = 0; m4 < NMMA / 4; ++m4)
                     __stcg(mine + m4, make_float4(outer[4 * m4], outer[4 * m4 + 1], outer[4 * m4 + 2], outer[4 * m4 + 3]));
-                __threadfence();
+                fence_acq_rel_gpu();
                 __syncwarp();
                 uint32_t prev = 0;
                 if (lane == 0) prev = atomicAdd(p.cnt + tile * 4 + q, 1u);
@@ -349,7 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // first tile: true for every contributor after the first (their
                     // ranges start inside the tile), and for the first one only
                     // when its range starts exactly at the tile.
-                    __threadfence();
+                    fence_acq_rel_gpu();
                     const int w_first = unit_begin(cf, p.U, p.G) == t0 ? 0 : 1;
                     float acc[NMMA];
 #pragma unroll
@@ -445,7 +452,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int NMMA, class F>
 cudaError_t launch(const Params& prm, const Schedule& s, const CUtensorMap& tmW, const CUtensorMap& tmX,
-                   cudaStream_t st) {
+                   bool overlap, cudaStream_t st) {
     using L = Layout<NMMA, F::kWBytes>;
     static int configured_device = -1;
     int dev = 0;
@@ -457,8 +464,19 @@ cudaError_t launch(const Params& prm, const Schedule& s, const CUtensorMap& tmW,
         if (e != cudaSuccess) return e;
         configured_device = dev;
     }
-    qgemm_kernel<NMMA, F><<<s.G, kThreads, L::kSmemBytes, st>>>(tmW, tmX, prm);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(s.G));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = L::kSmemBytes;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    if (overlap) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, qgemm_kernel<NMMA, F>, tmW, tmX, prm);
 }
 
 // Common parameter block for a schedule and workspace.

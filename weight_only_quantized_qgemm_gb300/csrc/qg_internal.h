@@ -55,6 +55,7 @@ struct LaunchCtl {
     int fault_unit;
     uint32_t* status;    // device status word
     int num_sms;
+    bool overlap;        // launch with programmatic stream serialization
 };
 
 cudaError_t launch_fp8(const Fp8Args& a, const Schedule& s, const CUtensorMap& tmW,

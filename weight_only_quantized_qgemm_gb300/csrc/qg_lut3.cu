@@ -112,8 +112,8 @@ cudaError_t launch_lut3(const Lut3Args& a, const Schedule& s, const CUtensorMap&
     p.ld_lut_scales = a.ldsc;
     p.KT = (a.K + 255) / 256;
     CUtensorMap unused{};
-    if (s.nmma == 16) return gemm::launch<16, Lut3Fmt>(p, s, unused, tmX, st);
-    return gemm::launch<32, Lut3Fmt>(p, s, unused, tmX, st);
+    if (s.nmma == 16) return gemm::launch<16, Lut3Fmt>(p, s, unused, tmX, c.overlap, st);
+    return gemm::launch<32, Lut3Fmt>(p, s, unused, tmX, c.overlap, st);
 }
 
 }  // namespace qg
