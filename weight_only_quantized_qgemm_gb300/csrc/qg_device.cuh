@@ -101,9 +101,6 @@ __device__ __forceinline__ void grid_dependents_launch() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// Release/acquire fence at GPU scope (lighter than a sequentially consistent one).
-__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
-
 // ----------------------------------------------------------------- TMA
 __device__ __forceinline__ uint64_t policy_evict_first() {
     uint64_t p;
@@ -256,23 +253,26 @@ __device__ __forceinline__ uint32_t f16x2_mul(uint32_t a, uint32_t b) {
 
 // Four E4M3 codes r = [c3 c2 c1 c0] (c0 = lowest K) -> lo = BF16x2 {c0, c1},
 // hi = BF16x2 {c2, c3}; exact for every finite code, subnormals included.
-// A byte permute builds, per output pair, [c1 | sgn(c0) x 8 | c0 | 0]; an
-// arithmetic shift right by 4 then leaves each code's 7 magnitude bits under
-// the BF16 exponent/mantissa boundary with its sign replicated above them, and
-// a mask keeps the sign bit and the magnitude.  The result is 2^-120 times the
-// E4M3 value (a BF16 subnormal when the E4M3 exponent field is 0); one BF16
-// multiply by 2^120 restores the scale exactly.
-__device__ __forceinline__ uint32_t shr_s32(uint32_t v, int n) {
-    return static_cast<uint32_t>(static_cast<int32_t>(v) >> n);
+// A byte permute builds, per output pair, [sgn(c1) x 8 | c1 | sgn(c0) x 8 | c0];
+// a shift left by 4 (an integer multiply by 16, which runs on the FMA pipe
+// and leaves the ALU pipe to the permute and the mask) puts each code's 7
+// magnitude bits under the BF16 exponent/mantissa boundary with copies of its
+// sign above them, and a mask keeps the sign bit and the magnitude.  The
+// result is 2^-120 times the E4M3 value (a BF16 subnormal when the E4M3
+// exponent field is 0); one BF16 multiply by 2^120 restores the scale exactly.
+__device__ __forceinline__ uint32_t mul_lo_u32(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("mul.lo.u32 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
 }
 
 __device__ __forceinline__ void e4m3x4_to_bf16(uint32_t r, uint32_t& lo, uint32_t& hi) {
     constexpr uint32_t kTwo120 = 0x7B807B80u;  // BF16x2 {2^120, 2^120}
     constexpr uint32_t kKeep = 0x87F087F0u;    // sign + 7 magnitude bits per half
-    const uint32_t p0 = prmt(r, 0u, 0x1804u);  // [c1 | sgn(c0) | c0 | 0]
-    const uint32_t p1 = prmt(r, 0u, 0x3A24u);  // [c3 | sgn(c2) | c2 | 0]
-    lo = bf16x2_mul(shr_s32(p0, 4) & kKeep, kTwo120);
-    hi = bf16x2_mul(shr_s32(p1, 4) & kKeep, kTwo120);
+    const uint32_t p0 = prmt(r, 0u, 0x9180u);  // [sgn(c1) | c1 | sgn(c0) | c0]
+    const uint32_t p1 = prmt(r, 0u, 0xB3A2u);  // [sgn(c3) | c3 | sgn(c2) | c2]
+    lo = bf16x2_mul(mul_lo_u32(p0, 16u) & kKeep, kTwo120);
+    hi = bf16x2_mul(mul_lo_u32(p1, 16u) & kKeep, kTwo120);
 }
 
 // Byte planes of an 8-entry FP16 table e[0..7] given as four FP16x2 words

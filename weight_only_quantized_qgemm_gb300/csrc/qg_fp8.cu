@@ -45,12 +45,13 @@ struct Fp8Fmt {
 #pragma unroll
             for (int j = 0; j < 8; ++j) c[j] = *reinterpret_cast<const uint4*>(wrow + ((j ^ (row & 7)) << 4));
         }
-        // returns once every loaded chunk is in registers
-        __device__ void settle() const {
+        // a value that depends on every loaded word (the pipeline releases the
+        // weight stage only through it)
+        __device__ uint32_t token() const {
             uint32_t d = 0;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) d ^= c[j].x;
-            asm volatile("" ::"r"(d));
+            for (int j = 0; j < 8; ++j) d ^= c[j].x ^ c[j].y ^ c[j].z ^ c[j].w;
+            return d;
         }
         // columns 32*hlf .. 32*hlf+31 of the row's A fragment (K 64*hlf .. 64*hlf+63)
         __device__ void convert(int hlf, uint32_t (&o)[32]) const {

@@ -81,6 +81,7 @@ struct Params {
     uint64_t timeout_ns;
     int fault_unit;
     uint32_t* status;
+    uint32_t opaque_zero;         // always 0; the compiler cannot know that
 };
 
 template <int NMMA, int WBYTES>
@@ -89,7 +90,13 @@ struct Layout {
     static constexpr int kXBox = NMMA * 128;
     static constexpr int kXStages = 8;
     static constexpr int kWBudget = 212992 - kXStages * kXSlot;   // 208 KB in all
-    static constexpr int kWStages = (kWBudget / WBYTES) < 24 ? (kWBudget / WBYTES) : 24;
+    // Even, so that every use of a weight stage falls to the same dequant group
+    // (units i and i + kWStages have the same parity).  A group's parity wait
+    // on a stage is then always for the phase right after one it has already
+    // seen; with an odd count it could be for a phase after the other group's
+    // still-pending one, and a parity wait cannot tell those two apart.
+    static constexpr int kWFit = (kWBudget / WBYTES) < 24 ? (kWBudget / WBYTES) : 24;
+    static constexpr int kWStages = kWFit & ~1;
     static constexpr int kXOff = kWStages * WBYTES;
     static constexpr int kBarOff = kXOff + kXStages * kXSlot;
     static constexpr int kNumBars = 2 * kWStages + 2 * kXStages + 3 * kNA;
@@ -97,7 +104,11 @@ struct Layout {
     static constexpr int kSmemBytes = kMiscOff + 64 + 1024;  // + alignment slack
     static_assert(WBYTES % 1024 == 0 && kXSlot % 1024 == 0, "keep the 1024-byte swizzle alignment");
     static_assert(kXStages >= 2 * kNA, "X slices are held until the unit kNA later is dequantised");
+    // the same ownership rule for the other rings: an X stage and an A/D buffer
+    // are always used by the same MMA issuer and the same dequant group
+    static_assert(kXStages % kIssuers == 0 && kNA % kIssuers == 0 && kNA % 2 == 0, "ring ownership");
     static_assert(kWStages >= 8, "the weight ring must cover HBM latency");
+    static_assert(kWStages % 2 == 0, "a weight stage must belong to one dequant group");
     static_assert(kSmemBytes <= 232448, "shared memory");
 };
 
@@ -342,7 +353,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int m4 = 0; m4 < NMMA / 4; ++m4)
                     __stcg(mine + m4, make_float4(outer[4 * m4], outer[4 * m4 + 1], outer[4 * m4 + 2], outer[4 * m4 + 3]));
-                fence_acq_rel_gpu();
+                // Every lane's partial must be visible GPU-wide before lane 0's
+                // arrival: a sequentially consistent fence per writing lane (an
+                // acquire-release fence is not enough, since the lanes that
+                // wrote are not the lane that performs the atomic).
+                __threadfence();
                 __syncwarp();
                 uint32_t prev = 0;
                 if (lane == 0) prev = atomicAdd(p.cnt + tile * 4 + q, 1u);
@@ -356,7 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // first tile: true for every contributor after the first (their
                     // ranges start inside the tile), and for the first one only
                     // when its range starts exactly at the tile.
-                    fence_acq_rel_gpu();
+                    __threadfence();
                     const int w_first = unit_begin(cf, p.U, p.G) == t0 ? 0 : 1;
                     float acc[NMMA];
 #pragma unroll
@@ -404,10 +419,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             dq.prepare(p, u0, i, nunits, row, slot);
             if (!warp_wait(wfull(s), (i / kWStages) & 1, wc)) return false;
             dq.load(gbase + s * F::kWBytes, row);
-            // the weight stage can be refilled once every lane holds its row
-            dq.settle();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(wempty(s));
+            // The weight stage is refilled as soon as it is released, so the
+            // release must not be performed before every lane's shared-memory
+            // loads have returned.  Program order alone does not ensure that: the
+            // arrive uses none of the loaded registers.  Its address is therefore
+            // made to depend on all of them, through a warp reduction of a word
+            // derived from each lane's loads and a zero known only at run time.
+            const uint32_t tok = __reduce_or_sync(0xffffffffu, dq.token());
+            if (lane == 0) mbar_arrive(wempty(s) + (tok & p.opaque_zero));
             if (i >= kNA) {
                 // unit i - kNA (this group's) is fully consumed once its MMAs are
                 // done: its A buffer is ours again and its X slice can be refilled
@@ -498,6 +517,7 @@ inline Params base_params(const Schedule& s, void* Y, int64_t ldy, int M, int N,
     p.timeout_ns = c.timeout_ns;
     p.fault_unit = c.fault_unit;
     p.status = c.status;
+    p.opaque_zero = 0;
     return p;
 }
 
