@@ -5,10 +5,15 @@ weights, [128 x 128] FP32 block scales, BF16 X and Y).  One step is one call of
 the whole path (weight stream, dequant, tensor-core MMA, two-level fold,
 split-K reduction, BF16 store).  Inputs are resident in HBM; the weight
 matrix rotates over enough copies (>= 2x the L2 size) that no step finds its
-weights in L2.  `value` is algorithmic bytes per call (W + scales + X + Y,
-each counted once) / device time per call.
+weights in L2.  Calls are launched with weight-prefetch overlap (a call may
+start streaming its weights while the previous call finishes; it waits for
+that call before it reads X or writes Y), as consecutive decode GEMMs would
+run; `--overlap 0` times them strictly one after another.  `value` is
+algorithmic bytes per call (W + scales + X + Y, each counted once) / device
+time per call.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--quick]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--quick] [--overlap 0|1]
 
 Under torchrun each rank runs an independent replica (the GEMM has no
 exchange step); rank 0 prints the line with the max time over ranks.
@@ -159,6 +164,8 @@ def gpu_uuid(torch, dev):
 
 # ----------------------------------------------------------------- our arm
 def time_calls(torch, stream, fn, steps, warmup):
+    """Device time per call (ms) of `steps` calls issued back to back on
+    `stream`, after `warmup` untimed ones; CUDA events on that stream."""
     with torch.cuda.stream(stream):
         for i in range(warmup):
             fn(i)
@@ -171,82 +178,100 @@ def time_calls(torch, stream, fn, steps, warmup):
             fn(i)
         e1.record(stream)
     torch.cuda.synchronize()
-    return e0.elapsed_time(e1) / steps  # ms per call
+    return e0.elapsed_time(e1) / steps
 
 
-def fp8_case(torch, qg, M, N, K, config_id, copies_min=1):
-    import workloads as wl
-    p = wl.make_fp8_problem(M, N, K, config_id=config_id)
-    copies = max(copies_min, -(-2 * L2_BYTES // (N * K)) + 1)
-    W = [torch.from_numpy(p.W).cuda() for _ in range(copies)]
-    S = torch.from_numpy(p.S).cuda()
-    X = torch.from_numpy(p.X.view(np.int16)).view(torch.bfloat16).cuda()
-    Y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
-    ws = qg.Workspace()
-    return p, W, S, X, Y, ws, copies
+class Fp8Case:
+    """One FP8 problem resident on the device: enough rotating weight copies
+    (>= 2x L2) that no call finds its weights in L2; M <= M_max runs on the
+    first M rows of X and Y."""
+
+    def __init__(self, torch, qg, M_max, N, K, config_id):
+        import workloads as wl
+        self.torch, self.qg = torch, qg
+        self.p = wl.make_fp8_problem(M_max, N, K, config_id=config_id)
+        self.N, self.K = N, K
+        self.copies = -(-2 * L2_BYTES // (N * K)) + 1
+        self.W = [torch.from_numpy(self.p.W).cuda() for _ in range(self.copies)]
+        self.S = torch.from_numpy(self.p.S).cuda()
+        self.X = torch.from_numpy(self.p.X.view(np.int16)).view(torch.bfloat16).cuda()
+        self.Y = torch.empty((M_max, N), dtype=torch.bfloat16, device="cuda")
+        self.ws = qg.Workspace()
+
+    def stepper(self, M, stream):
+        qg, N, K = self.qg, self.N, self.K
+        buf = self.ws.get(qg.workspace_bytes(qg.KIND_FP8_BLOCK, M, N, K))
+        ws_ptr = buf.data_ptr() if buf is not None else None
+        ws_n = buf.numel() if buf is not None else 0
+        lib, sptr, copies = qg.lib, stream.cuda_stream, self.copies
+        xp, yp, sp = self.X.data_ptr(), self.Y.data_ptr(), self.S.data_ptr()
+        wps = [w.data_ptr() for w in self.W]
+
+        def step(i):
+            r = lib.qgemm_fp8_block(xp, K, wps[i % copies], sp, yp, N, M, N, K, ws_ptr, ws_n, sptr)
+            if r:
+                raise RuntimeError(qg.status_string(r))
+        return step
+
+    def time(self, M, stream, steps, warmup):
+        ms = time_calls(self.torch, stream, self.stepper(M, stream), steps, warmup)
+        st = self.qg.last_device_status(stream)
+        if st:
+            raise RuntimeError(f"device status {self.qg.status_string(st)}")
+        return ms
+
+    def free(self):
+        self.W = self.S = self.X = self.Y = self.ws = None
 
 
-def bench_fp8(torch, qg, stream, M, N, K, config_id, steps, warmup):
-    p, W, S, X, Y, ws, copies = fp8_case(torch, qg, M, N, K, config_id)
-    wsbuf = ws.get(qg.workspace_bytes(qg.KIND_FP8_BLOCK, M, N, K))
-    ws_ptr = wsbuf.data_ptr() if wsbuf is not None else None
-    ws_n = wsbuf.numel() if wsbuf is not None else 0
-    lib = qg.lib
-    sptr = stream.cuda_stream
-    xp, yp, sp = X.data_ptr(), Y.data_ptr(), S.data_ptr()
-    wps = [w.data_ptr() for w in W]
+class Lut3Case:
+    """The 3-bit learned-LUT problem, packed once, rotated over >= 2x L2."""
 
-    def step(i):
-        r = lib.qgemm_fp8_block(xp, K, wps[i % copies], sp, yp, N, M, N, K, ws_ptr, ws_n, sptr)
-        if r:
-            raise RuntimeError(qg.status_string(r))
+    def __init__(self, torch, qg, M_max, N, K):
+        import workloads as wl
+        self.torch, self.qg = torch, qg
+        p = wl.make_lut3_problem(M_max, N, K, config_id=4)
+        packed = qg.pack_lut3(p.codes)
+        self.N, self.K = N, K
+        self.copies = -(-2 * L2_BYTES // packed.size) + 1
+        self.Wq = [torch.from_numpy(packed).cuda() for _ in range(self.copies)]
+        self.qm = torch.from_numpy(p.qmap.view(np.int16)).view(torch.float16).cuda()
+        self.sc = torch.from_numpy(p.scales.view(np.int16)).view(torch.float16).cuda()
+        self.X = torch.from_numpy(p.X.view(np.int16)).view(torch.float16).cuda()
+        self.Y = torch.empty((M_max, N), dtype=torch.float16, device="cuda")
+        self.ws = qg.Workspace()
 
-    ms = time_calls(torch, stream, step, steps, warmup)
-    st = qg.last_device_status(stream)
-    if st:
-        raise RuntimeError(f"device status {qg.status_string(st)}")
-    return ms, copies, p, (W, S, X, Y, ws)
+    def time(self, M, stream, steps, warmup):
+        qg, N, K = self.qg, self.N, self.K
+        buf = self.ws.get(qg.workspace_bytes(qg.KIND_LUT3, M, N, K))
+        ws_ptr = buf.data_ptr() if buf is not None else None
+        ws_n = buf.numel() if buf is not None else 0
+        lib, sptr, copies = qg.lib, stream.cuda_stream, self.copies
+        xp, yp, qp, scp = self.X.data_ptr(), self.Y.data_ptr(), self.qm.data_ptr(), self.sc.data_ptr()
+        wps = [w.data_ptr() for w in self.Wq]
 
+        def step(i):
+            r = lib.qgemm_lut3(xp, K, wps[i % copies], qp, scp, yp, N, M, N, K, ws_ptr, ws_n, sptr)
+            if r:
+                raise RuntimeError(qg.status_string(r))
+        ms = time_calls(self.torch, stream, step, steps, warmup)
+        st = qg.last_device_status(stream)
+        if st:
+            raise RuntimeError(f"device status {qg.status_string(st)}")
+        return ms
 
-def bench_lut3(torch, qg, stream, M, N, K, steps, warmup):
-    import workloads as wl
-    p = wl.make_lut3_problem(M, N, K, config_id=4)
-    packed = qg.pack_lut3(p.codes)
-    copies = max(1, -(-2 * L2_BYTES // packed.size) + 1)
-    Wq = [torch.from_numpy(packed).cuda() for _ in range(copies)]
-    qm = torch.from_numpy(p.qmap.view(np.int16)).view(torch.float16).cuda()
-    sc = torch.from_numpy(p.scales.view(np.int16)).view(torch.float16).cuda()
-    X = torch.from_numpy(p.X.view(np.int16)).view(torch.float16).cuda()
-    Y = torch.empty((M, N), dtype=torch.float16, device="cuda")
-    ws = qg.Workspace()
-    wsbuf = ws.get(qg.workspace_bytes(qg.KIND_LUT3, M, N, K))
-    ws_ptr = wsbuf.data_ptr() if wsbuf is not None else None
-    ws_n = wsbuf.numel() if wsbuf is not None else 0
-    lib = qg.lib
-    sptr = stream.cuda_stream
-    wps = [w.data_ptr() for w in Wq]
-
-    def step(i):
-        r = lib.qgemm_lut3(X.data_ptr(), K, wps[i % copies], qm.data_ptr(), sc.data_ptr(), Y.data_ptr(), N,
-                           M, N, K, ws_ptr, ws_n, sptr)
-        if r:
-            raise RuntimeError(qg.status_string(r))
-
-    ms = time_calls(torch, stream, step, steps, warmup)
-    st = qg.last_device_status(stream)
-    if st:
-        raise RuntimeError(f"device status {qg.status_string(st)}")
-    return ms, copies
+    def free(self):
+        self.Wq = self.qm = self.sc = self.X = self.Y = self.ws = None
 
 
-def e2e_fp8(torch, qg, stream, state, M, N, K, steps, warmup):
+def e2e_fp8(torch, qg, stream, case, M, steps, warmup):
     """Through the public Python API with host buffers: each step copies X in
     from pinned host memory and Y back out, inside the timed region."""
-    W, S, X, Y, ws = state
-    copies = len(W)
+    X, Y = case.X[:M], case.Y[:M]
     Xh = torch.empty(X.shape, dtype=X.dtype).pin_memory()
     Xh.copy_(X.cpu())
     Yh = torch.empty(Y.shape, dtype=Y.dtype).pin_memory()
+    W, S, ws, copies = case.W, case.S, case.ws, case.copies
 
     def step(i):
         X.copy_(Xh, non_blocking=True)
@@ -255,6 +280,39 @@ def e2e_fp8(torch, qg, stream, state, M, N, K, steps, warmup):
 
     ms = time_calls(torch, stream, step, steps, warmup)
     return ms, X.numel() * X.element_size(), Y.numel() * Y.element_size()
+
+
+def secondary_lines(torch, qg, stream, peak, steps=2000, warmup=50):
+    """The other configurations (not the headline): us/call, GB/s, fraction
+    of the HBM peak."""
+    out = {}
+
+    def rec(name, ms, nbytes):
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        out[name] = {"us": round(ms * 1e3, 3), "GBps": round(gbs, 1), "frac": round(gbs / peak, 4)}
+
+    c = Fp8Case(torch, qg, 16, 17408, 5120, 1)
+    for m in (1, 8):
+        rec(f"fp8_gateup_M{m}", c.time(m, stream, steps, warmup), fp8_bytes(m, 17408, 5120))
+    c.free()
+    c = Fp8Case(torch, qg, 32, 5120, 17408, 2)
+    for m in (1, 16, 32):
+        rec(f"fp8_down_M{m}", c.time(m, stream, steps, warmup), fp8_bytes(m, 5120, 17408))
+    c.free()
+    for n in (1024, 5120, 6144):
+        c = Fp8Case(torch, qg, 32, n, 5120, 3)
+        for m in (1, 2, 4, 5, 8, 16, 17, 24, 32):
+            rec(f"fp8_attn_N{n}_M{m}", c.time(m, stream, steps, warmup), fp8_bytes(m, n, 5120))
+        c.free()
+    c = Fp8Case(torch, qg, 1, 256, 512, 0)
+    rec("fp8_small_M1", c.time(1, stream, steps, warmup), fp8_bytes(1, 256, 512))
+    c.free()
+    c = Lut3Case(torch, qg, 16, 28672, 8192)
+    for m in (1, 4, 8, 16):
+        rec(f"lut3_M{m}", c.time(m, stream, steps, warmup), lut3_bytes(m, 28672, 8192))
+    c.free()
+    torch.cuda.empty_cache()
+    return out
 
 
 def cpu_baseline(M, N, K, config_id, budget_s=12.0):
@@ -322,6 +380,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--quick", action="store_true", help="headline only, no secondary configs or CPU baseline")
+    ap.add_argument("--overlap", type=int, choices=[0, 1], default=1,
+                    help="launch with weight-prefetch overlap of consecutive calls (default 1)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -345,22 +405,13 @@ def main():
     M, N, K, cid = HEAD["M"], HEAD["N"], HEAD["K"], HEAD["config_id"]
     stream = torch.cuda.Stream()
     sampler = ClockSampler(gpu_uuid(torch, local))
+    # consecutive calls may overlap: a call streams its weights while the one
+    # before it finishes (weights are never written by the preceding call)
+    qg.set_weight_prefetch_overlap(bool(args.overlap))
 
-    # headline: warm up, then the timed region with clocks sampled alongside
-    p, W, S, X, Y, ws, copies = fp8_case(torch, qg, M, N, K, cid)
-    wsbuf = ws.get(qg.workspace_bytes(qg.KIND_FP8_BLOCK, M, N, K))
-    ws_ptr = wsbuf.data_ptr() if wsbuf is not None else None
-    ws_n = wsbuf.numel() if wsbuf is not None else 0
-    lib = qg.lib
-    sptr = stream.cuda_stream
-    xp, yp, sp = X.data_ptr(), Y.data_ptr(), S.data_ptr()
-    wps = [w.data_ptr() for w in W]
-
-    def step(i):
-        r = lib.qgemm_fp8_block(xp, K, wps[i % copies], sp, yp, N, M, N, K, ws_ptr, ws_n, sptr)
-        if r:
-            raise RuntimeError(qg.status_string(r))
-
+    # headline: warm up, then exactly `steps` calls with clocks sampled alongside
+    case = Fp8Case(torch, qg, M, N, K, cid)
+    step = case.stepper(M, stream)
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
             step(i)
@@ -393,9 +444,12 @@ def main():
     per_call_bytes = fp8_bytes(M, N, K)
     value = per_call_bytes * world / (ms * 1e-3) / 1e9
     achieved = per_call_bytes / (ms * 1e-3) / 1e9
+    copies = case.copies
 
-    e2e_ms, h2d, d2h = e2e_fp8(torch, qg, stream, (W, S, X, Y, ws), M, N, K,
-                               steps=max(200, min(args.steps, 5000)), warmup=args.warmup)
+    e2e_ms, h2d, d2h = e2e_fp8(torch, qg, stream, case, M, steps=max(200, min(args.steps, 5000)),
+                               warmup=args.warmup)
+    case.free()
+    torch.cuda.empty_cache()
     if rank != 0:
         if world > 1:
             import torch.distributed as dist
@@ -406,28 +460,8 @@ def main():
     secondary = {}
     cpu = None
     if not args.quick:
-        sec_steps = 2000
         try:
-            for m in (1, 8):
-                ms2, _, _, _ = bench_fp8(torch, qg, stream, m, N, K, cid, sec_steps, 50)
-                secondary[f"fp8_gateup_M{m}"] = {"us": round(ms2 * 1e3, 3),
-                                                 "GBps": round(fp8_bytes(m, N, K) / (ms2 * 1e-3) / 1e9, 1)}
-            for m in (16, 32):
-                ms2, _, _, _ = bench_fp8(torch, qg, stream, m, 5120, 17408, 2, sec_steps, 50)
-                secondary[f"fp8_down_M{m}"] = {"us": round(ms2 * 1e3, 3),
-                                               "GBps": round(fp8_bytes(m, 5120, 17408) / (ms2 * 1e-3) / 1e9, 1)}
-            for n in (1024, 5120, 6144):
-                for m in (1, 16, 32):
-                    ms2, _, _, _ = bench_fp8(torch, qg, stream, m, n, 5120, 3, sec_steps, 50)
-                    secondary[f"fp8_attn_N{n}_M{m}"] = {
-                        "us": round(ms2 * 1e3, 3), "GBps": round(fp8_bytes(m, n, 5120) / (ms2 * 1e-3) / 1e9, 1)}
-            ms2, _, _, _ = bench_fp8(torch, qg, stream, 1, 256, 512, 0, sec_steps, 50)
-            secondary["fp8_small_M1"] = {"us": round(ms2 * 1e3, 3)}
-            for m in (1, 16):
-                ms3, _ = bench_lut3(torch, qg, stream, m, 28672, 8192, sec_steps, 50)
-                secondary[f"lut3_M{m}"] = {"us": round(ms3 * 1e3, 3),
-                                           "GBps": round(lut3_bytes(m, 28672, 8192) / (ms3 * 1e-3) / 1e9, 1),
-                                           "frac": round(lut3_bytes(m, 28672, 8192) / (ms3 * 1e-3) / 1e9 / peak, 4)}
+            secondary = secondary_lines(torch, qg, stream, peak)
         except Exception as e:  # secondary numbers must not hide the headline
             secondary["error"] = repr(e)[:300]
         cpu, _ = cpu_baseline(M, N, K, cid)
@@ -451,6 +485,7 @@ def main():
                    "M": M, "N": N, "K": K, "weights": "E4M3 [N,K] + FP32 [128x128] block scales",
                    "arith": "E4M3->BF16 exact dequant, BF16 x BF16 tcgen05 MMA, FP32 two-level fold, BF16 out",
                    "l2": f"inputs larger than L2: {copies} rotating weight copies ({copies * N * K / 1e6:.0f} MB)",
+                   "overlap": "weight prefetch overlaps the previous call" if args.overlap else "off",
                    "parallelism": "replicas" if world > 1 else "1 GPU"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": peak_kind,

@@ -67,9 +67,12 @@ enum { QG_KIND_FP8_BLOCK = 0, QG_KIND_LUT3 = 1 };
 
 /*
  * Bytes of device workspace a call of the given kind and shape needs on the
- * current device (0 if none).  The workspace holds split-K partial sums and
- * per-tile arrival counters.  It must be zero-filled once before its first
- * use; every successful call leaves it zero-filled again.
+ * current device (0 if none).  The workspace holds split-K partial sums
+ * (scratch, sized for the device's largest grid) followed by per-tile arrival
+ * counters (the last 16 * ceil(N/128) bytes, rounded up to 256).  It must be
+ * zero-filled once before its first use; every successful call leaves its
+ * counters at zero again, so one workspace serves later calls of any shape
+ * without clearing.
  */
 size_t qg_workspace_bytes(int kind, int M, int N, int K);
 

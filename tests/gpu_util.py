@@ -115,3 +115,13 @@ def sample_indices(M, N, count, seed=0):
     ms = np.concatenate([ms, [0, M - 1, 0, M - 1]])
     ns = np.concatenate([ns, [0, 0, N - 1, N - 1]])
     return ms.astype(np.int32), ns.astype(np.int32)
+
+
+def assert_counters_clear(q, ws, kind, M, N, K):
+    """The workspace's arrival counters (everything from the counter offset
+    on, for every shape) are zero, as the header promises after a call."""
+    need = q.workspace_bytes(kind, M, N, K)
+    assert need > 0
+    cnt_bytes = (16 * (-(-N // 128)) + 255) // 256 * 256
+    off = need - cnt_bytes
+    assert int(ws.buf[off:].count_nonzero()) == 0

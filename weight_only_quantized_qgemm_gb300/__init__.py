@@ -106,9 +106,9 @@ def workspace_bytes(kind: int, M: int, N: int, K: int) -> int:
 
 
 class Workspace:
-    """A zero-filled device byte buffer that grows on demand.  Calls leave it
-    zero-filled again, so one buffer serves any sequence of calls on one
-    stream."""
+    """A zero-filled device byte buffer that grows on demand.  Calls leave
+    its arrival counters at zero again (the partial-sum area in front of them
+    is scratch), so one buffer serves any sequence of calls on one stream."""
 
     def __init__(self, device=None):
         self.device = device

@@ -91,11 +91,28 @@ LaunchCtl launch_ctl(const DeviceInfo* d) {
 
 // ----------------------------------------------------------------- dispatch
 // Per-(kind, M, N, K) choice of MMA width and grid.  The MMA N side is 16 for
-// M <= 16 and 32 above (one weight pass for every M <= 32).  The grid is one
-// CTA per SM, capped so that a 128-row tile is split over at most
-// kMaxPiecesPerTile CTAs: the CTA finishing a tile sums the other pieces one
-// after another, so small-N shapes run faster on fewer, longer CTAs.
+// M <= 16 and 32 above (one weight pass for every M <= 32).  Two grids are
+// weighed by the work units (128 rows x 128 K) of their busiest CTA:
+//  - one CTA per 128-row tile, when the tiles fit on the SMs: no tile is
+//    split, so no partial sums and no reduction;
+//  - stream-K: one CTA per SM, the units split evenly, capped so that a tile
+//    is shared by about kMaxPiecesPerTile CTAs at most.  A split tile costs
+//    the CTA that finishes it a partial-sum store, an arrival atomic and the
+//    reduction, at the end of the kernel; that tail measured about as long
+//    as kSplitCostUnits units of steady streaming.
+// Ties go to the grid without splits.
 constexpr int kMaxPiecesPerTile = 4;
+constexpr long long kSplitCostUnits = 10;
+
+long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
+
+bool splits(long long U, int KU, int G) {
+    for (int c = 0; c <= G; ++c) {
+        const long long b = static_cast<long long>(c) * U / G;
+        if (b % KU != 0) return true;
+    }
+    return false;
+}
 
 Schedule choose_schedule(int kind, int M, int N, int K, int sms) {
     (void)kind;
@@ -107,25 +124,39 @@ Schedule choose_schedule(int kind, int M, int N, int K, int sms) {
     long long g = sms;
     if (g > s.U) g = s.U;
     if (g > static_cast<long long>(kMaxPiecesPerTile) * s.T) g = static_cast<long long>(kMaxPiecesPerTile) * s.T;
-    s.G = static_cast<int>(g < 1 ? 1 : g);
+    if (g < 1) g = 1;
+    long long cost = ceil_div(s.U, g) + (splits(s.U, s.KU, static_cast<int>(g)) ? kSplitCostUnits : 0);
+    if (s.T <= sms && static_cast<long long>(s.KU) <= cost) g = s.T;
+    s.G = static_cast<int>(g);
+    s.max_ctas = sms > s.G ? sms : s.G;
     return s;
 }
 
 // True when some tile's units are spread over more than one CTA.
-bool schedule_splits(const Schedule& s) {
-    for (int c = 0; c <= s.G; ++c) {
-        const long long b = static_cast<long long>(c) * s.U / s.G;
-        if (b % s.KU != 0) return true;
-    }
-    return false;
-}
+bool schedule_splits(const Schedule& s) { return splits(s.U, s.KU, s.G); }
 
 }  // namespace
+
+size_t workspace_partial_bytes(const Schedule& s) {
+    return static_cast<size_t>(s.max_ctas) * 2 * 32 * 128 * sizeof(float);
+}
 
 size_t workspace_bytes(const Schedule& s) {
     if (!schedule_splits(s)) return 0;
     const size_t cnt = (static_cast<size_t>(s.T) * 4 * sizeof(uint32_t) + 255) & ~static_cast<size_t>(255);
-    return cnt + static_cast<size_t>(s.G) * 2 * s.nmma * 128 * sizeof(float);
+    return workspace_partial_bytes(s) + cnt;
+}
+
+void workspace_counters(int kind, int M, int N, int K, size_t* offset, size_t* bytes) {
+    *offset = 0;
+    *bytes = 0;
+    DeviceInfo* d = device_info();
+    if (!d || M <= 0 || N <= 0 || K <= 0) return;
+    const Schedule s = choose_schedule(kind, M, N, K, d->sms);
+    const size_t total = workspace_bytes(s);
+    if (total == 0) return;
+    *offset = workspace_partial_bytes(s);
+    *bytes = total - *offset;
 }
 
 uint32_t* device_status_ptr() {

@@ -34,30 +34,33 @@ struct Fp8Fmt {
         static_cast<__nv_bfloat16*>(Y)[idx] = __float2bfloat16_rn(v);
     }
 
-    // One thread dequantises one weight row (128 codes) of a unit.
+    // One thread dequantises one weight row (128 codes) of a unit.  Two
+    // register slots: the pipeline loads the group's next unit into one while
+    // it converts the current unit from the other.
     struct Deq {
-        static constexpr int kAhead = 1;
-        uint4 c[8];
+        static constexpr int kUnroll = 2;
+        uint4 c[2][8];
         __device__ Deq(const gemm::Params&, long long, int, int, int) {}
-        __device__ void prepare(const gemm::Params&, long long, int, int, int, int) {}
-        __device__ void load(const uint8_t* stage, int row) {
+        __device__ void prepare(const gemm::Params&, int, int, int, int) {}
+        __device__ void load(int slot, const uint8_t* stage, int row) {
             const uint8_t* wrow = stage + row * 128;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) c[j] = *reinterpret_cast<const uint4*>(wrow + ((j ^ (row & 7)) << 4));
+            for (int j = 0; j < 8; ++j)
+                c[slot][j] = *reinterpret_cast<const uint4*>(wrow + ((j ^ (row & 7)) << 4));
         }
-        // a value that depends on every loaded word (the pipeline releases the
-        // weight stage only through it)
-        __device__ uint32_t token() const {
+        // a value that depends on every loaded word of the slot (the pipeline
+        // releases the weight stage only through it)
+        __device__ uint32_t token(int slot) const {
             uint32_t d = 0;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) d ^= c[j].x ^ c[j].y ^ c[j].z ^ c[j].w;
+            for (int j = 0; j < 8; ++j) d ^= c[slot][j].x ^ c[slot][j].y ^ c[slot][j].z ^ c[slot][j].w;
             return d;
         }
-        // columns 32*hlf .. 32*hlf+31 of the row's A fragment (K 64*hlf .. 64*hlf+63)
-        __device__ void convert(int hlf, uint32_t (&o)[32]) const {
+        // columns 16*qtr .. 16*qtr+15 of the row's A fragment (K 32*qtr .. 32*qtr+31)
+        __device__ void convert(int slot, int qtr, uint32_t (&o)[16]) const {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const uint4 w = c[4 * hlf + j];
+            for (int j = 0; j < 2; ++j) {
+                const uint4 w = c[slot][2 * qtr + j];
                 e4m3x4_to_bf16(w.x, o[8 * j + 0], o[8 * j + 1]);
                 e4m3x4_to_bf16(w.y, o[8 * j + 2], o[8 * j + 3]);
                 e4m3x4_to_bf16(w.z, o[8 * j + 4], o[8 * j + 5]);

@@ -29,7 +29,7 @@
 //   warps 2-5     fold / epilogue, one per TMEM lane quadrant.
 //   warps 6-13    dequant, two groups of four warps taking alternate units:
 //                 shared memory -> registers -> exact BF16/FP16 -> tcgen05.st
-//                 into a 4-deep A ring in TMEM.
+//                 into a ring of A buffers in TMEM (6 deep at N=16, 4 at N=32).
 // The per-unit commit (accumulator ready) also frees the unit's A buffer and,
 // through the dequant group that next reuses that buffer, its X slice.
 //
@@ -56,9 +56,7 @@ constexpr int kWarpDeq0 = 6;
 constexpr int kWarpMma2 = 14;
 constexpr int kWarpXProd = 15;
 constexpr int kIssuers = 2;
-constexpr int kNA = 4;            // A buffers in TMEM (64 columns each) = accumulators
 constexpr int kTmemCols = 512;
-constexpr int kDCol0 = kNA * 64;  // accumulators at columns 256 + 32 a
 
 struct Params {
     // weights
@@ -76,8 +74,8 @@ struct Params {
     int KB;                       // units (128-wide K blocks) per tile
     long long U;                  // total units
     int G;                        // CTAs
-    uint32_t* cnt;                // per (tile, quadrant) arrival counters
-    float* part;                  // [G][2][128][NMMA] partial sums
+    float* part;                  // [G][2][128][NMMA] partial sums (scratch)
+    uint32_t* cnt;                // per (tile, quadrant) arrival counters, zero between calls
     uint64_t timeout_ns;
     int fault_unit;
     uint32_t* status;
@@ -86,9 +84,14 @@ struct Params {
 
 template <int NMMA, int WBYTES>
 struct Layout {
+    // A buffers in TMEM (64 columns each), one accumulator (NMMA columns) each:
+    // as many as fit in the 512 columns, an even number
+    static constexpr int kNA = NMMA == 16 ? 6 : 4;
+    static constexpr int kDCol0 = kNA * 64;               // accumulator a at kDCol0 + NMMA a
+    static_assert(kDCol0 + kNA * NMMA <= kTmemCols, "TMEM columns");
     static constexpr int kXSlot = NMMA * 256;             // two 64-element X boxes
     static constexpr int kXBox = NMMA * 128;
-    static constexpr int kXStages = 8;
+    static constexpr int kXStages = 2 * kNA;
     static constexpr int kWBudget = 212992 - kXStages * kXSlot;   // 208 KB in all
     // Even, so that every use of a weight stage falls to the same dequant group
     // (units i and i + kWStages have the same parity).  A group's parity wait
@@ -162,6 +165,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     using L = Layout<NMMA, F::kWBytes>;
     constexpr int kWStages = L::kWStages;
     constexpr int kXStages = L::kXStages;
+    constexpr int kNA = L::kNA;
+    constexpr int kDCol0 = L::kDCol0;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -272,7 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 // the descriptor's start-address field counts 16-byte units
                 const uint64_t xd = desc0 + static_cast<uint64_t>((s * L::kXSlot) >> 4);
-                const uint32_t dt = tmem + kDCol0 + a * 32;
+                const uint32_t dt = tmem + kDCol0 + a * NMMA;
                 const uint32_t at = tmem + a * 64;
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
@@ -321,8 +326,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!warp_wait(dfull(a), (i / kNA) & 1, wc)) break;
             tc_fence_after();
             uint32_t v0[16], v1[16];
-            tmem_ld_x16(tl + kDCol0 + a * 32, v0);
-            if constexpr (NMMA == 32) tmem_ld_x16(tl + kDCol0 + a * 32 + 16, v1);
+            tmem_ld_x16(tl + kDCol0 + a * NMMA, v0);
+            if constexpr (NMMA == 32) tmem_ld_x16(tl + kDCol0 + a * NMMA + 16, v1);
             tmem_wait_ld();
             tc_fence_before();
             __syncwarp();
@@ -366,32 +371,41 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int cf = unit_owner(t0, p.U, p.G);
                 const int cl = unit_owner(t0 + p.KB - 1, p.U, p.G);
                 if (static_cast<int>(prev) == cl - cf) {
-                    // Last piece to arrive: sum all pieces in ascending K order.
+                    // Last piece to arrive: sum all pieces in ascending K order,
+                    // this CTA's own piece included (just stored above), loading
+                    // kBatch pieces at a time so that their latencies overlap.
                     // A contributor's piece sits in its slot 0 when the tile is its
                     // first tile: true for every contributor after the first (their
                     // ranges start inside the tile), and for the first one only
                     // when its range starts exactly at the tile.
                     __threadfence();
                     const int w_first = unit_begin(cf, p.U, p.G) == t0 ? 0 : 1;
+                    constexpr int kBatch = NMMA == 16 ? 4 : 1;
                     float acc[NMMA];
 #pragma unroll
                     for (int m = 0; m < NMMA; ++m) acc[m] = 0.0f;
-                    for (int c2 = cf; c2 <= cl; ++c2) {
-                        float4* slot = reinterpret_cast<float4*>(p.part) +
-                                       ((static_cast<size_t>(c2) * 2 + (c2 == cf ? w_first : 0)) * 128 + row) * (NMMA / 4);
-                        float4 piece[NMMA / 4];
+                    for (int c0 = cf; c0 <= cl; c0 += kBatch) {
+                        float4 piece[kBatch][NMMA / 4];
 #pragma unroll
-                        for (int m4 = 0; m4 < NMMA / 4; ++m4)
-                            piece[m4] = c2 == cta ? make_float4(outer[4 * m4], outer[4 * m4 + 1], outer[4 * m4 + 2],
-                                                                outer[4 * m4 + 3])
-                                                  : __ldcg(slot + m4);
+                        for (int b = 0; b < kBatch; ++b) {
+                            const int c2 = c0 + b;
+                            if (c2 > cl) break;
+                            const float4* slot =
+                                reinterpret_cast<const float4*>(p.part) +
+                                ((static_cast<size_t>(c2) * 2 + (c2 == cf ? w_first : 0)) * 128 + row) * (NMMA / 4);
 #pragma unroll
-                        for (int m4 = 0; m4 < NMMA / 4; ++m4) {
-                            acc[4 * m4 + 0] = __fadd_rn(acc[4 * m4 + 0], piece[m4].x);
-                            acc[4 * m4 + 1] = __fadd_rn(acc[4 * m4 + 1], piece[m4].y);
-                            acc[4 * m4 + 2] = __fadd_rn(acc[4 * m4 + 2], piece[m4].z);
-                            acc[4 * m4 + 3] = __fadd_rn(acc[4 * m4 + 3], piece[m4].w);
-                            __stcg(slot + m4, make_float4(0.0f, 0.0f, 0.0f, 0.0f));   // leave the workspace zero-filled
+                            for (int m4 = 0; m4 < NMMA / 4; ++m4) piece[b][m4] = __ldcg(slot + m4);
+                        }
+#pragma unroll
+                        for (int b = 0; b < kBatch; ++b) {
+                            if (c0 + b > cl) break;
+#pragma unroll
+                            for (int m4 = 0; m4 < NMMA / 4; ++m4) {
+                                acc[4 * m4 + 0] = __fadd_rn(acc[4 * m4 + 0], piece[b][m4].x);
+                                acc[4 * m4 + 1] = __fadd_rn(acc[4 * m4 + 1], piece[b][m4].y);
+                                acc[4 * m4 + 2] = __fadd_rn(acc[4 * m4 + 2], piece[b][m4].z);
+                                acc[4 * m4 + 3] = __fadd_rn(acc[4 * m4 + 3], piece[b][m4].w);
+                            }
                         }
                     }
                     if (n < p.N) {
@@ -399,7 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int m = 0; m < NMMA; ++m)
                             if (m < p.M) F::store(p.Y, static_cast<int64_t>(m) * p.ldy + n, acc[m]);
                     }
-                    if (lane == 0) p.cnt[tile * 4 + q] = 0u;   // leave the workspace clean
+                    if (lane == 0) p.cnt[tile * 4 + q] = 0u;   // ready for the next call
                 }
             }
 #pragma unroll
@@ -412,21 +426,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row = q * 32 + lane;
         const uint32_t tl = tmem + (static_cast<uint32_t>(q * 32) << 16);
         typename F::Deq dq(p, u0, grp, nunits, row);
-        // one unit of this group; false when a wait gave up
-        auto unit = [&](int i, int slot) -> bool {
+        // The group's next unit is loaded from shared memory into the other
+        // register slot before the current one is converted, so the load
+        // latency overlaps the conversion.  Unit i's weights into `slot`:
+        auto issue = [&](int i, int slot) -> bool {
             const int s = i % kWStages;
-            const int a = i % kNA;
-            dq.prepare(p, u0, i, nunits, row, slot);
+            dq.prepare(p, i, nunits, row, slot);
             if (!warp_wait(wfull(s), (i / kWStages) & 1, wc)) return false;
-            dq.load(gbase + s * F::kWBytes, row);
-            // The weight stage is refilled as soon as it is released, so the
-            // release must not be performed before every lane's shared-memory
-            // loads have returned.  Program order alone does not ensure that: the
-            // arrive uses none of the loaded registers.  Its address is therefore
-            // made to depend on all of them, through a warp reduction of a word
-            // derived from each lane's loads and a zero known only at run time.
-            const uint32_t tok = __reduce_or_sync(0xffffffffu, dq.token());
-            if (lane == 0) mbar_arrive(wempty(s) + (tok & p.opaque_zero));
+            dq.load(slot, gbase + s * F::kWBytes, row);
+            return true;
+        };
+        // Unit i's weight stage is refilled as soon as it is released, so the
+        // release must not be performed before every lane's shared-memory loads
+        // have returned.  Program order alone does not ensure that: the arrive
+        // uses none of the loaded registers.  Its address is therefore made to
+        // depend on all of them, through a warp reduction of a word derived
+        // from each lane's loads and a zero known only at run time.
+        auto release = [&](int i, int slot) {
+            const uint32_t tok = __reduce_or_sync(0xffffffffu, dq.token(slot));
+            if (lane == 0) mbar_arrive(wempty(i % kWStages) + (tok & p.opaque_zero));
+        };
+        // unit i (already loaded into `slot`); false when a wait gave up
+        auto unit = [&](int i, int slot, int nslot) -> bool {
+            const int a = i % kNA;
+            const int inext = i + 2;
+            const bool more = inext < nunits;
+            if (more && !issue(inext, nslot)) return false;
             if (i >= kNA) {
                 // unit i - kNA (this group's) is fully consumed once its MMAs are
                 // done: its A buffer is ours again and its X slice can be refilled
@@ -436,26 +461,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             tc_fence_after();
 #pragma unroll
-            for (int hlf = 0; hlf < 2; ++hlf) {
-                uint32_t o[32];
-                dq.convert(hlf, o);
-                tmem_st_x32(tl + a * 64 + hlf * 32, o);
+            for (int qtr = 0; qtr < 4; ++qtr) {
+                uint32_t o[16];
+                dq.convert(slot, qtr, o);
+                tmem_st_x16(tl + a * 64 + qtr * 16, o);
             }
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(afull(a));
+            if (more) release(inext, nslot);
             return true;
         };
-        // unrolled by the dequantiser's look-ahead so that any per-unit value it
-        // prefetches lives in a fixed register slot (no moves that would wait)
-        constexpr int kAhead = F::Deq::kAhead;
-        bool ok = true;
-        for (int i0 = grp; i0 < nunits && ok; i0 += 2 * kAhead) {
+        // unrolled so that every register slot index is a constant (no moves
+        // between slots that would wait for a load)
+        constexpr int kU = F::Deq::kUnroll;
+        static_assert(kU % 2 == 0, "two register slots alternate");
+        bool ok = grp < nunits && issue(grp, 0);
+        if (ok) release(grp, 0);
+        for (int i0 = grp; i0 < nunits && ok; i0 += 2 * kU) {
 #pragma unroll
-            for (int j = 0; j < kAhead; ++j) {
+            for (int j = 0; j < kU; ++j) {
                 const int i = i0 + 2 * j;
-                if (i < nunits && ok) ok = unit(i, j);
+                if (i < nunits && ok) ok = unit(i, j, (j + 1) % kU);
             }
         }
     }
@@ -511,9 +539,8 @@ inline Params base_params(const Schedule& s, void* Y, int64_t ldy, int M, int N,
     p.U = s.U;
     p.G = s.G;
     uint8_t* w = static_cast<uint8_t*>(ws);
-    const size_t cnt_bytes = (static_cast<size_t>(s.T) * 4 * sizeof(uint32_t) + 255) & ~static_cast<size_t>(255);
-    p.cnt = reinterpret_cast<uint32_t*>(w);
-    p.part = w ? reinterpret_cast<float*>(w + cnt_bytes) : nullptr;
+    p.part = reinterpret_cast<float*>(w);
+    p.cnt = w ? reinterpret_cast<uint32_t*>(w + workspace_partial_bytes(s)) : nullptr;
     p.timeout_ns = c.timeout_ns;
     p.fault_unit = c.fault_unit;
     p.status = c.status;

@@ -20,10 +20,20 @@ struct Schedule {
     long long U = 0;  // T * KU
     int G = 0;        // CTAs
     int nmma = 16;    // MMA N (16 or 32)
+    int max_ctas = 0; // CTAs the device holds at once (one per SM): bounds G
 };
 
-// Workspace layout for a schedule: per-tile counters, then per-CTA partials.
-size_t workspace_bytes(const Schedule& s);
+// Workspace layout for a schedule that splits tiles: split-K partial sums
+// (scratch; two slots per CTA), sized for the largest grid and MMA width the
+// device runs, so that the arrival counters behind them sit at the same
+// offset for every shape and never overlap another shape's partial sums;
+// then 4 arrival counters per tile, which are zero between calls.
+size_t workspace_partial_bytes(const Schedule& s);   // = offset of the counters
+size_t workspace_bytes(const Schedule& s);           // 0 when no tile is split
+
+// Offset and size of the arrival counters of a call (0, 0 when it needs no
+// workspace), for callers that must clear them.
+void workspace_counters(int kind, int M, int N, int K, size_t* offset, size_t* bytes);
 
 struct Fp8Args {
     const void* X;

@@ -37,16 +37,19 @@ struct Lut3Fmt {
     }
 
     // One thread dequantises one weight row (128 codes, one scale group) of a
-    // unit.  The thread's scale for a unit is fetched kAhead of its units in
-    // advance into a fixed slot of scq (the caller unrolls its loop by kAhead),
-    // so the load latency stays off the dequant.
+    // unit.  The thread's scale for a unit is fetched kUnroll of its units in
+    // advance into a fixed slot of scq (the caller unrolls its loop by
+    // kUnroll), so the load latency stays off the dequant.  Codes and the
+    // scaled table have two register slots (slot & 1): the pipeline loads the
+    // group's next unit into one while it converts the current unit from the
+    // other.
     struct Deq {
-        static constexpr int kAhead = 4;
+        static constexpr int kUnroll = 4;
         uint4 qm;
-        uint4 c[4];
-        uint32_t sc;
-        uint32_t scq[kAhead];
-        LutPlanes t;
+        uint4 c[2][4];
+        uint32_t sc[2];
+        uint32_t scq[kUnroll];
+        LutPlanes t[2];
         gemm::Cursor ahead;   // the unit whose scale is fetched next
         __device__ static uint32_t scale_of(const gemm::Params& p, const gemm::Cursor& c, int row) {
             const int n = c.tile * 128 + row;
@@ -54,49 +57,51 @@ struct Lut3Fmt {
                            : 0u;
         }
         // this thread handles units grp, grp + 2, grp + 4, ...; slot j holds the
-        // scale of its j-th unit modulo kAhead
+        // scale of its j-th unit modulo kUnroll
         __device__ Deq(const gemm::Params& p, long long u0, int grp, int nunits, int row)
             : qm(__ldg(p.qmap)), ahead(u0 + grp, p.KB) {
 #pragma unroll
-            for (int j = 0; j < kAhead; ++j) {
+            for (int j = 0; j < kUnroll; ++j) {
                 const int i = grp + 2 * j;
                 scq[j] = i < nunits ? scale_of(p, ahead, row) : 0u;
                 ahead.step(2, p.KB);
             }
         }
-        __device__ void prepare(const gemm::Params& p, long long, int i, int nunits, int row, int slot) {
-            sc = scq[slot];
-            const int inext = i + 2 * kAhead;
+        // called for each of the group's units in order, just before load()
+        __device__ void prepare(const gemm::Params& p, int i, int nunits, int row, int slot) {
+            sc[slot & 1] = scq[slot];
+            const int inext = i + 2 * kUnroll;
             scq[slot] = inext < nunits ? scale_of(p, ahead, row) : 0u;
             ahead.step(2, p.KB);
         }
-        __device__ void load(const uint8_t* stage, int row) {
+        __device__ void load(int slot, const uint8_t* stage, int row) {
+            const int b = slot & 1;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) c[j] = *reinterpret_cast<const uint4*>(stage + ((j * 128 + row) << 4));
-            const uint32_t sc2 = sc | (sc << 16);
-            t = lut_planes(f16x2_mul(qm.x, sc2), f16x2_mul(qm.y, sc2), f16x2_mul(qm.z, sc2), f16x2_mul(qm.w, sc2));
+            for (int j = 0; j < 4; ++j) c[b][j] = *reinterpret_cast<const uint4*>(stage + ((j * 128 + row) << 4));
+            const uint32_t sc2 = sc[b] | (sc[b] << 16);
+            t[b] = lut_planes(f16x2_mul(qm.x, sc2), f16x2_mul(qm.y, sc2), f16x2_mul(qm.z, sc2),
+                              f16x2_mul(qm.w, sc2));
         }
-        // a value that depends on every loaded word (the pipeline releases the
-        // weight stage only through it)
-        __device__ uint32_t token() const {
+        // a value that depends on every loaded word of the slot (the pipeline
+        // releases the weight stage only through it)
+        __device__ uint32_t token(int slot) const {
+            const int b = slot & 1;
             uint32_t d = 0;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) d ^= c[j].x ^ c[j].y ^ c[j].z ^ c[j].w;
+            for (int j = 0; j < 4; ++j) d ^= c[b][j].x ^ c[b][j].y ^ c[b][j].z ^ c[b][j].w;
             return d;
         }
-        // columns 32*hlf .. 32*hlf+31 of the row's A fragment (K 64*hlf .. 64*hlf+63)
-        __device__ void convert(int hlf, uint32_t (&o)[32]) const {
+        // columns 16*qtr .. 16*qtr+15 of the row's A fragment (K 32*qtr .. 32*qtr+31)
+        __device__ void convert(int slot, int qtr, uint32_t (&o)[16]) const {
+            const int b = slot & 1;
+            const uint4 cw = c[b][qtr];
+            const uint32_t w4[4] = {cw.x, cw.y, cw.z, cw.w};
 #pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const uint4 cw = c[2 * hlf + j];
-                const uint32_t w4[4] = {cw.x, cw.y, cw.z, cw.w};
+            for (int w = 0; w < 4; ++w) {
+                uint32_t r4[4];
+                lut3x8_to_f16(w4[w], t[b], r4);
 #pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                    uint32_t r4[4];
-                    lut3x8_to_f16(w4[w], t, r4);
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) o[16 * j + 4 * w + e] = r4[e];
-                }
+                for (int e = 0; e < 4; ++e) o[4 * w + e] = r4[e];
             }
         }
     };

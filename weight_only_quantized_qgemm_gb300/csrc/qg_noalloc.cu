@@ -48,8 +48,13 @@ extern "C" qg_status qgemm_fp8_block_noalloc(const void* X, int64_t ldx, const u
     if (need > qg::kNoAllocScratchBytes) return QG_ERR_WORKSPACE;
     void* scratch = qg::scratch_on_current_device();
     if (!scratch) return QG_ERR_CUDA;
-    // The array keeps whatever the previous call left; the arrival counters
-    // must start at zero, so the part this call uses is cleared first.
-    if (need > 0 && cudaMemsetAsync(scratch, 0, need, stream) != cudaSuccess) return QG_ERR_CUDA;
+    // The array keeps whatever the previous call left (a call that timed out
+    // leaves its arrival counters set); the counters must start at zero, so
+    // this call's are cleared first.  The partial sums need no clearing.
+    size_t cnt_off = 0, cnt_bytes = 0;
+    qg::workspace_counters(QG_KIND_FP8_BLOCK, M, N, K, &cnt_off, &cnt_bytes);
+    if (cnt_bytes > 0 &&
+        cudaMemsetAsync(static_cast<unsigned char*>(scratch) + cnt_off, 0, cnt_bytes, stream) != cudaSuccess)
+        return QG_ERR_CUDA;
     return qgemm_fp8_block(X, ldx, W, W_scale, Y, ldy, M, N, K, scratch, qg::kNoAllocScratchBytes, stream);
 }
