@@ -31,6 +31,13 @@ __device__ __forceinline__ void raise_abort(const WaitCtl& c, uint32_t code) {
 }
 
 // ----------------------------------------------------------------- smem / mbarrier
+// True in exactly one active lane of the (converged) warp.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t e;
+    asm volatile("{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}" : "=r"(e));
+    return e != 0;
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

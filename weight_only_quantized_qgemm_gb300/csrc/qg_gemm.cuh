@@ -22,10 +22,10 @@
 //                 until the unit's MMAs complete.
 //   warps 1,14    MMA issuers, unit i taken by issuer i % 2: 8 tcgen05.mma
 //                 kind::f16 (M=128, N=16|32, K=16), A from TMEM, B (X) from
-//                 shared memory, then one tcgen05.commit.  A single thread
-//                 gets an MMA accepted only every ~55-120 cycles, while the
-//                 tensor core takes one every ~30 at this shape, so two issuers
-//                 keep it ahead of the memory stream.
+//                 shared memory, then one tcgen05.commit, from one elected
+//                 lane.  A single issuing thread gets an MMA accepted only
+//                 every ~55-120 cycles, while the tensor core takes one every
+//                 ~30 at this shape, so two issuers share the units.
 //   warps 2-5     fold / epilogue, one per TMEM lane quadrant.
 //   warps 6-13    dequant, two groups of four warps taking alternate units:
 //                 shared memory -> registers -> exact BF16/FP16 -> tcgen05.st
@@ -263,7 +263,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1 || warp == kWarpMma2) {
         // ------------------------------------------------------------ MMA issuers
-        if (lane == 0) {
+        // The whole warp runs the loop and its waits (the per-unit values stay
+        // warp-uniform); one elected lane issues the MMAs and the commit.  This
+        // issues measurably faster than a loop confined to lane 0.
+        {
+            const bool elected = elect_one();
             const int first = warp == 1 ? 0 : 1;
             constexpr uint32_t idesc = idesc_f16(NMMA, F::kBf16);
             const uint64_t desc0 = smem_desc_sw128(base + L::kXOff);
@@ -271,22 +275,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = first; i < nunits; i += kIssuers) {
                 const int s = i % kXStages;
                 const int a = i % kNA;
-                if (!wait_bounded(xfull(s), (i / kXStages) & 1, wc)) break;
-                if (!wait_bounded(afull(a), (i / kNA) & 1, wc)) break;
-                if (i >= kNA && !wait_bounded(dempty(a), ((i / kNA) - 1) & 1, wc)) break;
+                if (!warp_wait(xfull(s), (i / kXStages) & 1, wc)) break;
+                if (!warp_wait(afull(a), (i / kNA) & 1, wc)) break;
+                if (i >= kNA && !warp_wait(dempty(a), ((i / kNA) - 1) & 1, wc)) break;
                 tc_fence_after();
                 // the descriptor's start-address field counts 16-byte units
                 const uint64_t xd = desc0 + static_cast<uint64_t>((s * L::kXSlot) >> 4);
                 const uint32_t dt = tmem + kDCol0 + a * NMMA;
                 const uint32_t at = tmem + a * 64;
+                if (elected) {
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    mma_ts_f16(dt, at + j * 8, xd + (((j >> 2) * L::kXBox + (j & 3) * 32) >> 4), idesc,
-                               j > 0 ? 1u : 0u);
-                tc_commit(dfull(a));
+                    for (int j = 0; j < 8; ++j)
+                        mma_ts_f16(dt, at + j * 8, xd + (((j >> 2) * L::kXBox + (j & 3) * 32) >> 4), idesc,
+                                   j > 0 ? 1u : 0u);
+                    tc_commit(dfull(a));
+                }
+                __syncwarp();
                 last = i;
             }
-            if (last >= 0) drain_wait(dfull(last % kNA), (last / kNA) & 1, p.timeout_ns);
+            if (last >= 0 && elected) drain_wait(dfull(last % kNA), (last / kNA) & 1, p.timeout_ns);
         }
     } else if (warp < kWarpDeq0) {
         // ------------------------------------------------------------ fold / epilogue
@@ -294,6 +301,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row = q * 32 + lane;
         const uint32_t tl = tmem + (static_cast<uint32_t>(q * 32) << 16);
         const int first_tile = static_cast<int>(u0 / p.KB);
+        // A CTA ends a split piece only in its first and its last tile.  For
+        // both, the first and last contributing CTAs (cf, cl) and the slot
+        // holding cf's piece (slot 0 when the tile is cf's first tile, i.e. when
+        // cf's range starts exactly at the tile; every later contributor's range
+        // starts inside the tile, so their pieces are all in slot 0) are worked
+        // out here, before any unit is ready, so that the 64-bit divisions stay
+        // out of the reduction.  Lane 3w + k holds value k (cf, cl, slot) of the
+        // first (w = 0) or last (w = 1) tile; the reduction fetches them by shuffle.
+        int split_info = 0;
+        if (lane < 6) {
+            const long long t = lane < 3 ? u0 / p.KB : (u1 - 1) / p.KB;
+            const long long t0 = t * p.KB;
+            const int cf = unit_owner(t0, p.U, p.G);
+            if (lane % 3 == 0) split_info = cf;
+            if (lane % 3 == 1) split_info = unit_owner(t0 + p.KB - 1, p.U, p.G);
+            if (lane % 3 == 2) split_info = unit_begin(cf, p.U, p.G) == t0 ? 0 : 1;
+        }
         // Y and the workspace may still be in use by the preceding grid
         grid_dependency_wait();
         float outer[NMMA];
@@ -367,19 +391,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t prev = 0;
                 if (lane == 0) prev = atomicAdd(p.cnt + tile * 4 + q, 1u);
                 prev = __shfl_sync(0xffffffffu, prev, 0);
-                const long long t0 = static_cast<long long>(tile) * p.KB;
-                const int cf = unit_owner(t0, p.U, p.G);
-                const int cl = unit_owner(t0 + p.KB - 1, p.U, p.G);
+                const int cf = __shfl_sync(0xffffffffu, split_info, 3 * which);
+                const int cl = __shfl_sync(0xffffffffu, split_info, 3 * which + 1);
+                const int w_first = __shfl_sync(0xffffffffu, split_info, 3 * which + 2);
                 if (static_cast<int>(prev) == cl - cf) {
                     // Last piece to arrive: sum all pieces in ascending K order,
                     // this CTA's own piece included (just stored above), loading
                     // kBatch pieces at a time so that their latencies overlap.
-                    // A contributor's piece sits in its slot 0 when the tile is its
-                    // first tile: true for every contributor after the first (their
-                    // ranges start inside the tile), and for the first one only
-                    // when its range starts exactly at the tile.
                     __threadfence();
-                    const int w_first = unit_begin(cf, p.U, p.G) == t0 ? 0 : 1;
                     constexpr int kBatch = NMMA == 16 ? 4 : 1;
                     float acc[NMMA];
 #pragma unroll
