@@ -485,11 +485,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 dq.convert(slot, qtr, o);
                 tmem_st_x16(tl + a * 64 + qtr * 16, o);
             }
+            // the next unit's stage is released while the TMEM stores complete
+            if (more) release(inext, nslot);
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(afull(a));
-            if (more) release(inext, nslot);
             return true;
         };
         // unrolled so that every register slot index is a constant (no moves
