@@ -48,15 +48,6 @@ struct Fp8Fmt {
             for (int j = 0; j < 8; ++j)
                 c[slot][j] = *reinterpret_cast<const uint4*>(wrow + ((j ^ (row & 7)) << 4));
         }
-        // a value that depends on every shared-memory load of the slot (one word
-        // of each 16-byte load, which completes as a whole); the pipeline
-        // releases the weight stage only through it
-        __device__ uint32_t token(int slot) const {
-            uint32_t d = 0;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) d ^= c[slot][j].x;
-            return d;
-        }
         // columns 16*qtr .. 16*qtr+15 of the row's A fragment (K 32*qtr .. 32*qtr+31)
         __device__ void convert(int slot, int qtr, uint32_t (&o)[16]) const {
 #pragma unroll

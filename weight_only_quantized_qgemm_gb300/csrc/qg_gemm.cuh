@@ -30,8 +30,8 @@
 //   warps 6-13    dequant, two groups of four warps taking alternate units:
 //                 shared memory -> registers -> exact BF16/FP16 -> tcgen05.st
 //                 into a ring of A buffers in TMEM (6 deep at N=16, 4 at N=32).
-// The per-unit commit (accumulator ready) also frees the unit's A buffer and,
-// through the dequant group that next reuses that buffer, its X slice.
+// The per-unit commits free the unit's X slice (to the X producer) and mark
+// its accumulator ready, which also frees its A buffer for the dequant group.
 //
 // Work units are split evenly over the CTAs in tile-major order (stream-K);
 // a tile shared by several CTAs is summed, in ascending K order of its
@@ -79,7 +79,6 @@ struct Params {
     uint64_t timeout_ns;
     int fault_unit;
     uint32_t* status;
-    uint32_t opaque_zero;         // always 0; the compiler cannot know that
 };
 
 template <int NMMA, int WBYTES>
@@ -106,7 +105,7 @@ struct Layout {
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     static constexpr int kSmemBytes = kMiscOff + 64 + 1024;  // + alignment slack
     static_assert(WBYTES % 1024 == 0 && kXSlot % 1024 == 0, "keep the 1024-byte swizzle alignment");
-    static_assert(kXStages >= 2 * kNA, "X slices are held until the unit kNA later is dequantised");
+    static_assert(kXStages >= kNA, "X copies run at least as far ahead as the dequant");
     // the same ownership rule for the other rings: an X stage and an A/D buffer
     // are always used by the same MMA issuer and the same dequant group
     static_assert(kXStages % kIssuers == 0 && kNA % kIssuers == 0 && kNA % 2 == 0, "ring ownership");
@@ -198,7 +197,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int s = 0; s < kXStages; ++s) {
             mbar_init(xfull(s), 1);
-            mbar_init(xempty(s), 4);   // the dequant group that saw the unit's MMAs complete
+            mbar_init(xempty(s), 1);   // a commit: the unit's MMAs are complete
         }
         for (int a = 0; a < kNA; ++a) {
             mbar_init(afull(a), 4);
@@ -288,12 +287,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int j = 0; j < 8; ++j)
                         mma_ts_f16(dt, at + j * 8, xd + (((j >> 2) * L::kXBox + (j & 3) * 32) >> 4), idesc,
                                    j > 0 ? 1u : 0u);
+                    // the X slot returns to the producer the moment these MMAs
+                    // complete, so the copies run as far ahead as the ring allows
+                    tc_commit(xempty(s));
                     tc_commit(dfull(a));
                 }
                 __syncwarp();
                 last = i;
             }
-            if (last >= 0 && elected) drain_wait(dfull(last % kNA), (last / kNA) & 1, p.timeout_ns);
+            if (last >= 0 && elected) {
+                drain_wait(xempty(last % kXStages), (last / kXStages) & 1, p.timeout_ns);
+                drain_wait(dfull(last % kNA), (last / kNA) & 1, p.timeout_ns);
+            }
         }
     } else if (warp < kWarpDeq0) {
         // ------------------------------------------------------------ fold / epilogue
@@ -455,28 +460,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             dq.load(slot, gbase + s * F::kWBytes, row);
             return true;
         };
-        // Unit i's weight stage is refilled as soon as it is released, so the
-        // release must not be performed before every lane's shared-memory loads
-        // have returned.  Program order alone does not ensure that: the arrive
-        // uses none of the loaded registers.  Its address is therefore made to
-        // depend on all of them, through a warp reduction of a word derived
-        // from each lane's loads and a zero known only at run time.
-        auto release = [&](int i, int slot) {
-            const uint32_t tok = __reduce_or_sync(0xffffffffu, dq.token(slot));
-            if (lane == 0) mbar_arrive(wempty(i % kWStages) + (tok & p.opaque_zero));
-        };
         // unit i (already loaded into `slot`); false when a wait gave up
         auto unit = [&](int i, int slot, int nslot) -> bool {
             const int a = i % kNA;
             const int inext = i + 2;
             const bool more = inext < nunits;
             if (more && !issue(inext, nslot)) return false;
-            if (i >= kNA) {
-                // unit i - kNA (this group's) is fully consumed once its MMAs are
-                // done: its A buffer is ours again and its X slice can be refilled
-                if (!warp_wait(dfull(a), ((i - kNA) / kNA) & 1, wc)) return false;
-                if (lane == 0) mbar_arrive(xempty((i - kNA) % kXStages));
-            }
+            // unit i - kNA (this group's) is done with its A buffer once its MMAs are
+            if (i >= kNA && !warp_wait(dfull(a), ((i - kNA) / kNA) & 1, wc)) return false;
             __syncwarp();
             tc_fence_after();
 #pragma unroll
@@ -485,8 +476,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 dq.convert(slot, qtr, o);
                 tmem_st_x16(tl + a * 64 + qtr * 16, o);
             }
-            // the next unit's stage is released while the TMEM stores complete
-            if (more) release(inext, nslot);
+            // Unit i's weight stage is refilled as soon as it is released, so the
+            // release must not be performed before every lane's shared-memory
+            // loads of it have returned.  It comes after the TMEM stores of the
+            // converted weights, which need those loads: both the stores and the
+            // arrive are ordered memory operations (neither the compiler nor the
+            // in-order issue can put the arrive first), and a store cannot issue
+            // before the registers it reads are written.
+            __syncwarp();
+            if (lane == 0) mbar_arrive(wempty(i % kWStages));
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
@@ -498,7 +496,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         constexpr int kU = F::Deq::kUnroll;
         static_assert(kU % 2 == 0, "two register slots alternate");
         bool ok = grp < nunits && issue(grp, 0);
-        if (ok) release(grp, 0);
         for (int i0 = grp; i0 < nunits && ok; i0 += 2 * kU) {
 #pragma unroll
             for (int j = 0; j < kU; ++j) {
@@ -564,7 +561,6 @@ inline Params base_params(const Schedule& s, void* Y, int64_t ldy, int M, int N,
     p.timeout_ns = c.timeout_ns;
     p.fault_unit = c.fault_unit;
     p.status = c.status;
-    p.opaque_zero = 0;
     return p;
 }
 

@@ -82,16 +82,6 @@ struct Lut3Fmt {
             t[b] = lut_planes(f16x2_mul(qm.x, sc2), f16x2_mul(qm.y, sc2), f16x2_mul(qm.z, sc2),
                               f16x2_mul(qm.w, sc2));
         }
-        // a value that depends on every shared-memory load of the slot (one word
-        // of each 16-byte load, which completes as a whole); the pipeline
-        // releases the weight stage only through it
-        __device__ uint32_t token(int slot) const {
-            const int b = slot & 1;
-            uint32_t d = 0;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) d ^= c[b][j].x;
-            return d;
-        }
         // columns 16*qtr .. 16*qtr+15 of the row's A fragment (K 32*qtr .. 32*qtr+31)
         __device__ void convert(int slot, int qtr, uint32_t (&o)[16]) const {
             const int b = slot & 1;
