@@ -30,8 +30,9 @@
 //   warps 6-13    dequant, two groups of four warps taking alternate units:
 //                 shared memory -> registers -> exact BF16/FP16 -> tcgen05.st
 //                 into a ring of A buffers in TMEM (6 deep at N=16, 4 at N=32).
-// The per-unit commits free the unit's X slice (to the X producer) and mark
-// its accumulator ready, which also frees its A buffer for the dequant group.
+// The per-unit commit marks the unit's accumulator ready, which also frees its
+// A buffer for the dequant group; the first fold warp to see it then returns
+// the unit's X slot to the X producer.
 //
 // Work units are split evenly over the CTAs in tile-major order (stream-K);
 // a tile shared by several CTAs is summed, in ascending K order of its
@@ -197,7 +198,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int s = 0; s < kXStages; ++s) {
             mbar_init(xfull(s), 1);
-            mbar_init(xempty(s), 1);   // a commit: the unit's MMAs are complete
+            mbar_init(xempty(s), 1);   // fold warp 2, once the unit's MMAs are complete
         }
         for (int a = 0; a < kNA; ++a) {
             mbar_init(afull(a), 4);
@@ -287,18 +288,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int j = 0; j < 8; ++j)
                         mma_ts_f16(dt, at + j * 8, xd + (((j >> 2) * L::kXBox + (j & 3) * 32) >> 4), idesc,
                                    j > 0 ? 1u : 0u);
-                    // the X slot returns to the producer the moment these MMAs
-                    // complete, so the copies run as far ahead as the ring allows
-                    tc_commit(xempty(s));
                     tc_commit(dfull(a));
                 }
                 __syncwarp();
                 last = i;
             }
-            if (last >= 0 && elected) {
-                drain_wait(xempty(last % kXStages), (last / kXStages) & 1, p.timeout_ns);
-                drain_wait(dfull(last % kNA), (last / kNA) & 1, p.timeout_ns);
-            }
+            if (last >= 0 && elected) drain_wait(dfull(last % kNA), (last / kNA) & 1, p.timeout_ns);
         }
     } else if (warp < kWarpDeq0) {
         // ------------------------------------------------------------ fold / epilogue
@@ -361,6 +356,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(dempty(a));
+            // the unit's MMAs are complete, so its X slot can be refilled (one
+            // arrival suffices; a commit in the MMA stream would cost about as
+            // much as another MMA)
+            if (warp == kWarpFold0 && lane == 0) mbar_arrive(xempty(i % kXStages));
 #pragma unroll
             for (int m = 0; m < 16; ++m) outer[m] = F::fold(outer[m], __uint_as_float(v0[m]), sc);
             if constexpr (NMMA == 32) {
