@@ -91,7 +91,9 @@ struct Layout {
     static_assert(kDCol0 + kNA * NMMA <= kTmemCols, "TMEM columns");
     static constexpr int kXSlot = NMMA * 256;             // two 64-element X boxes
     static constexpr int kXBox = NMMA * 128;
-    static constexpr int kXStages = 2 * kNA;
+    // X slots: as many as leave the weight ring 8 stages (the X copies then run
+    // far enough ahead of the MMA to hide their latency behind the weight stream)
+    static constexpr int kXStages = (NMMA == 16 ? 3 : 2) * kNA;
     static constexpr int kWBudget = 212992 - kXStages * kXSlot;   // 208 KB in all
     // Even, so that every use of a weight stage falls to the same dequant group
     // (units i and i + kWStages have the same parity).  A group's parity wait
