@@ -285,12 +285,9 @@ qg_status qgemm_fp8_block(const void* X, int64_t ldx, const uint8_t* W, const fl
     const size_t need = workspace_bytes(s);
     if (need > 0 && (!workspace || workspace_bytes_ < need || (reinterpret_cast<uintptr_t>(workspace) & 255u)))
         return QG_ERR_WORKSPACE;
-    CUtensorMap tmW, tmX;
+    CUtensorMap tmW;
     if (!make_tmap(&tmW, W, CU_TENSOR_MAP_DATA_TYPE_UINT8, static_cast<uint64_t>(K), static_cast<uint64_t>(N),
                    static_cast<uint64_t>(K), 128, 128))
-        return QG_ERR_CUDA;
-    if (!make_tmap(&tmX, X, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<uint64_t>(K), static_cast<uint64_t>(M),
-                   static_cast<uint64_t>(ldx) * 2, 64, static_cast<uint32_t>(s.nmma)))
         return QG_ERR_CUDA;
     Fp8Args a;
     a.X = X;
@@ -304,7 +301,7 @@ qg_status qgemm_fp8_block(const void* X, int64_t ldx, const uint8_t* W, const fl
     a.N = N;
     a.K = K;
     a.ws = need > 0 ? workspace : nullptr;
-    return launch_fp8(a, s, tmW, tmX, launch_ctl(d), stream) == cudaSuccess ? QG_OK : QG_ERR_CUDA;
+    return launch_fp8(a, s, tmW, launch_ctl(d), stream) == cudaSuccess ? QG_OK : QG_ERR_CUDA;
 }
 
 qg_status qgemm_lut3(const void* X, int64_t ldx, const void* Wq, const void* qmap, const void* scales, void* Y,

@@ -146,6 +146,19 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
         : "memory");
 }
 
+// 16-byte copy global -> shared through the load/store path (not the TMA
+// engine), completion tracked per thread by commit groups.  src_bytes = 0
+// reads nothing and fills zeros.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Waits until at most n of this thread's committed groups are still pending.
+template <int n>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(n) : "memory");
+}
+
 // ----------------------------------------------------------------- tcgen05
 __device__ __forceinline__ void tmem_alloc(uint32_t slot_smem, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_smem),
@@ -173,6 +186,17 @@ __device__ __forceinline__ void mma_ts_f16(uint32_t d_tmem, uint32_t a_tmem, uin
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
         "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// D[tmem] (+)= A[smem] x B[smem]^T, kind::f8f6f4 (E4M3 x E4M3 products, FP32
+// accumulate); both operands through shared-memory descriptors.
+__device__ __forceinline__ void mma_ss_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
@@ -225,12 +249,40 @@ __device__ __forceinline__ void tmem_ld_x16(uint32_t taddr, uint32_t (&r)[16]) {
         : "memory");
 }
 
+__device__ __forceinline__ void tmem_ld_x32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+        "%12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, "
+        "%30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
+          "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
+          "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+
+// Generic-proxy shared-memory writes become visible to the async proxy
+// (tensor core, TMA) once the writer has executed this fence.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // Instruction descriptor of tcgen05.mma kind::f16: FP32 accumulator, A and B
 // K-major, M = 128, N = n; ab_bf16 selects BF16 (else FP16) for both A and B.
 __host__ __device__ constexpr uint32_t idesc_f16(int n, bool ab_bf16) {
     return (1u << 4)                              // D format: F32
            | ((ab_bf16 ? 1u : 0u) << 7)           // A format
            | ((ab_bf16 ? 1u : 0u) << 10)          // B format
+           | (static_cast<uint32_t>(n >> 3) << 17)  // N >> 3
+           | (static_cast<uint32_t>(128 >> 4) << 24);  // M >> 4
+}
+
+// Instruction descriptor of tcgen05.mma kind::f8f6f4: FP32 accumulator, A and
+// B both E4M3 (format code 0) and K-major, M = 128, N = n.
+__host__ __device__ constexpr uint32_t idesc_f8_e4m3(int n) {
+    return (1u << 4)                              // D format: F32
            | (static_cast<uint32_t>(n >> 3) << 17)  // N >> 3
            | (static_cast<uint32_t>(128 >> 4) << 24);  // M >> 4
 }
@@ -289,6 +341,37 @@ __device__ __forceinline__ void e4m3x4_to_bf16(uint32_t r, uint32_t& lo, uint32_
     const uint32_t p1 = prmt(r, 0u, 0xB3A2u);  // [sgn(c3) | c3 | sgn(c2) | c2]
     lo = bf16x2_mul(mul_lo_u32(p0, 16u) & kKeep, kTwo120);
     hi = bf16x2_mul(mul_lo_u32(p1, 16u) & kKeep, kTwo120);
+}
+
+// ---- activation split for the E4M3 tensor-core path
+// Per-halfword unsigned maximum (used on |x| bit patterns, which order like
+// the magnitudes they encode).
+__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// Two BF16 values x0 (low half of xw) and x1, already scaled by a power of
+// two so that |x| < 256, become a high and a low E4M3 pair with
+//   x = hi + lo / 16
+// exactly whenever |x| >= 2^-6 (and to within 2^-14 below that):
+//  - x is exact in FP16 (8 significant bits, |x| < 256),
+//  - hi = E4M3 round-to-nearest-even of x (4 significant bits),
+//  - x - hi is exact in FP16 and, as a multiple of x's BF16 quantum no larger
+//    than half of hi's quantum, has at most 3 significant bits; times 16 it is
+//    an E4M3 value whenever hi is a normal E4M3 number.
+// Low byte of each result = element 0.
+__device__ __forceinline__ void split_e4m3x2(uint32_t xw, uint16_t& hi, uint16_t& lo) {
+    const float f0 = __uint_as_float(xw << 16);
+    const float f1 = __uint_as_float(xw & 0xFFFF0000u);
+    uint32_t h2, hh, d;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(h2) : "f"(f1), "f"(f0));
+    asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(hi) : "r"(h2));
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(hh) : "h"(hi));
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(h2), "r"(hh));
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(d), "r"(0x4C004C00u));   // x 16
+    asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(lo) : "r"(d));
 }
 
 // Byte planes of an 8-entry FP16 table e[0..7] given as four FP16x2 words

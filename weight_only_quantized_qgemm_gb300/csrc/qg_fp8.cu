@@ -1,76 +1,459 @@
-// W8A16 FP8 block-scaled format for the decode GEMM pipeline (qg_gemm.cuh).
+// W8A16 FP8 block-scaled decode GEMM for sm_103a.
 //
 //   Y[m, n] = bf16( sum_kb  s[n/128, kb] * ( sum_{k in kb} x[m,k] * e4m3(W[n,k]) ) )
 //
 // The two-level fold ("atlas" m16_tc module page, section NUMERICS): each
 // 128-wide K block is reduced on the tensor core into its own FP32
 // accumulator, then multiplied by that block's FP32 scale once and added to an
-// FP32 outer accumulator held in registers.  Weights stream as 128 x 128 E4M3
-// tiles through a 2-D TMA map with the 128-byte swizzle (one row per lane is
-// then read conflict-free) and become BF16 exactly in registers; the scale is
-// never applied to individual weights.
+// FP32 outer accumulator held in registers.
+//
+// The weights are never converted.  A 128 x 128 E4M3 tile goes from HBM to
+// shared memory by TMA (128-byte swizzle, the tensor core's K-major layout)
+// and is the A operand of tcgen05.mma kind::f8f6f4 as it is.  The activations
+// are the ones turned into E4M3: for each (row m, K block) a power of two 2^e
+// brings max |x| into [128, 256), and every scaled x splits into two E4M3
+// values, x * 2^e = hi + lo / 16, exact for every element within 2^13 of the
+// row's block maximum (below that the error is at most 2^-14 * 2^-e, under
+// 2^-21 of the block's largest |x|; see split_e4m3x2).  The hi and lo planes
+// are the MMA's B rows 0..NX-1 and NX..2NX-1 (swap-AB: the 128 weight rows
+// are the MMA's M side, the activation rows its narrow N side), so one MMA
+// pass of N = 2 NX gives both partial sums; every product is exact in the
+// tensor core and accumulates in FP32.  The fold then forms
+//   inner[m] = (hi_sum[m] + lo_sum[m] / 16) * 2^-e[m]
+// and adds inner[m] * s to the outer accumulator: the same two-level fold,
+// with the block sum taken in a different order.
+//
+// One persistent CTA per SM, 480 threads (15 warps):
+//   warp 0       weight producer: one 16 KB TMA tile per unit (evict-first)
+//                into a ring of 10 (NX = 16) / 8 (NX = 32) stages.
+//   warps 1, 2   MMA issuers, alternate units: 4 tcgen05.mma kind::f8f6f4
+//                (M = 128, N = 2 NX, K = 32) from one lane, then commits
+//                that free the unit's weight stage and X planes and mark its
+//                accumulator ready once the MMAs complete.
+//   warps 3-6    fold / epilogue, one per TMEM lane quadrant (warp % 4).
+//   warps 7-14   X split, two groups of four warps taking alternate units.
+//                Each thread copies its own share of a unit's BF16 X slice
+//                several units ahead (cp.async through the load/store path: a
+//                TMA copy would queue behind the weight tiles already in
+//                flight and arrive microseconds later), takes the row maxima
+//                and exponents of its group's next unit while it converts the
+//                current one, and writes the hi/lo E4M3 planes in the
+//                swizzled K-major layout, 2^-e per row beside them.
+// A unit is 128 weight rows x one 128-wide K block.  The schedule (tiles of
+// 128 rows, split-K pieces, last-arriver reduction) is the shared one of
+// qg_gemm.cuh.
 #include "qg_gemm.cuh"
 
 namespace qg {
 namespace {
 
-struct Fp8Fmt {
-    static constexpr int kWBytes = 128 * 128;
-    static constexpr bool kBf16 = true;
-    static constexpr bool kUsesTensorMapW = true;
+using gemm::Cursor;
+using gemm::Params;
 
-    __device__ static void load_w(uint32_t dst, const CUtensorMap* tmW, const gemm::Params&, uint32_t bar,
-                                  int tile, int kb, uint64_t pol) {
-        tma_load_2d(dst, tmW, bar, kb * 128, tile * 128, pol);
-    }
-    static constexpr bool kHasFoldScale = true;
-    __device__ static const float* fold_scale_ptr(const gemm::Params& p, int tile, int kb) {
-        return p.S + static_cast<int64_t>(tile) * p.lds + kb;
-    }
-    __device__ static float fold(float outer, float inner, float sc) {
-        return __fadd_rn(outer, __fmul_rn(inner, sc));
-    }
+constexpr int kThreads = 480;
+constexpr int kWarpMma0 = 1;      // warps 1, 2
+constexpr int kIssuers = 2;
+constexpr int kWarpFold0 = 3;     // warps 3..6: TMEM lane quadrant warp % 4
+constexpr int kFoldWarps = 4;
+constexpr int kWarpConv0 = 7;     // warps 7..14: two groups of four
+constexpr int kConvWarps = 4;     // per group
+
+template <int NX>
+struct Fp8Layout {
+    static constexpr int kN = 2 * NX;            // MMA N: hi plane, then lo plane
+    static constexpr int kWBytes = 128 * 128;    // one E4M3 unit
+    static constexpr int kXbSlot = NX * 256;     // BF16 X slice, [16-byte chunk j][split thread]
+    static constexpr int kX8Slot = kN * 128;     // both planes, 128-byte rows
+    static constexpr int kXAhead = NX == 16 ? 3 : 2;   // a group's units of X copied ahead
+    static constexpr int kXbStages = kXAhead + 1;      // per group
+    // X plane slots: a slot is refilled once the MMAs that read it complete, so
+    // the ring has to cover the split latency plus the MMA latency
+    static constexpr int kX8Stages = NX == 16 ? 8 : 4;
+    static constexpr int kNA = NX == 16 ? 8 : 4; // TMEM accumulators of kN columns
+    static constexpr int kTmemCols = kNA * kN;
+    // Row factors 2^-e of a unit live in their own ring, kFacStages deep: the
+    // split group writes unit i's factors only after the MMAs of unit
+    // i - kX8Stages completed, which were issued after the fold released unit
+    // i - kX8Stages - kNA's accumulator, having read its factors; so the fold is
+    // done with every unit before i - kX8Stages - kNA >= i - kFacStages.
+    static constexpr int kFacStages = 16;
+    static constexpr int kFacBytes = kFacStages * NX * 4;
+    static constexpr int kMaxWStages = 16;
+    static constexpr int kFixed = 2 * kXbStages * kXbSlot + kX8Stages * kX8Slot + kFacBytes +
+                                  8 * (2 * kMaxWStages + 2 * kX8Stages + 2 * kNA) + 64 + 1024;
+    static constexpr int kWFit = (232448 - kFixed) / kWBytes;
+    // even: every use of a weight stage (and of an X plane slot and an
+    // accumulator) then falls to the same MMA issuer, so each issuer waits on
+    // the phases of a barrier in order
+    static constexpr int kWStages = (kWFit < kMaxWStages ? kWFit : kMaxWStages) & ~1;
+    static constexpr int kXbOff = kWStages * kWBytes;
+    static constexpr int kX8Off = kXbOff + 2 * kXbStages * kXbSlot;
+    static constexpr int kFacOff = kX8Off + kX8Stages * kX8Slot;
+    static constexpr int kBarOff = kFacOff + kFacBytes;
+    static constexpr int kNumBars = 2 * kWStages + 2 * kX8Stages + 2 * kNA;
+    static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+    static constexpr int kSmemBytes = kMiscOff + 64 + 1024;   // + alignment slack
+    static_assert(kX8Off % 1024 == 0 && kX8Slot % 1024 == 0, "keep the 1024-byte swizzle alignment");
+    static_assert(kWStages >= 8 && kWStages % kIssuers == 0, "weight ring");
+    // the same for the X plane slots and the accumulators, whose units also
+    // alternate between the two split groups
+    static_assert(kX8Stages % kIssuers == 0 && kNA % kIssuers == 0, "ring ownership");
+    static_assert(kTmemCols == 256, "TMEM allocation");
+    static_assert(kFacStages >= kX8Stages + kNA, "factor ring");
+    static_assert(kSmemBytes <= 232448, "shared memory");
+};
+
+struct Bf16Store {
     __device__ static void store(void* Y, int64_t idx, float v) {
         static_cast<__nv_bfloat16*>(Y)[idx] = __float2bfloat16_rn(v);
     }
+};
 
-    // One thread dequantises one weight row (128 codes) of a unit.  Two
-    // register slots: the pipeline loads the group's next unit into one while
-    // it converts the current unit from the other.
-    struct Deq {
-        static constexpr int kUnroll = 2;
-        uint4 c[2][8];
-        __device__ Deq(const gemm::Params&, long long, int, int, int) {}
-        __device__ void prepare(const gemm::Params&, int, int, int, int) {}
-        __device__ void load(int slot, const uint8_t* stage, int row) {
-            const uint8_t* wrow = stage + row * 128;
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-                c[slot][j] = *reinterpret_cast<const uint4*>(wrow + ((j ^ (row & 7)) << 4));
+template <int NX>
+__global__ void __launch_bounds__(kThreads, 1)
+    fp8_kernel(const __grid_constant__ CUtensorMap tmW, const Params p) {
+    using L = Fp8Layout<NX>;
+    constexpr int kN = L::kN;
+    constexpr int kWStages = L::kWStages;
+    constexpr int kX8Stages = L::kX8Stages;
+    constexpr int kNA = L::kNA;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* gbase = smem_raw + (base - raw);
+
+    const uint32_t bar0 = base + L::kBarOff;
+    auto wfull = [&](int s) { return bar0 + 8u * s; };
+    auto wempty = [&](int s) { return bar0 + 8u * (kWStages + s); };
+    constexpr int kBarX8 = 2 * kWStages;
+    auto x8full = [&](int s) { return bar0 + 8u * (kBarX8 + s); };
+    auto x8empty = [&](int s) { return bar0 + 8u * (kBarX8 + kX8Stages + s); };
+    constexpr int kBarD = kBarX8 + 2 * kX8Stages;
+    auto dfull = [&](int a) { return bar0 + 8u * (kBarD + a); };
+    auto dempty = [&](int a) { return bar0 + 8u * (kBarD + kNA + a); };
+    float* facs = reinterpret_cast<float*>(gbase + L::kFacOff);   // [kFacStages][NX]
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + L::kMiscOff);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + L::kMiscOff + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int cta = blockIdx.x;
+    const long long u0 = gemm::unit_begin(cta, p.U, p.G);
+    const long long u1 = gemm::unit_begin(cta + 1, p.U, p.G);
+    const int nunits = static_cast<int>(u1 - u0);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kWStages; ++s) {
+            mbar_init(wfull(s), 1);
+            mbar_init(wempty(s), 1);            // commit: the unit's MMAs are complete
         }
-        // columns 16*qtr .. 16*qtr+15 of the row's A fragment (K 32*qtr .. 32*qtr+31)
-        __device__ void convert(int slot, int qtr, uint32_t (&o)[16]) const {
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const uint4 w = c[slot][2 * qtr + j];
-                e4m3x4_to_bf16(w.x, o[8 * j + 0], o[8 * j + 1]);
-                e4m3x4_to_bf16(w.y, o[8 * j + 2], o[8 * j + 3]);
-                e4m3x4_to_bf16(w.z, o[8 * j + 4], o[8 * j + 5]);
-                e4m3x4_to_bf16(w.w, o[8 * j + 6], o[8 * j + 7]);
+        for (int s = 0; s < kX8Stages; ++s) {
+            mbar_init(x8full(s), kConvWarps);
+            mbar_init(x8empty(s), 1);           // commit: the unit's MMAs are complete
+        }
+        for (int a = 0; a < kNA; ++a) {
+            mbar_init(dfull(a), 1);
+            mbar_init(dempty(a), kFoldWarps);
+        }
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    __syncwarp();
+    if (warp == 0) tmem_alloc(smem_u32(tmem_slot), L::kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const WaitCtl wc{p.timeout_ns, p.status, abort_flag};
+    // The next grid on the stream may be scheduled now; its CTAs start as ours
+    // exit, and only its weight stream runs before it waits for this grid.
+    grid_dependents_launch();
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ weight producer
+        if (lane == 0) {
+            prefetch_tmap(&tmW);
+            const uint64_t pol_w = policy_evict_first();
+            int issued = 0;
+            Cursor cur(u0, p.KB);
+            for (int i = 0; i < nunits; ++i, cur.step(p.KB)) {
+                const int s = i % kWStages;
+                if (i >= kWStages && !wait_bounded(wempty(s), ((i / kWStages) - 1) & 1, wc)) break;
+                if (cta == 0 && i == p.fault_unit) continue;   // failure-path test hook
+                mbar_arrive_expect_tx(wfull(s), L::kWBytes);
+                tma_load_2d(base + s * L::kWBytes, &tmW, wfull(s), cur.kr * 128, cur.tile * 128, pol_w);
+                issued = i + 1;
+            }
+            // Every copy this thread started must land before the CTA can exit.
+            for (int i = issued - kWStages < 0 ? 0 : issued - kWStages; i < issued; ++i) {
+                if (cta == 0 && i == p.fault_unit) continue;
+                gemm::drain_wait(wfull(i % kWStages), (i / kWStages) & 1, p.timeout_ns);
             }
         }
-    };
-};
+    } else if (warp >= kWarpConv0) {
+        // ------------------------------------------------------------ X split
+        // Group g takes units i with i % 2 == g.  Thread (r, c) of a group:
+        // row r, elements [c * EPT, c * EPT + EPT) of the unit's 128-wide
+        // slice; the LPR lanes of a row are adjacent lanes.  Each thread copies
+        // and reads back only its own chunks, so the staging ring needs no
+        // barrier: a thread's wait on its own copy groups is enough.
+        constexpr int LPR = 128 / NX;          // lanes per row: 8 or 4
+        constexpr int EPT = 128 / LPR;         // elements per thread: 16 or 32
+        constexpr int CH_IN = EPT / 8;         // 16-byte BF16 chunks read
+        constexpr int CH_OUT = EPT / 16;       // 16-byte E4M3 chunks written per plane
+        constexpr int kAhead = L::kXAhead;
+        const int g = (warp - kWarpConv0) >> 2;
+        const int ct = ((warp - kWarpConv0) & 3) * 32 + lane;
+        const int r = ct / LPR;
+        const int c = ct % LPR;
+        const uint32_t sw = static_cast<uint32_t>(r & 7);
+        const int xring = L::kXbOff + g * L::kXbStages * L::kXbSlot + ct * 16;   // byte offset
+        const __nv_bfloat16* xrow = static_cast<const __nv_bfloat16*>(p.X) + static_cast<int64_t>(r) * p.ldx;
+        // X may be the output of the preceding grid on the stream
+        grid_dependency_wait();
+        Cursor pf(u0 + g, p.KB);   // the group's unit copied next
+        auto prefetch = [&](int i) {
+            if (i < nunits) {
+                const uint32_t slot = base + static_cast<uint32_t>(xring + ((i >> 1) % L::kXbStages) * L::kXbSlot);
+#pragma unroll
+                for (int j = 0; j < CH_IN; ++j) {
+                    const int k = pf.kr * 128 + (c * CH_IN + j) * 8;   // K % 8 == 0: a chunk is in or out
+                    const bool ok = r < p.M && k < p.K;
+                    cp_async_16(slot + j * 2048, ok ? static_cast<const void*>(xrow + k) : p.X, ok ? 16u : 0u);
+                }
+                pf.step(2, p.KB);
+            }
+            cp_async_commit();   // one group per unit, empty past the end
+        };
+        // Unit i's slice into registers, its row maximum and exponent: 2^e
+        // with max |x| * 2^e in [128, 256), e = 134 - (BF16 biased exponent of
+        // the maximum), capped so that 2^e and 2^-e stay normal.
+        auto scan = [&](int i, uint4 (&xin)[CH_IN], uint32_t& pw2, int& e) {
+            const uint8_t* xs = gbase + xring + ((i >> 1) % L::kXbStages) * L::kXbSlot;
+#pragma unroll
+            for (int j = 0; j < CH_IN; ++j) xin[j] = *reinterpret_cast<const uint4*>(xs + j * 2048);
+            uint32_t mx2 = 0;
+#pragma unroll
+            for (int j = 0; j < CH_IN; ++j) {
+                mx2 = max_u16x2(mx2, xin[j].x & 0x7FFF7FFFu);
+                mx2 = max_u16x2(mx2, xin[j].y & 0x7FFF7FFFu);
+                mx2 = max_u16x2(mx2, xin[j].z & 0x7FFF7FFFu);
+                mx2 = max_u16x2(mx2, xin[j].w & 0x7FFF7FFFu);
+            }
+            uint32_t mx = max(mx2 & 0xFFFFu, mx2 >> 16);
+#pragma unroll
+            for (int o = 1; o < LPR; o <<= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            e = 134 - static_cast<int>(mx >> 7);
+            e = e > 126 ? 126 : e;
+            const uint32_t pw = static_cast<uint32_t>(e + 127) << 7;   // BF16 2^e
+            pw2 = pw | (pw << 16);
+        };
+#pragma unroll 1
+        for (int j = 0; j < kAhead; ++j) prefetch(g + 2 * j);
+        uint4 xc[CH_IN];
+        uint32_t pc = 0;
+        int ec = 0;
+        if (g < nunits) {
+            cp_async_wait<kAhead - 1>();
+            scan(g, xc, pc, ec);
+        }
+        for (int i = g; i < nunits; i += 2) {
+            const int s8 = i % kX8Stages;
+            // into the slot scanned in the previous iteration
+            prefetch(i + 2 * kAhead);
+            // the next unit's scan overlaps this unit's conversion
+            uint4 xn[CH_IN];
+            uint32_t pn = 0;
+            int en = 0;
+            cp_async_wait<kAhead - 1>();
+            if (i + 2 < nunits) scan(i + 2, xn, pn, en);
+            if (i >= kX8Stages && !gemm::warp_wait(x8empty(s8), ((i / kX8Stages) - 1) & 1, wc)) break;
+            uint8_t* xo = gbase + L::kX8Off + s8 * L::kX8Slot;
+#pragma unroll
+            for (int h = 0; h < CH_OUT; ++h) {
+                uint32_t hw[4], lw[4];
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    // elements 16h + 4 q4 .. +3 of this thread: BF16 words 8h + 2 q4, +1
+                    const int wi = 8 * h + 2 * q4;
+                    const uint4& src = xc[wi >> 2];
+                    const uint32_t w0 = (wi & 3) == 0 ? src.x : src.z;
+                    const uint32_t w1 = (wi & 3) == 0 ? src.y : src.w;
+                    uint16_t h0, l0, h1, l1;
+                    split_e4m3x2(bf16x2_mul(w0, pc), h0, l0);
+                    split_e4m3x2(bf16x2_mul(w1, pc), h1, l1);
+                    hw[q4] = static_cast<uint32_t>(h0) | (static_cast<uint32_t>(h1) << 16);
+                    lw[q4] = static_cast<uint32_t>(l0) | (static_cast<uint32_t>(l1) << 16);
+                }
+                const uint32_t oc = static_cast<uint32_t>(c * CH_OUT + h);   // 16-element chunk (0..7)
+                const int rh = r, rl = NX + r;
+                *reinterpret_cast<uint4*>(xo + (rh >> 3) * 1024 + (rh & 7) * 128 + ((oc ^ sw) << 4)) =
+                    make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                *reinterpret_cast<uint4*>(xo + (rl >> 3) * 1024 + (rl & 7) * 128 + ((oc ^ sw) << 4)) =
+                    make_uint4(lw[0], lw[1], lw[2], lw[3]);
+            }
+            if (c == 0) facs[(i % L::kFacStages) * NX + r] = __uint_as_float(static_cast<uint32_t>(127 - ec) << 23);   // 2^-e
+            // the planes are read by the tensor core (async proxy)
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(x8full(s8));
+#pragma unroll
+            for (int j = 0; j < CH_IN; ++j) xc[j] = xn[j];
+            pc = pn;
+            ec = en;
+        }
+    } else if (warp >= kWarpMma0 && warp < kWarpMma0 + kIssuers) {
+        // ------------------------------------------------------------ MMA issuers
+        // The whole warp runs the loop and its waits; one elected lane issues.
+        const bool elected = elect_one();
+        const int first = warp - kWarpMma0;
+        constexpr uint32_t idesc = idesc_f8_e4m3(kN);
+        const uint64_t dw0 = smem_desc_sw128(base);
+        const uint64_t dx0 = smem_desc_sw128(base + L::kX8Off);
+        int last = -1;
+        for (int i = first; i < nunits; i += kIssuers) {
+            const int sw = i % kWStages;
+            const int s8 = i % kX8Stages;
+            const int a = i % kNA;
+            if (!gemm::warp_wait(wfull(sw), (i / kWStages) & 1, wc)) break;
+            if (!gemm::warp_wait(x8full(s8), (i / kX8Stages) & 1, wc)) break;
+            if (i >= kNA && !gemm::warp_wait(dempty(a), ((i / kNA) - 1) & 1, wc)) break;
+            tc_fence_after();
+            // descriptor start addresses count 16-byte units; one MMA takes 32 K
+            // bytes of both operands
+            const uint64_t ad = dw0 + static_cast<uint64_t>((sw * L::kWBytes) >> 4);
+            const uint64_t bd = dx0 + static_cast<uint64_t>((s8 * L::kX8Slot) >> 4);
+            const uint32_t dt = tmem + a * kN;
+            if (elected) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) mma_ss_f8(dt, ad + 2 * j, bd + 2 * j, idesc, j > 0 ? 1u : 0u);
+                tc_commit(wempty(sw));
+                tc_commit(x8empty(s8));
+                tc_commit(dfull(a));
+            }
+            __syncwarp();
+            last = i;
+        }
+        if (last >= 0 && elected) gemm::drain_wait(dfull(last % kNA), (last / kNA) & 1, p.timeout_ns);
+    } else if (warp >= kWarpFold0 && warp < kWarpFold0 + kFoldWarps) {
+        // ------------------------------------------------------------ fold / epilogue
+        const int q = warp & 3;
+        const uint32_t tl = tmem + (static_cast<uint32_t>(q * 32) << 16);
+        const int first_tile = static_cast<int>(u0 / p.KB);
+        const int split_info = gemm::split_info_lane(p, u0, u1, lane);
+        // Y and the workspace may still be in use by the preceding grid
+        grid_dependency_wait();
+        float outer[NX];
+#pragma unroll
+        for (int m = 0; m < NX; ++m) outer[m] = 0.0f;
+        // Block scales, 32 units per batch: lane l holds the scale of unit
+        // 32 b + l of the current batch and of the next one, fetched a whole
+        // batch ahead.
+        auto batch_scale = [&](int b) -> float {
+            const int i = 32 * b + lane;
+            if (i >= nunits) return 0.0f;
+            Cursor c(u0 + i, p.KB);
+            return __ldg(p.S + static_cast<int64_t>(c.tile) * p.lds + c.kr);
+        };
+        float sc_cur = batch_scale(0);
+        float sc_next = batch_scale(1);
+        Cursor cur(u0, p.KB);
+        for (int i = 0; i < nunits; ++i, cur.step(p.KB)) {
+            const int a = i % kNA;
+            if ((i & 31) == 0 && i > 0) {
+                sc_cur = sc_next;
+                sc_next = batch_scale((i >> 5) + 1);
+            }
+            const float sc = __shfl_sync(0xffffffffu, sc_cur, i & 31);
+            if (!gemm::warp_wait(dfull(a), (i / kNA) & 1, wc)) break;
+            tc_fence_after();
+            // hi columns [0, NX), lo columns [NX, 2 NX); 16 rows of X at a time,
+            // with the unit's row factors (valid until the fold reaches unit
+            // i + kFacStages - kX8Stages - kNA > i, see kFacStages).
+            const float4* f4 = reinterpret_cast<const float4*>(facs + (i % L::kFacStages) * NX);
+            auto fold16 = [&](int m0, const uint32_t (&vh)[16], const uint32_t (&vl)[16]) {
+#pragma unroll
+                for (int m4 = 0; m4 < 4; ++m4) {
+                    const float4 f = f4[m0 / 4 + m4];
+                    const float fm[4] = {f.x, f.y, f.z, f.w};
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int jj = 4 * m4 + j;
+                        const float t = __fmaf_rn(__uint_as_float(vl[jj]), 0.0625f, __uint_as_float(vh[jj]));
+                        outer[m0 + jj] = __fadd_rn(outer[m0 + jj], __fmul_rn(t, __fmul_rn(sc, fm[j])));
+                    }
+                }
+            };
+            uint32_t vh[16], vl[16];
+            tmem_ld_x16(tl + a * kN, vh);
+            tmem_ld_x16(tl + a * kN + NX, vl);
+            tmem_wait_ld();
+            if constexpr (NX == 32) {
+                fold16(0, vh, vl);
+                tmem_ld_x16(tl + a * kN + 16, vh);
+                tmem_ld_x16(tl + a * kN + NX + 16, vl);
+                tmem_wait_ld();
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(dempty(a));
+            fold16(NX - 16, vh, vl);
+
+            if (cur.kb != p.KB - 1 && i != nunits - 1) continue;
+            gemm::end_piece<NX, Bf16Store>(p, outer, cur.tile, cur.kb, u0 + i, u0, first_tile, split_info, q, lane);
+#pragma unroll
+            for (int m = 0; m < NX; ++m) outer[m] = 0.0f;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, L::kTmemCols);
+    }
+}
+
+template <int NX>
+cudaError_t launch_nx(const Params& prm, const Schedule& s, const CUtensorMap& tmW, bool overlap,
+                      cudaStream_t st) {
+    using L = Fp8Layout<NX>;
+    static int configured_device = -1;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (configured_device != dev) {
+        e = cudaFuncSetAttribute(fp8_kernel<NX>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        configured_device = dev;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(s.G));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = L::kSmemBytes;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    if (overlap) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, fp8_kernel<NX>, tmW, prm);
+}
 
 }  // namespace
 
-cudaError_t launch_fp8(const Fp8Args& a, const Schedule& s, const CUtensorMap& tmW, const CUtensorMap& tmX,
-                       const LaunchCtl& c, cudaStream_t st) {
+cudaError_t launch_fp8(const Fp8Args& a, const Schedule& s, const CUtensorMap& tmW, const LaunchCtl& c,
+                       cudaStream_t st) {
     gemm::Params p = gemm::base_params(s, a.Y, a.ldy, a.M, a.N, a.K, a.ws, c);
     p.S = a.S;
     p.lds = a.lds;
-    if (s.nmma == 16) return gemm::launch<16, Fp8Fmt>(p, s, tmW, tmX, c.overlap, st);
-    return gemm::launch<32, Fp8Fmt>(p, s, tmW, tmX, c.overlap, st);
+    p.X = a.X;
+    p.ldx = a.ldx;
+    if (s.nmma == 16) return launch_nx<16>(p, s, tmW, c.overlap, st);
+    return launch_nx<32>(p, s, tmW, c.overlap, st);
 }
 
 }  // namespace qg

@@ -68,6 +68,8 @@ struct Params {
     int KT;                       // LUT3: 256-wide packed blocks per tile row
     const float* S;               // FP8 block scales
     int64_t lds;
+    const void* X;                // activations (FP8 path: read by the split warps)
+    int64_t ldx;
     // output and shape
     void* Y;
     int64_t ldy;
@@ -127,21 +129,39 @@ __device__ __forceinline__ long long unit_begin(int c, long long U, int G) {
 
 // (tile, K block) of a running unit index, advanced without divisions (a 64-bit
 // division costs hundreds of cycles and used to dominate the per-unit loops).
+// kb is the unit's place in its tile's K order (which decides where pieces
+// end); kr is the K block it actually covers: tile t takes its blocks in the
+// order t mod KB, t mod KB + 1, ..., wrapping around, so that at any moment
+// the CTAs streaming different tiles read different slices of X instead of
+// all hitting the same few L2 lines.
 struct Cursor {
-    int tile, kb;
-    __device__ Cursor(long long u, int KB) : tile(static_cast<int>(u / KB)), kb(static_cast<int>(u % KB)) {}
+    int tile, kb, kr;
+    __device__ static int first_block(int tile, int KB) { return tile % KB; }
+    __device__ Cursor(long long u, int KB) : tile(static_cast<int>(u / KB)), kb(static_cast<int>(u % KB)) {
+        kr = kb + first_block(tile, KB);
+        if (kr >= KB) kr -= KB;
+    }
     __device__ void step(int KB) {
+        if (++kr == KB) kr = 0;
         if (++kb == KB) {
             kb = 0;
             ++tile;
+            kr = first_block(tile, KB);
         }
     }
     __device__ void step(int n, int KB) {
         kb += n;
+        if (kb < KB) {
+            kr += n;
+            while (kr >= KB) kr -= KB;
+            return;
+        }
         while (kb >= KB) {
             kb -= KB;
             ++tile;
         }
+        kr = kb + first_block(tile, KB);
+        if (kr >= KB) kr -= KB;
     }
 };
 
@@ -158,6 +178,107 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64
         if (mbar_try_wait(bar, parity)) return;
         if (globaltimer() - t0 > timeout_ns) return;
     }
+}
+
+// A CTA ends a split piece only in its first and its last tile.  For both,
+// the first and last contributing CTAs (cf, cl) and the slot holding cf's
+// piece (slot 0 when the tile is cf's first tile, i.e. when cf's range starts
+// exactly at the tile; every later contributor's range starts inside the
+// tile, so their pieces are all in slot 0) are worked out once per CTA,
+// before any unit is ready, so that the 64-bit divisions stay out of the
+// reduction.  Lane 3w + k holds value k (cf, cl, slot) of the first (w = 0) or
+// last (w = 1) tile; the reduction fetches them by shuffle.
+__device__ __forceinline__ int split_info_lane(const Params& p, long long u0, long long u1, int lane) {
+    int v = 0;
+    if (lane < 6) {
+        const long long t = lane < 3 ? u0 / p.KB : (u1 - 1) / p.KB;
+        const long long t0 = t * p.KB;
+        const int cf = unit_owner(t0, p.U, p.G);
+        if (lane % 3 == 0) v = cf;
+        if (lane % 3 == 1) v = unit_owner(t0 + p.KB - 1, p.U, p.G);
+        if (lane % 3 == 2) v = unit_begin(cf, p.U, p.G) == t0 ? 0 : 1;
+    }
+    return v;
+}
+
+// End of a CTA's piece of `tile` (one warp, TMEM lane quadrant q, one output
+// row per lane).  A whole tile is stored directly; a split piece goes to the
+// workspace, and the last of the tile's CTAs to arrive sums every piece in
+// ascending K order and stores the tile.  Store::store(Y, index, value)
+// writes one output element.
+template <int NOUT, class Store>
+__device__ __forceinline__ void end_piece(const Params& p, const float (&outer)[NOUT], int tile, int kb,
+                                          long long u, long long u0, int first_tile, int split_info, int q,
+                                          int lane) {
+    const int row = q * 32 + lane;
+    const int n = tile * 128 + row;
+    const int cta = blockIdx.x;
+    const bool whole = (kb == p.KB - 1) && (u - kb >= u0);
+    if (whole) {
+        if (n < p.N) {
+#pragma unroll
+            for (int m = 0; m < NOUT; ++m)
+                if (m < p.M) Store::store(p.Y, static_cast<int64_t>(m) * p.ldy + n, outer[m]);
+        }
+        return;
+    }
+    // Partial sums are stored row-major per thread ([slot][row][m]) so that a
+    // whole row moves with independent 16-byte accesses.
+    const int which = (tile == first_tile) ? 0 : 1;
+    float4* mine = reinterpret_cast<float4*>(p.part) + ((static_cast<size_t>(cta) * 2 + which) * 128 + row) * (NOUT / 4);
+#pragma unroll
+    for (int m4 = 0; m4 < NOUT / 4; ++m4)
+        __stcg(mine + m4, make_float4(outer[4 * m4], outer[4 * m4 + 1], outer[4 * m4 + 2], outer[4 * m4 + 3]));
+    // Every lane's partial must be visible GPU-wide before lane 0's arrival: a
+    // sequentially consistent fence per writing lane (an acquire-release fence
+    // is not enough, since the lanes that wrote are not the lane that performs
+    // the atomic).
+    __threadfence();
+    __syncwarp();
+    uint32_t prev = 0;
+    if (lane == 0) prev = atomicAdd(p.cnt + tile * 4 + q, 1u);
+    prev = __shfl_sync(0xffffffffu, prev, 0);
+    const int cf = __shfl_sync(0xffffffffu, split_info, 3 * which);
+    const int cl = __shfl_sync(0xffffffffu, split_info, 3 * which + 1);
+    const int w_first = __shfl_sync(0xffffffffu, split_info, 3 * which + 2);
+    if (static_cast<int>(prev) != cl - cf) return;
+    // Last piece to arrive: sum all pieces in ascending K order, this CTA's own
+    // piece included (just stored above), loading kBatch pieces at a time so
+    // that their latencies overlap.
+    __threadfence();
+    constexpr int kBatch = NOUT == 16 ? 2 : 1;
+    float acc[NOUT];
+#pragma unroll
+    for (int m = 0; m < NOUT; ++m) acc[m] = 0.0f;
+    for (int c0 = cf; c0 <= cl; c0 += kBatch) {
+        float4 piece[kBatch][NOUT / 4];
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+            const int c2 = c0 + b;
+            if (c2 > cl) break;
+            const float4* slot = reinterpret_cast<const float4*>(p.part) +
+                                 ((static_cast<size_t>(c2) * 2 + (c2 == cf ? w_first : 0)) * 128 + row) * (NOUT / 4);
+#pragma unroll
+            for (int m4 = 0; m4 < NOUT / 4; ++m4) piece[b][m4] = __ldcg(slot + m4);
+        }
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+            if (c0 + b > cl) break;
+#pragma unroll
+            for (int m4 = 0; m4 < NOUT / 4; ++m4) {
+                acc[4 * m4 + 0] = __fadd_rn(acc[4 * m4 + 0], piece[b][m4].x);
+                acc[4 * m4 + 1] = __fadd_rn(acc[4 * m4 + 1], piece[b][m4].y);
+                acc[4 * m4 + 2] = __fadd_rn(acc[4 * m4 + 2], piece[b][m4].z);
+                acc[4 * m4 + 3] = __fadd_rn(acc[4 * m4 + 3], piece[b][m4].w);
+            }
+        }
+    }
+    if (n < p.N) {
+#pragma unroll
+        for (int m = 0; m < NOUT; ++m)
+            if (m < p.M) Store::store(p.Y, static_cast<int64_t>(m) * p.ldy + n, acc[m]);
+    }
+    if (lane == 0) p.cnt[tile * 4 + q] = 0u;   // ready for the next call
 }
 
 template <int NMMA, class F>
@@ -300,26 +421,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp < kWarpDeq0) {
         // ------------------------------------------------------------ fold / epilogue
         const int q = warp & 3;
-        const int row = q * 32 + lane;
         const uint32_t tl = tmem + (static_cast<uint32_t>(q * 32) << 16);
         const int first_tile = static_cast<int>(u0 / p.KB);
-        // A CTA ends a split piece only in its first and its last tile.  For
-        // both, the first and last contributing CTAs (cf, cl) and the slot
-        // holding cf's piece (slot 0 when the tile is cf's first tile, i.e. when
-        // cf's range starts exactly at the tile; every later contributor's range
-        // starts inside the tile, so their pieces are all in slot 0) are worked
-        // out here, before any unit is ready, so that the 64-bit divisions stay
-        // out of the reduction.  Lane 3w + k holds value k (cf, cl, slot) of the
-        // first (w = 0) or last (w = 1) tile; the reduction fetches them by shuffle.
-        int split_info = 0;
-        if (lane < 6) {
-            const long long t = lane < 3 ? u0 / p.KB : (u1 - 1) / p.KB;
-            const long long t0 = t * p.KB;
-            const int cf = unit_owner(t0, p.U, p.G);
-            if (lane % 3 == 0) split_info = cf;
-            if (lane % 3 == 1) split_info = unit_owner(t0 + p.KB - 1, p.U, p.G);
-            if (lane % 3 == 2) split_info = unit_begin(cf, p.U, p.G) == t0 ? 0 : 1;
-        }
+        const int split_info = split_info_lane(p, u0, u1, lane);
         // Y and the workspace may still be in use by the preceding grid
         grid_dependency_wait();
         float outer[NMMA];
@@ -370,77 +474,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
 
             if (kb != p.KB - 1 && u != u1 - 1) continue;
-            // ---- end of this CTA's piece of `tile`
-            const int n = tile * 128 + row;
-            const bool whole = (kb == p.KB - 1) && (u - kb >= u0);
-            if (whole) {
-                if (n < p.N) {
-#pragma unroll
-                    for (int m = 0; m < NMMA; ++m)
-                        if (m < p.M) F::store(p.Y, static_cast<int64_t>(m) * p.ldy + n, outer[m]);
-                }
-            } else {
-                // Partial sums are stored row-major per thread ([slot][row][m]) so
-                // that a whole row moves with independent 16-byte accesses.
-                const int which = (tile == first_tile) ? 0 : 1;
-                float4* mine = reinterpret_cast<float4*>(p.part) +
-                               ((static_cast<size_t>(cta) * 2 + which) * 128 + row) * (NMMA / 4);
-#pragma unroll
-                for (int m4 = 0; m4 < NMMA / 4; ++m4)
-                    __stcg(mine + m4, make_float4(outer[4 * m4], outer[4 * m4 + 1], outer[4 * m4 + 2], outer[4 * m4 + 3]));
-                // Every lane's partial must be visible GPU-wide before lane 0's
-                // arrival: a sequentially consistent fence per writing lane (an
-                // acquire-release fence is not enough, since the lanes that
-                // wrote are not the lane that performs the atomic).
-                __threadfence();
-                __syncwarp();
-                uint32_t prev = 0;
-                if (lane == 0) prev = atomicAdd(p.cnt + tile * 4 + q, 1u);
-                prev = __shfl_sync(0xffffffffu, prev, 0);
-                const int cf = __shfl_sync(0xffffffffu, split_info, 3 * which);
-                const int cl = __shfl_sync(0xffffffffu, split_info, 3 * which + 1);
-                const int w_first = __shfl_sync(0xffffffffu, split_info, 3 * which + 2);
-                if (static_cast<int>(prev) == cl - cf) {
-                    // Last piece to arrive: sum all pieces in ascending K order,
-                    // this CTA's own piece included (just stored above), loading
-                    // kBatch pieces at a time so that their latencies overlap.
-                    __threadfence();
-                    constexpr int kBatch = NMMA == 16 ? 4 : 1;
-                    float acc[NMMA];
-#pragma unroll
-                    for (int m = 0; m < NMMA; ++m) acc[m] = 0.0f;
-                    for (int c0 = cf; c0 <= cl; c0 += kBatch) {
-                        float4 piece[kBatch][NMMA / 4];
-#pragma unroll
-                        for (int b = 0; b < kBatch; ++b) {
-                            const int c2 = c0 + b;
-                            if (c2 > cl) break;
-                            const float4* slot =
-                                reinterpret_cast<const float4*>(p.part) +
-                                ((static_cast<size_t>(c2) * 2 + (c2 == cf ? w_first : 0)) * 128 + row) * (NMMA / 4);
-#pragma unroll
-                            for (int m4 = 0; m4 < NMMA / 4; ++m4) piece[b][m4] = __ldcg(slot + m4);
-                        }
-#pragma unroll
-                        for (int b = 0; b < kBatch; ++b) {
-                            if (c0 + b > cl) break;
-#pragma unroll
-                            for (int m4 = 0; m4 < NMMA / 4; ++m4) {
-                                acc[4 * m4 + 0] = __fadd_rn(acc[4 * m4 + 0], piece[b][m4].x);
-                                acc[4 * m4 + 1] = __fadd_rn(acc[4 * m4 + 1], piece[b][m4].y);
-                                acc[4 * m4 + 2] = __fadd_rn(acc[4 * m4 + 2], piece[b][m4].z);
-                                acc[4 * m4 + 3] = __fadd_rn(acc[4 * m4 + 3], piece[b][m4].w);
-                            }
-                        }
-                    }
-                    if (n < p.N) {
-#pragma unroll
-                        for (int m = 0; m < NMMA; ++m)
-                            if (m < p.M) F::store(p.Y, static_cast<int64_t>(m) * p.ldy + n, acc[m]);
-                    }
-                    if (lane == 0) p.cnt[tile * 4 + q] = 0u;   // ready for the next call
-                }
-            }
+            end_piece<NMMA, F>(p, outer, tile, kb, u, u0, first_tile, split_info, q, lane);
 #pragma unroll
             for (int m = 0; m < NMMA; ++m) outer[m] = 0.0f;
         }

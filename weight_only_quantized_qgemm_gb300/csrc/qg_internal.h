@@ -68,8 +68,8 @@ struct LaunchCtl {
     bool overlap;        // launch with programmatic stream serialization
 };
 
-cudaError_t launch_fp8(const Fp8Args& a, const Schedule& s, const CUtensorMap& tmW,
-                       const CUtensorMap& tmX, const LaunchCtl& c, cudaStream_t st);
+cudaError_t launch_fp8(const Fp8Args& a, const Schedule& s, const CUtensorMap& tmW, const LaunchCtl& c,
+                       cudaStream_t st);
 cudaError_t launch_lut3(const Lut3Args& a, const Schedule& s, const CUtensorMap& tmX,
                         const LaunchCtl& c, cudaStream_t st);
 
