@@ -74,13 +74,27 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// As mbar_try_wait, but a thread whose phase is not complete yet sleeps until
+// it completes or `ns` nanoseconds pass, instead of polling: polling warps take
+// issue slots from the warps doing the work.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Waits for the phase with the given parity to complete.  Returns false if the
 // CTA is aborting or the wait ran past its bound (which starts the abort).
 // The iteration cap is a second, clock-independent bound.
 static __device__ __noinline__ bool wait_bounded_slow(uint32_t bar, uint32_t parity, const WaitCtl& c) {
     const uint64_t t0 = globaltimer();
     for (uint32_t it = 0; it < (1u << 26); ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
         if (*c.abort) return false;
         if (globaltimer() - t0 > c.timeout_ns) {
             raise_abort(c, kDevTimeout);
@@ -372,6 +386,24 @@ __device__ __forceinline__ void split_e4m3x2(uint32_t xw, uint16_t& hi, uint16_t
     asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(h2), "r"(hh));
     asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(d), "r"(0x4C004C00u));   // x 16
     asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(lo) : "r"(d));
+}
+
+// Per half: the larger magnitude of a and b (the sign bit of the result is the
+// XOR of the operands' signs; callers mask it off).
+__device__ __forceinline__ uint32_t bf16x2_absmax(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// split_e4m3x2 on two BF16 pairs: x0..x3 (low half of xa first) -> hi and lo
+// words of four E4M3 codes each, element 0 in the low byte.
+__device__ __forceinline__ void split_e4m3x4(uint32_t xa, uint32_t xb, uint32_t& hi, uint32_t& lo) {
+    uint16_t h0, l0, h1, l1;
+    split_e4m3x2(xa, h0, l0);
+    split_e4m3x2(xb, h1, l1);
+    asm("mov.b32 %0, {%1, %2};" : "=r"(hi) : "h"(h0), "h"(h1));
+    asm("mov.b32 %0, {%1, %2};" : "=r"(lo) : "h"(l0), "h"(l1));
 }
 
 // Byte planes of an 8-entry FP16 table e[0..7] given as four FP16x2 words

@@ -31,14 +31,17 @@
 //                that free the unit's weight stage and X planes and mark its
 //                accumulator ready once the MMAs complete.
 //   warps 3-6    fold / epilogue, one per TMEM lane quadrant (warp % 4).
-//   warps 7-14   X split, two groups of four warps taking alternate units.
-//                Each thread copies its own share of a unit's BF16 X slice
-//                several units ahead (cp.async through the load/store path: a
-//                TMA copy would queue behind the weight tiles already in
-//                flight and arrive microseconds later), takes the row maxima
-//                and exponents of its group's next unit while it converts the
+//   warps 7-14   X split: four groups of 2 warps taking every fourth unit (two
+//                groups of 4 warps, alternate units, for 32 rows), 32
+//                elements of a row per thread.  Each
+//                thread copies its own share of a unit's BF16 X slice several
+//                units ahead (cp.async through the load/store path: a TMA copy
+//                would queue behind the weight tiles already in flight and
+//                arrive microseconds later), takes the row maxima and
+//                exponents of its group's next unit while it converts the
 //                current one, and writes the hi/lo E4M3 planes in the
-//                swizzled K-major layout, 2^-e per row beside them.
+//                swizzled K-major layout, and s * 2^-e per row beside them
+//                (s = the unit's block scale).
 // A unit is 128 weight rows x one 128-wide K block.  The schedule (tiles of
 // 128 rows, split-K pieces, last-arriver reduction) is the shared one of
 // qg_gemm.cuh.
@@ -50,28 +53,35 @@ namespace {
 using gemm::Cursor;
 using gemm::Params;
 
-constexpr int kThreads = 480;
 constexpr int kWarpMma0 = 1;      // warps 1, 2
 constexpr int kIssuers = 2;
 constexpr int kWarpFold0 = 3;     // warps 3..6: TMEM lane quadrant warp % 4
 constexpr int kFoldWarps = 4;
-constexpr int kWarpConv0 = 7;     // warps 7..14: two groups of four
-constexpr int kConvWarps = 4;     // per group
+constexpr int kWarpConv0 = 7;     // then two groups of split warps
+constexpr int kEpt = 32;          // X elements per split thread and unit
+constexpr int kLpr = 128 / kEpt;  // split lanes per row
+
+template <int NX>
+struct Split {
+    static constexpr int kWarps = NX * kLpr / 32;   // per group: 2 or 4
+    static constexpr int kGroups = NX == 16 ? 4 : 2; // taking units i with i % kGroups == g
+    static constexpr int kThreads = 32 * (kWarpConv0 + kGroups * kWarps);
+};
 
 template <int NX>
 struct Fp8Layout {
     static constexpr int kN = 2 * NX;            // MMA N: hi plane, then lo plane
     static constexpr int kWBytes = 128 * 128;    // one E4M3 unit
-    static constexpr int kXbSlot = NX * 256;     // BF16 X slice, [16-byte chunk j][split thread]
+    static constexpr int kXbSlot = NX * 256;     // BF16 X slice, [16-byte chunk j][split thread of the group]
     static constexpr int kX8Slot = kN * 128;     // both planes, 128-byte rows
-    static constexpr int kXAhead = NX == 16 ? 3 : 2;   // a group's units of X copied ahead
+    static constexpr int kXAhead = NX == 16 ? 1 : 2;   // a group's units of X copied ahead
     static constexpr int kXbStages = kXAhead + 1;      // per group
     // X plane slots: a slot is refilled once the MMAs that read it complete, so
     // the ring has to cover the split latency plus the MMA latency
     static constexpr int kX8Stages = NX == 16 ? 8 : 4;
     static constexpr int kNA = NX == 16 ? 8 : 4; // TMEM accumulators of kN columns
     static constexpr int kTmemCols = kNA * kN;
-    // Row factors 2^-e of a unit live in their own ring, kFacStages deep: the
+    // Row factors s * 2^-e of a unit live in their own ring, kFacStages deep: the
     // split group writes unit i's factors only after the MMAs of unit
     // i - kX8Stages completed, which were issued after the fold released unit
     // i - kX8Stages - kNA's accumulator, having read its factors; so the fold is
@@ -79,7 +89,7 @@ struct Fp8Layout {
     static constexpr int kFacStages = 16;
     static constexpr int kFacBytes = kFacStages * NX * 4;
     static constexpr int kMaxWStages = 16;
-    static constexpr int kFixed = 2 * kXbStages * kXbSlot + kX8Stages * kX8Slot + kFacBytes +
+    static constexpr int kFixed = Split<NX>::kGroups * kXbStages * kXbSlot + kX8Stages * kX8Slot + kFacBytes +
                                   8 * (2 * kMaxWStages + 2 * kX8Stages + 2 * kNA) + 64 + 1024;
     static constexpr int kWFit = (232448 - kFixed) / kWBytes;
     // even: every use of a weight stage (and of an X plane slot and an
@@ -87,7 +97,7 @@ struct Fp8Layout {
     // the phases of a barrier in order
     static constexpr int kWStages = (kWFit < kMaxWStages ? kWFit : kMaxWStages) & ~1;
     static constexpr int kXbOff = kWStages * kWBytes;
-    static constexpr int kX8Off = kXbOff + 2 * kXbStages * kXbSlot;
+    static constexpr int kX8Off = kXbOff + Split<NX>::kGroups * kXbStages * kXbSlot;
     static constexpr int kFacOff = kX8Off + kX8Stages * kX8Slot;
     static constexpr int kBarOff = kFacOff + kFacBytes;
     static constexpr int kNumBars = 2 * kWStages + 2 * kX8Stages + 2 * kNA;
@@ -95,9 +105,10 @@ struct Fp8Layout {
     static constexpr int kSmemBytes = kMiscOff + 64 + 1024;   // + alignment slack
     static_assert(kX8Off % 1024 == 0 && kX8Slot % 1024 == 0, "keep the 1024-byte swizzle alignment");
     static_assert(kWStages >= 8 && kWStages % kIssuers == 0, "weight ring");
-    // the same for the X plane slots and the accumulators, whose units also
-    // alternate between the two split groups
+    // the same for the X plane slots and the accumulators, and for the split
+    // groups, which take every kGroups-th unit
     static_assert(kX8Stages % kIssuers == 0 && kNA % kIssuers == 0, "ring ownership");
+    static_assert(kX8Stages % Split<NX>::kGroups == 0, "ring ownership");
     static_assert(kTmemCols == 256, "TMEM allocation");
     static_assert(kFacStages >= kX8Stages + kNA, "factor ring");
     static_assert(kSmemBytes <= 232448, "shared memory");
@@ -110,7 +121,7 @@ struct Bf16Store {
 };
 
 template <int NX>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Split<NX>::kThreads, 1)
     fp8_kernel(const __grid_constant__ CUtensorMap tmW, const Params p) {
     using L = Fp8Layout<NX>;
     constexpr int kN = L::kN;
@@ -131,7 +142,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int kBarD = kBarX8 + 2 * kX8Stages;
     auto dfull = [&](int a) { return bar0 + 8u * (kBarD + a); };
     auto dempty = [&](int a) { return bar0 + 8u * (kBarD + kNA + a); };
-    float* facs = reinterpret_cast<float*>(gbase + L::kFacOff);   // [kFacStages][NX]
+    float* facs = reinterpret_cast<float*>(gbase + L::kFacOff);   // [kFacStages][NX]: s * 2^-e
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + L::kMiscOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + L::kMiscOff + 4);
 
@@ -148,7 +159,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(wempty(s), 1);            // commit: the unit's MMAs are complete
         }
         for (int s = 0; s < kX8Stages; ++s) {
-            mbar_init(x8full(s), kConvWarps);
+            mbar_init(x8full(s), Split<NX>::kWarps);
             mbar_init(x8empty(s), 1);           // commit: the unit's MMAs are complete
         }
         for (int a = 0; a < kNA; ++a) {
@@ -192,81 +203,90 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp >= kWarpConv0) {
         // ------------------------------------------------------------ X split
-        // Group g takes units i with i % 2 == g.  Thread (r, c) of a group:
-        // row r, elements [c * EPT, c * EPT + EPT) of the unit's 128-wide
-        // slice; the LPR lanes of a row are adjacent lanes.  Each thread copies
-        // and reads back only its own chunks, so the staging ring needs no
-        // barrier: a thread's wait on its own copy groups is enough.
-        constexpr int LPR = 128 / NX;          // lanes per row: 8 or 4
-        constexpr int EPT = 128 / LPR;         // elements per thread: 16 or 32
-        constexpr int CH_IN = EPT / 8;         // 16-byte BF16 chunks read
-        constexpr int CH_OUT = EPT / 16;       // 16-byte E4M3 chunks written per plane
+        // Group g takes units i with i % kG == g.  Thread (r, c) of a group:
+        // row r, elements [32 c, 32 c + 32) of the unit's 128-wide slice; the
+        // four lanes of a row are adjacent lanes.  Each thread copies and reads
+        // back only its own chunks, so the staging ring needs no barrier: a
+        // thread's wait on its own copy groups is enough.
+        constexpr int CH_IN = kEpt / 8;        // 16-byte BF16 chunks read
+        constexpr int CH_OUT = kEpt / 16;      // 16-byte E4M3 chunks written per plane
+        constexpr int kGT = 32 * Split<NX>::kWarps;   // threads per group
         constexpr int kAhead = L::kXAhead;
-        const int g = (warp - kWarpConv0) >> 2;
-        const int ct = ((warp - kWarpConv0) & 3) * 32 + lane;
-        const int r = ct / LPR;
-        const int c = ct % LPR;
+        constexpr int kG = Split<NX>::kGroups;
+        const int g = (warp - kWarpConv0) / Split<NX>::kWarps;
+        const int ct = ((warp - kWarpConv0) % Split<NX>::kWarps) * 32 + lane;
+        const int r = ct / kLpr;
+        const int c = ct % kLpr;
         const uint32_t sw = static_cast<uint32_t>(r & 7);
         const int xring = L::kXbOff + g * L::kXbStages * L::kXbSlot + ct * 16;   // byte offset
         const __nv_bfloat16* xrow = static_cast<const __nv_bfloat16*>(p.X) + static_cast<int64_t>(r) * p.ldx;
         // X may be the output of the preceding grid on the stream
         grid_dependency_wait();
         Cursor pf(u0 + g, p.KB);   // the group's unit copied next
+        Cursor sq(u0 + g, p.KB);   // the group's unit scanned next
         auto prefetch = [&](int i) {
             if (i < nunits) {
-                const uint32_t slot = base + static_cast<uint32_t>(xring + ((i >> 1) % L::kXbStages) * L::kXbSlot);
+                const uint32_t slot = base + static_cast<uint32_t>(xring + ((i / kG) % L::kXbStages) * L::kXbSlot);
+                const int k0 = pf.kr * 128 + c * kEpt;   // K % 8 == 0: a chunk is in or out
+                const bool rok = r < p.M;
 #pragma unroll
                 for (int j = 0; j < CH_IN; ++j) {
-                    const int k = pf.kr * 128 + (c * CH_IN + j) * 8;   // K % 8 == 0: a chunk is in or out
-                    const bool ok = r < p.M && k < p.K;
-                    cp_async_16(slot + j * 2048, ok ? static_cast<const void*>(xrow + k) : p.X, ok ? 16u : 0u);
+                    const bool ok = rok && k0 + j * 8 < p.K;
+                    cp_async_16(slot + j * (kGT * 16), ok ? static_cast<const void*>(xrow + k0 + j * 8) : p.X,
+                                ok ? 16u : 0u);
                 }
-                pf.step(2, p.KB);
+                pf.step(kG, p.KB);
             }
             cp_async_commit();   // one group per unit, empty past the end
         };
         // Unit i's slice into registers, its row maximum and exponent: 2^e
         // with max |x| * 2^e in [128, 256), e = 134 - (BF16 biased exponent of
-        // the maximum), capped so that 2^e and 2^-e stay normal.
-        auto scan = [&](int i, uint4 (&xin)[CH_IN], uint32_t& pw2, int& e) {
-            const uint8_t* xs = gbase + xring + ((i >> 1) % L::kXbStages) * L::kXbSlot;
+        // the maximum), capped so that 2^e and 2^-e stay normal; and the unit's
+        // block scale.
+        auto scan = [&](int i, uint4 (&xin)[CH_IN], uint32_t& pw2, int& e, float& sblk) {
+            sblk = __ldg(p.S + static_cast<int64_t>(sq.tile) * p.lds + sq.kr);
+            sq.step(kG, p.KB);
+            const uint8_t* xs = gbase + xring + ((i / kG) % L::kXbStages) * L::kXbSlot;
 #pragma unroll
-            for (int j = 0; j < CH_IN; ++j) xin[j] = *reinterpret_cast<const uint4*>(xs + j * 2048);
-            uint32_t mx2 = 0;
+            for (int j = 0; j < CH_IN; ++j) xin[j] = *reinterpret_cast<const uint4*>(xs + j * (kGT * 16));
+            // max(|a|, |b|) per half, sign bits set aside below
+            uint32_t m2 = bf16x2_absmax(xin[0].x, xin[0].y);
+            m2 = bf16x2_absmax(m2, bf16x2_absmax(xin[0].z, xin[0].w));
 #pragma unroll
-            for (int j = 0; j < CH_IN; ++j) {
-                mx2 = max_u16x2(mx2, xin[j].x & 0x7FFF7FFFu);
-                mx2 = max_u16x2(mx2, xin[j].y & 0x7FFF7FFFu);
-                mx2 = max_u16x2(mx2, xin[j].z & 0x7FFF7FFFu);
-                mx2 = max_u16x2(mx2, xin[j].w & 0x7FFF7FFFu);
+            for (int j = 1; j < CH_IN; ++j) {
+                m2 = bf16x2_absmax(m2, bf16x2_absmax(xin[j].x, xin[j].y));
+                m2 = bf16x2_absmax(m2, bf16x2_absmax(xin[j].z, xin[j].w));
             }
-            uint32_t mx = max(mx2 & 0xFFFFu, mx2 >> 16);
+            m2 &= 0x7FFF7FFFu;
+            uint32_t mx = max(m2 & 0xFFFFu, m2 >> 16);
 #pragma unroll
-            for (int o = 1; o < LPR; o <<= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            for (int o = 1; o < kLpr; o <<= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
             e = 134 - static_cast<int>(mx >> 7);
             e = e > 126 ? 126 : e;
             const uint32_t pw = static_cast<uint32_t>(e + 127) << 7;   // BF16 2^e
             pw2 = pw | (pw << 16);
         };
 #pragma unroll 1
-        for (int j = 0; j < kAhead; ++j) prefetch(g + 2 * j);
+        for (int j = 0; j < kAhead; ++j) prefetch(g + kG * j);
         uint4 xc[CH_IN];
         uint32_t pc = 0;
         int ec = 0;
+        float scur = 0.0f;
         if (g < nunits) {
             cp_async_wait<kAhead - 1>();
-            scan(g, xc, pc, ec);
+            scan(g, xc, pc, ec, scur);
         }
-        for (int i = g; i < nunits; i += 2) {
+        for (int i = g; i < nunits; i += kG) {
             const int s8 = i % kX8Stages;
             // into the slot scanned in the previous iteration
-            prefetch(i + 2 * kAhead);
+            prefetch(i + kG * kAhead);
             // the next unit's scan overlaps this unit's conversion
             uint4 xn[CH_IN];
             uint32_t pn = 0;
             int en = 0;
+            float snext = 0.0f;
             cp_async_wait<kAhead - 1>();
-            if (i + 2 < nunits) scan(i + 2, xn, pn, en);
+            if (i + kG < nunits) scan(i + kG, xn, pn, en, snext);
             if (i >= kX8Stages && !gemm::warp_wait(x8empty(s8), ((i / kX8Stages) - 1) & 1, wc)) break;
             uint8_t* xo = gbase + L::kX8Off + s8 * L::kX8Slot;
 #pragma unroll
@@ -279,11 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint4& src = xc[wi >> 2];
                     const uint32_t w0 = (wi & 3) == 0 ? src.x : src.z;
                     const uint32_t w1 = (wi & 3) == 0 ? src.y : src.w;
-                    uint16_t h0, l0, h1, l1;
-                    split_e4m3x2(bf16x2_mul(w0, pc), h0, l0);
-                    split_e4m3x2(bf16x2_mul(w1, pc), h1, l1);
-                    hw[q4] = static_cast<uint32_t>(h0) | (static_cast<uint32_t>(h1) << 16);
-                    lw[q4] = static_cast<uint32_t>(l0) | (static_cast<uint32_t>(l1) << 16);
+                    split_e4m3x4(bf16x2_mul(w0, pc), bf16x2_mul(w1, pc), hw[q4], lw[q4]);
                 }
                 const uint32_t oc = static_cast<uint32_t>(c * CH_OUT + h);   // 16-element chunk (0..7)
                 const int rh = r, rl = NX + r;
@@ -292,7 +308,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 *reinterpret_cast<uint4*>(xo + (rl >> 3) * 1024 + (rl & 7) * 128 + ((oc ^ sw) << 4)) =
                     make_uint4(lw[0], lw[1], lw[2], lw[3]);
             }
-            if (c == 0) facs[(i % L::kFacStages) * NX + r] = __uint_as_float(static_cast<uint32_t>(127 - ec) << 23);   // 2^-e
+            // s * 2^-e: exact, a power-of-two multiple of the FP32 block scale
+            if (c == 0)
+                facs[(i % L::kFacStages) * NX + r] = __fmul_rn(scur, __uint_as_float(static_cast<uint32_t>(127 - ec) << 23));
             // the planes are read by the tensor core (async proxy)
             fence_proxy_async_smem();
             __syncwarp();
@@ -301,6 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; j < CH_IN; ++j) xc[j] = xn[j];
             pc = pn;
             ec = en;
+            scur = snext;
         }
     } else if (warp >= kWarpMma0 && warp < kWarpMma0 + kIssuers) {
         // ------------------------------------------------------------ MMA issuers
@@ -346,30 +365,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         float outer[NX];
 #pragma unroll
         for (int m = 0; m < NX; ++m) outer[m] = 0.0f;
-        // Block scales, 32 units per batch: lane l holds the scale of unit
-        // 32 b + l of the current batch and of the next one, fetched a whole
-        // batch ahead.
-        auto batch_scale = [&](int b) -> float {
-            const int i = 32 * b + lane;
-            if (i >= nunits) return 0.0f;
-            Cursor c(u0 + i, p.KB);
-            return __ldg(p.S + static_cast<int64_t>(c.tile) * p.lds + c.kr);
-        };
-        float sc_cur = batch_scale(0);
-        float sc_next = batch_scale(1);
         Cursor cur(u0, p.KB);
         for (int i = 0; i < nunits; ++i, cur.step(p.KB)) {
             const int a = i % kNA;
-            if ((i & 31) == 0 && i > 0) {
-                sc_cur = sc_next;
-                sc_next = batch_scale((i >> 5) + 1);
-            }
-            const float sc = __shfl_sync(0xffffffffu, sc_cur, i & 31);
             if (!gemm::warp_wait(dfull(a), (i / kNA) & 1, wc)) break;
             tc_fence_after();
             // hi columns [0, NX), lo columns [NX, 2 NX); 16 rows of X at a time,
-            // with the unit's row factors (valid until the fold reaches unit
-            // i + kFacStages - kX8Stages - kNA > i, see kFacStages).
+            // with the unit's row factors s * 2^-e (valid until the fold reaches
+            // unit i + kFacStages - kX8Stages - kNA > i, see kFacStages):
+            //   outer += (hi + lo / 16) * s * 2^-e
             const float4* f4 = reinterpret_cast<const float4*>(facs + (i % L::kFacStages) * NX);
             auto fold16 = [&](int m0, const uint32_t (&vh)[16], const uint32_t (&vl)[16]) {
 #pragma unroll
@@ -380,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int j = 0; j < 4; ++j) {
                         const int jj = 4 * m4 + j;
                         const float t = __fmaf_rn(__uint_as_float(vl[jj]), 0.0625f, __uint_as_float(vh[jj]));
-                        outer[m0 + jj] = __fadd_rn(outer[m0 + jj], __fmul_rn(t, __fmul_rn(sc, fm[j])));
+                        outer[m0 + jj] = __fmaf_rn(t, fm[j], outer[m0 + jj]);
                     }
                 }
             };
@@ -430,7 +434,7 @@ cudaError_t launch_nx(const Params& prm, const Schedule& s, const CUtensorMap& t
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(s.G));
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(Split<NX>::kThreads);
     cfg.dynamicSmemBytes = L::kSmemBytes;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];

@@ -354,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (i >= kWStages && !wait_bounded(wempty(s), ((i / kWStages) - 1) & 1, wc)) break;
                 if (cta == 0 && i == p.fault_unit) continue;   // failure-path test hook
                 mbar_arrive_expect_tx(wfull(s), F::kWBytes);
-                F::load_w(base + s * F::kWBytes, &tmW, p, wfull(s), cur.tile, cur.kb, pol_w);
+                F::load_w(base + s * F::kWBytes, &tmW, p, wfull(s), cur.tile, cur.kr, pol_w);
                 issued = i + 1;
             }
             // Every copy this thread started must land before the CTA can exit.
@@ -377,8 +377,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (i >= kXStages && !wait_bounded(xempty(s), ((i / kXStages) - 1) & 1, wc)) break;
                 const uint32_t st = base + L::kXOff + s * L::kXSlot;
                 mbar_arrive_expect_tx(xfull(s), L::kXSlot);
-                tma_load_2d(st, &tmX, xfull(s), cur.kb * 128, 0, pol_x);
-                tma_load_2d(st + L::kXBox, &tmX, xfull(s), cur.kb * 128 + 64, 0, pol_x);
+                tma_load_2d(st, &tmX, xfull(s), cur.kr * 128, 0, pol_x);
+                tma_load_2d(st + L::kXBox, &tmX, xfull(s), cur.kr * 128 + 64, 0, pol_x);
                 issued = i + 1;
             }
             for (int i = issued - kXStages < 0 ? 0 : issued - kXStages; i < issued; ++i)
@@ -438,7 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int i = 32 * b + lane;
             if (i >= nunits) return 0.0f;
             Cursor c(u0 + i, p.KB);
-            return __ldg(F::fold_scale_ptr(p, c.tile, c.kb));
+            return __ldg(F::fold_scale_ptr(p, c.tile, c.kr));
         };
         float sc_cur = batch_scale(0);
         float sc_next = batch_scale(1);

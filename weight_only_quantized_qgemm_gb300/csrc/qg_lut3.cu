@@ -53,7 +53,7 @@ struct Lut3Fmt {
         gemm::Cursor ahead;   // the unit whose scale is fetched next
         __device__ static uint32_t scale_of(const gemm::Params& p, const gemm::Cursor& c, int row) {
             const int n = c.tile * 128 + row;
-            return n < p.N ? static_cast<uint32_t>(__ldg(p.lut_scales + static_cast<int64_t>(n) * p.ld_lut_scales + c.kb))
+            return n < p.N ? static_cast<uint32_t>(__ldg(p.lut_scales + static_cast<int64_t>(n) * p.ld_lut_scales + c.kr))
                            : 0u;
         }
         // this thread handles units grp, grp + 2, grp + 4, ...; slot j holds the
