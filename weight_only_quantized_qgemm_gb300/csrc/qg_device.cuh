@@ -423,10 +423,12 @@ __device__ __forceinline__ LutPlanes lut_planes(uint32_t e01, uint32_t e23, uint
 }
 
 // Eight 3-bit codes, one per nibble of w (nibble i = K offset i) -> four
-// FP16x2 words {d0,d1}, {d2,d3}, {d4,d5}, {d6,d7}: one shift and eight byte
-// permutes (the code word is the permute selector).
+// FP16x2 words {d0,d1}, {d2,d3}, {d4,d5}, {d6,d7}: eight byte permutes (the
+// code word is the permute selector) and a shift of the word's high half,
+// done as a high multiply so that it runs on the FMA pipe instead of adding
+// to the permutes on the integer pipe.
 __device__ __forceinline__ void lut3x8_to_f16(uint32_t w, const LutPlanes& t, uint32_t (&o)[4]) {
-    const uint32_t w2 = w >> 16;
+    const uint32_t w2 = __umulhi(w, 65536u);
     const uint32_t l0 = prmt(t.lo0, t.lo1, w);
     const uint32_t h0 = prmt(t.hi0, t.hi1, w);
     const uint32_t l1 = prmt(t.lo0, t.lo1, w2);

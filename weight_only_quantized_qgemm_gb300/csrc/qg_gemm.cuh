@@ -165,6 +165,24 @@ struct Cursor {
     }
 };
 
+// Slot of a ring of N slots and the parity of that slot's current use, for a
+// running unit index advanced by a fixed stride: i % N and (i / N) & 1 kept
+// incrementally (divisions by ring sizes that are not powers of two cost a
+// handful of integer instructions per use, on the pipe the dequantiser needs).
+template <int N>
+struct Ring {
+    int slot;
+    uint32_t phase;
+    __device__ explicit Ring(int i) : slot(i % N), phase(static_cast<uint32_t>((i / N) & 1)) {}
+    __device__ __forceinline__ void step(int d) {   // d <= N
+        slot += d;
+        if (slot >= N) {
+            slot -= N;
+            phase ^= 1u;
+        }
+    }
+};
+
 // Warp-uniform bounded wait: every lane polls, the warp agrees on the outcome.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const WaitCtl& c) {
     const bool ok = wait_bounded(bar, parity, c);
@@ -349,9 +367,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t pol_w = policy_evict_first();
             int issued = 0;
             Cursor cur(u0, p.KB);
-            for (int i = 0; i < nunits; ++i, cur.step(p.KB)) {
-                const int s = i % kWStages;
-                if (i >= kWStages && !wait_bounded(wempty(s), ((i / kWStages) - 1) & 1, wc)) break;
+            Ring<kWStages> rw(0);
+            for (int i = 0; i < nunits; ++i, cur.step(p.KB), rw.step(1)) {
+                const int s = rw.slot;
+                if (i >= kWStages && !wait_bounded(wempty(s), rw.phase ^ 1u, wc)) break;
                 if (cta == 0 && i == p.fault_unit) continue;   // failure-path test hook
                 mbar_arrive_expect_tx(wfull(s), F::kWBytes);
                 F::load_w(base + s * F::kWBytes, &tmW, p, wfull(s), cur.tile, cur.kr, pol_w);
@@ -372,9 +391,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t pol_x = policy_evict_last();
             int issued = 0;
             Cursor cur(u0, p.KB);
-            for (int i = 0; i < nunits; ++i, cur.step(p.KB)) {
-                const int s = i % kXStages;
-                if (i >= kXStages && !wait_bounded(xempty(s), ((i / kXStages) - 1) & 1, wc)) break;
+            Ring<kXStages> rx(0);
+            for (int i = 0; i < nunits; ++i, cur.step(p.KB), rx.step(1)) {
+                const int s = rx.slot;
+                if (i >= kXStages && !wait_bounded(xempty(s), rx.phase ^ 1u, wc)) break;
                 const uint32_t st = base + L::kXOff + s * L::kXSlot;
                 mbar_arrive_expect_tx(xfull(s), L::kXSlot);
                 tma_load_2d(st, &tmX, xfull(s), cur.kr * 128, 0, pol_x);
@@ -395,12 +415,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t idesc = idesc_f16(NMMA, F::kBf16);
             const uint64_t desc0 = smem_desc_sw128(base + L::kXOff);
             int last = -1;
-            for (int i = first; i < nunits; i += kIssuers) {
-                const int s = i % kXStages;
-                const int a = i % kNA;
-                if (!warp_wait(xfull(s), (i / kXStages) & 1, wc)) break;
-                if (!warp_wait(afull(a), (i / kNA) & 1, wc)) break;
-                if (i >= kNA && !warp_wait(dempty(a), ((i / kNA) - 1) & 1, wc)) break;
+            Ring<kXStages> rx(first);
+            Ring<kNA> ra(first);
+            for (int i = first; i < nunits; i += kIssuers, rx.step(kIssuers), ra.step(kIssuers)) {
+                const int s = rx.slot;
+                const int a = ra.slot;
+                if (!warp_wait(xfull(s), rx.phase, wc)) break;
+                if (!warp_wait(afull(a), ra.phase, wc)) break;
+                if (i >= kNA && !warp_wait(dempty(a), ra.phase ^ 1u, wc)) break;
                 tc_fence_after();
                 // the descriptor's start-address field counts 16-byte units
                 const uint64_t xd = desc0 + static_cast<uint64_t>((s * L::kXSlot) >> 4);
@@ -443,17 +465,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         float sc_cur = batch_scale(0);
         float sc_next = batch_scale(1);
         Cursor cur(u0, p.KB);
-        for (int i = 0; i < nunits; ++i, cur.step(p.KB)) {
+        Ring<kNA> ra(0);
+        Ring<kXStages> rx(0);
+        for (int i = 0; i < nunits; ++i, cur.step(p.KB), ra.step(1), rx.step(1)) {
             const long long u = u0 + i;
             const int tile = cur.tile;
             const int kb = cur.kb;
-            const int a = i % kNA;
+            const int a = ra.slot;
             if ((i & 31) == 0 && i > 0) {
                 sc_cur = sc_next;
                 sc_next = batch_scale((i >> 5) + 1);
             }
             const float sc = __shfl_sync(0xffffffffu, sc_cur, i & 31);
-            if (!warp_wait(dfull(a), (i / kNA) & 1, wc)) break;
+            if (!warp_wait(dfull(a), ra.phase, wc)) break;
             tc_fence_after();
             uint32_t v0[16], v1[16];
             tmem_ld_x16(tl + kDCol0 + a * NMMA, v0);
@@ -465,7 +489,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the unit's MMAs are complete, so its X slot can be refilled (one
             // arrival suffices; a commit in the MMA stream would cost about as
             // much as another MMA)
-            if (warp == kWarpFold0 && lane == 0) mbar_arrive(xempty(i % kXStages));
+            if (warp == kWarpFold0 && lane == 0) mbar_arrive(xempty(rx.slot));
 #pragma unroll
             for (int m = 0; m < 16; ++m) outer[m] = F::fold(outer[m], __uint_as_float(v0[m]), sc);
             if constexpr (NMMA == 32) {
@@ -485,24 +509,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row = q * 32 + lane;
         const uint32_t tl = tmem + (static_cast<uint32_t>(q * 32) << 16);
         typename F::Deq dq(p, u0, grp, nunits, row);
+        // Rings of the unit being converted (weight stage, A buffer) and of the
+        // next unit issued (weight stage); the group's units are 2 apart.
+        Ring<kWStages> rw(grp);
+        Ring<kWStages> rwn(grp);
+        Ring<kNA> ra(grp);
         // The group's next unit is loaded from shared memory into the other
         // register slot before the current one is converted, so the load
         // latency overlaps the conversion.  Unit i's weights into `slot`:
         auto issue = [&](int i, int slot) -> bool {
-            const int s = i % kWStages;
+            const int s = rwn.slot;
+            const uint32_t ph = rwn.phase;
+            rwn.step(2);
             dq.prepare(p, i, nunits, row, slot);
-            if (!warp_wait(wfull(s), (i / kWStages) & 1, wc)) return false;
+            if (!warp_wait(wfull(s), ph, wc)) return false;
             dq.load(slot, gbase + s * F::kWBytes, row);
             return true;
         };
         // unit i (already loaded into `slot`); false when a wait gave up
         auto unit = [&](int i, int slot, int nslot) -> bool {
-            const int a = i % kNA;
+            const int a = ra.slot;
+            const uint32_t aph = ra.phase;
+            const int sw = rw.slot;
+            ra.step(2);
+            rw.step(2);
             const int inext = i + 2;
             const bool more = inext < nunits;
             if (more && !issue(inext, nslot)) return false;
             // unit i - kNA (this group's) is done with its A buffer once its MMAs are
-            if (i >= kNA && !warp_wait(dfull(a), ((i - kNA) / kNA) & 1, wc)) return false;
+            if (i >= kNA && !warp_wait(dfull(a), aph ^ 1u, wc)) return false;
             __syncwarp();
             tc_fence_after();
 #pragma unroll
@@ -519,7 +554,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // in-order issue can put the arrive first), and a store cannot issue
             // before the registers it reads are written.
             __syncwarp();
-            if (lane == 0) mbar_arrive(wempty(i % kWStages));
+            if (lane == 0) mbar_arrive(wempty(sw));
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
