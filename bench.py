@@ -483,7 +483,9 @@ def main():
         "data": "synthetic",
         "config": {"workload": "fp8_block gate/up M=16 N=17408 K=5120",
                    "M": M, "N": N, "K": K, "weights": "E4M3 [N,K] + FP32 [128x128] block scales",
-                   "arith": "E4M3->BF16 exact dequant, BF16 x BF16 tcgen05 MMA, FP32 two-level fold, BF16 out",
+                   "arith": "E4M3 weights as stored into tcgen05 kind::f8f6f4 (no weight dequant); BF16 X split "
+                            "per (row, 128-K block) into two power-of-two-scaled E4M3 planes; FP32 two-level fold; "
+                            "BF16 out",
                    "l2": f"inputs larger than L2: {copies} rotating weight copies ({copies * N * K / 1e6:.0f} MB)",
                    "overlap": "weight prefetch overlaps the previous call" if args.overlap else "off",
                    "parallelism": "replicas" if world > 1 else "1 GPU"},
