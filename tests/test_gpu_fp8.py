@@ -208,3 +208,41 @@ def test_back_to_back_calls_bit_identical(M, N, K, cid):
         y = to_bits(Y)
         assert np.array_equal(y, first), f"call {i}: {int((y != first).sum())} elements differ"
     _check(p, outs[0])
+
+
+def _wide_range_x(rng, M, K, binades):
+    """BF16 activations whose magnitudes are log-uniform over `binades`
+    binades below 4 (random signs), so that every 128-wide block holds values
+    far apart in size."""
+    mag = np.exp2(rng.uniform(-binades, 0.0, size=(M, K))) * 4.0
+    sign = np.where(rng.random((M, K)) < 0.5, -1.0, 1.0)
+    return wl.bf16_bits_from_f32((mag * sign).astype(np.float32))
+
+
+@pytest.mark.parametrize("binades", [12, 24])
+def test_wide_dynamic_range_activations(binades):
+    """The E4M3 tensor-core path splits each (row, 128-K block) of X into two
+    power-of-two-scaled E4M3 planes; values within 2^13 of their block's
+    maximum are represented exactly, smaller ones to within 2^-21 of it.  Rows
+    spanning 12 binades (all exact) and 24 binades (many elements below the
+    exact window) must both meet the comparison rule."""
+    M, N, K = 16, 1024, 2048
+    rng = np.random.default_rng(77 + binades)
+    base = _problem(M, N, K, 44)
+    Xb = _wide_range_x(rng, M, K, binades)
+    p = wl.Fp8Problem(M, N, K, Xb, base.W, base.S)
+    _check(p, Fp8Device(p).run())
+
+
+def test_zero_rows_and_zero_blocks_in_x():
+    """All-zero X rows and all-zero 128-wide blocks inside a row (the split
+    takes no exponent from an empty block) alongside normal data."""
+    M, N, K = 8, 512, 1024
+    base = _problem(M, N, K, 45)
+    X = base.X.copy()
+    X[3] = 0                    # a whole row of +0
+    X[5, 128:256] = 0x8000      # a block of -0
+    X[6, :128] = 0
+    p = wl.Fp8Problem(M, N, K, X, base.W, base.S)
+    y, _ = _check(p, Fp8Device(p).run())
+    assert np.all((y[3] & 0x7FFF) == 0)

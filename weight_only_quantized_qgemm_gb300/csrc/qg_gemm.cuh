@@ -86,11 +86,15 @@ struct Params {
 
 template <int NMMA, int WBYTES>
 struct Layout {
-    // A buffers in TMEM (64 columns each), one accumulator (NMMA columns) each:
-    // as many as fit in the 512 columns, an even number
-    static constexpr int kNA = NMMA == 16 ? 6 : 4;
-    static constexpr int kDCol0 = kNA * 64;               // accumulator a at kDCol0 + NMMA a
-    static_assert(kDCol0 + kNA * NMMA <= kTmemCols, "TMEM columns");
+    // TMEM: kNA A buffers (64 columns, 128 rows x 128 K of 16-bit weights),
+    // then four accumulators of NMMA columns: one per MMA issuer for each of
+    // two tile pieces in flight (a piece = the units of one tile in this CTA's
+    // range).  The format has no per-block fold scale, so a piece's MMAs
+    // accumulate in TMEM across its K blocks and the fold reads each piece
+    // once instead of once per unit.
+    static constexpr int kNA = 6;
+    static constexpr int kDCol0 = kNA * 64;               // accumulator (b, j) at kDCol0 + NMMA (2 b + j)
+    static_assert(kDCol0 + 4 * NMMA <= kTmemCols, "TMEM columns");
     static constexpr int kXSlot = NMMA * 256;             // two 64-element X boxes
     static constexpr int kXBox = NMMA * 128;
     // X slots: as many as leave the weight ring 8 stages (the X copies then run
@@ -106,12 +110,12 @@ struct Layout {
     static constexpr int kWStages = kWFit & ~1;
     static constexpr int kXOff = kWStages * WBYTES;
     static constexpr int kBarOff = kXOff + kXStages * kXSlot;
-    static constexpr int kNumBars = 2 * kWStages + 2 * kXStages + 3 * kNA;
+    static constexpr int kNumBars = 2 * kWStages + 2 * kXStages + 2 * kNA + 6;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     static constexpr int kSmemBytes = kMiscOff + 64 + 1024;  // + alignment slack
     static_assert(WBYTES % 1024 == 0 && kXSlot % 1024 == 0, "keep the 1024-byte swizzle alignment");
     static_assert(kXStages >= kNA, "X copies run at least as far ahead as the dequant");
-    // the same ownership rule for the other rings: an X stage and an A/D buffer
+    // the same ownership rule for the other rings: an X stage and an A buffer
     // are always used by the same MMA issuer and the same dequant group
     static_assert(kXStages % kIssuers == 0 && kNA % kIssuers == 0 && kNA % 2 == 0, "ring ownership");
     static_assert(kWStages >= 8, "the weight ring must cover HBM latency");
@@ -320,8 +324,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto xempty = [&](int s) { return bar0 + 8u * (2 * kWStages + kXStages + s); };
     constexpr int kBarA = 2 * kWStages + 2 * kXStages;
     auto afull = [&](int a) { return bar0 + 8u * (kBarA + a); };
-    auto dfull = [&](int a) { return bar0 + 8u * (kBarA + kNA + a); };
-    auto dempty = [&](int a) { return bar0 + 8u * (kBarA + 2 * kNA + a); };
+    auto afree = [&](int a) { return bar0 + 8u * (kBarA + kNA + a); };
+    // accumulator (b, j) of piece buffer b, issuer j: complete / drained
+    auto dfull = [&](int b, int j) { return bar0 + 8u * (kBarA + 2 * kNA + 2 * b + j); };
+    auto dempty = [&](int b) { return bar0 + 8u * (kBarA + 2 * kNA + 4 + b); };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + L::kMiscOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + L::kMiscOff + 4);
 
@@ -339,12 +345,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int s = 0; s < kXStages; ++s) {
             mbar_init(xfull(s), 1);
-            mbar_init(xempty(s), 1);   // fold warp 2, once the unit's MMAs are complete
+            mbar_init(xempty(s), 1);   // commit: the unit's MMAs are complete
         }
         for (int a = 0; a < kNA; ++a) {
-            mbar_init(afull(a), 4);
-            mbar_init(dfull(a), 1);
-            mbar_init(dempty(a), 4);
+            mbar_init(afull(a), 4);   // the four warps of the dequant group
+            mbar_init(afree(a), 1);   // commit: the unit's MMAs are complete
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(dfull(b, 0), 1);   // commit: the issuer's last MMAs of the piece are complete
+            mbar_init(dfull(b, 1), 1);
+            mbar_init(dempty(b), 4);     // the four fold warps
         }
         *abort_flag = 0;
         fence_barrier_init();
@@ -406,101 +416,119 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1 || warp == kWarpMma2) {
         // ------------------------------------------------------------ MMA issuers
-        // The whole warp runs the loop and its waits (the per-unit values stay
-        // warp-uniform); one elected lane issues the MMAs and the commit.  This
-        // issues measurably faster than a loop confined to lane 0.
+        // Issuer j takes units i with i % 2 == j and accumulates them into its
+        // own accumulator of the piece's buffer b = piece % 2 (two issuers never
+        // write one accumulator).  The whole warp runs the loop and its waits;
+        // one elected lane issues the MMAs and the commits: X slot free and A
+        // buffer free after every unit, accumulator complete after the
+        // issuer's last unit of the piece.
+        //
+        // Before its first unit of piece p >= 2 an issuer waits for the fold to
+        // have drained piece p - 2 (the same buffer).  Only the first and the
+        // last piece of a CTA's range can be a single unit (every other piece
+        // is a whole tile of KB >= 2 units, or every piece is a single unit and
+        // each issuer keeps to one buffer), so an issuer that skipped piece
+        // p - 2 did so for p - 2 = 0 and the parity wait is unambiguous.
         {
             const bool elected = elect_one();
-            const int first = warp == 1 ? 0 : 1;
+            const int j = warp == 1 ? 0 : 1;
             constexpr uint32_t idesc = idesc_f16(NMMA, F::kBf16);
             const uint64_t desc0 = smem_desc_sw128(base + L::kXOff);
+            const int first_tile = static_cast<int>(u0 / p.KB);
             int last = -1;
-            Ring<kXStages> rx(first);
-            Ring<kNA> ra(first);
-            for (int i = first; i < nunits; i += kIssuers, rx.step(kIssuers), ra.step(kIssuers)) {
+            int last_a = 0;
+            uint32_t last_aph = 0;
+            int piece = -1;
+            Ring<kXStages> rx(j);
+            Ring<kNA> ra(j);
+            Cursor cur(u0 + j, p.KB);
+            for (int i = j; i < nunits; i += kIssuers, rx.step(kIssuers), ra.step(kIssuers), cur.step(kIssuers, p.KB)) {
                 const int s = rx.slot;
                 const int a = ra.slot;
+                const int pc = cur.tile - first_tile;
+                const int b = pc & 1;
+                const bool fresh = pc != piece;   // the issuer's first unit of this piece
+                if (fresh) {
+                    piece = pc;
+                    if (pc >= 2 && !warp_wait(dempty(b), static_cast<uint32_t>(((pc >> 1) - 1) & 1), wc)) break;
+                }
                 if (!warp_wait(xfull(s), rx.phase, wc)) break;
                 if (!warp_wait(afull(a), ra.phase, wc)) break;
-                if (i >= kNA && !warp_wait(dempty(a), ra.phase ^ 1u, wc)) break;
                 tc_fence_after();
+                // the issuer's last unit of the piece: its next unit is past the
+                // range or in the next tile
+                const bool closes = i + kIssuers >= nunits || cur.kb + kIssuers >= p.KB;
                 // the descriptor's start-address field counts 16-byte units
                 const uint64_t xd = desc0 + static_cast<uint64_t>((s * L::kXSlot) >> 4);
-                const uint32_t dt = tmem + kDCol0 + a * NMMA;
+                const uint32_t dt = tmem + kDCol0 + (2 * b + j) * NMMA;
                 const uint32_t at = tmem + a * 64;
                 if (elected) {
 #pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        mma_ts_f16(dt, at + j * 8, xd + (((j >> 2) * L::kXBox + (j & 3) * 32) >> 4), idesc,
-                                   j > 0 ? 1u : 0u);
-                    tc_commit(dfull(a));
+                    for (int k = 0; k < 8; ++k)
+                        mma_ts_f16(dt, at + k * 8, xd + (((k >> 2) * L::kXBox + (k & 3) * 32) >> 4), idesc,
+                                   (k > 0 || !fresh) ? 1u : 0u);
+                    tc_commit(xempty(s));
+                    tc_commit(afree(a));
+                    if (closes) tc_commit(dfull(b, j));
                 }
                 __syncwarp();
                 last = i;
+                last_a = a;
+                last_aph = ra.phase;
             }
-            if (last >= 0 && elected) drain_wait(dfull(last % kNA), (last / kNA) & 1, p.timeout_ns);
+            if (last >= 0 && elected) drain_wait(afree(last_a), last_aph, p.timeout_ns);
         }
     } else if (warp < kWarpDeq0) {
         // ------------------------------------------------------------ fold / epilogue
+        // One pass per piece: wait for the accumulators of the issuers that
+        // had units in it, add them, release the buffer, store or reduce.
         const int q = warp & 3;
         const uint32_t tl = tmem + (static_cast<uint32_t>(q * 32) << 16);
         const int first_tile = static_cast<int>(u0 / p.KB);
         const int split_info = split_info_lane(p, u0, u1, lane);
         // Y and the workspace may still be in use by the preceding grid
         grid_dependency_wait();
-        float outer[NMMA];
-#pragma unroll
-        for (int m = 0; m < NMMA; ++m) outer[m] = 0.0f;
-        // Block scales, 32 units per batch: lane l holds the scale of unit
-        // 32 b + l of the current batch and of the next one, which is fetched a
-        // whole batch ahead, so the per-unit value is a register shuffle and the
-        // load latency never meets the fold.
-        auto batch_scale = [&](int b) -> float {
-            if (!F::kHasFoldScale) return 1.0f;
-            const int i = 32 * b + lane;
-            if (i >= nunits) return 0.0f;
-            Cursor c(u0 + i, p.KB);
-            return __ldg(F::fold_scale_ptr(p, c.tile, c.kr));
-        };
-        float sc_cur = batch_scale(0);
-        float sc_next = batch_scale(1);
-        Cursor cur(u0, p.KB);
-        Ring<kNA> ra(0);
-        Ring<kXStages> rx(0);
-        for (int i = 0; i < nunits; ++i, cur.step(p.KB), ra.step(1), rx.step(1)) {
-            const long long u = u0 + i;
-            const int tile = cur.tile;
-            const int kb = cur.kb;
-            const int a = ra.slot;
-            if ((i & 31) == 0 && i > 0) {
-                sc_cur = sc_next;
-                sc_next = batch_scale((i >> 5) + 1);
+        uint32_t done[2][2] = {{0u, 0u}, {0u, 0u}};   // completions seen per accumulator
+        auto load_acc = [&](int b, int j, uint32_t (&v)[NMMA]) {
+            const uint32_t col = tl + kDCol0 + (2 * b + j) * NMMA;
+            uint32_t (&v0)[16] = *reinterpret_cast<uint32_t (*)[16]>(&v[0]);
+            tmem_ld_x16(col, v0);
+            if constexpr (NMMA == 32) {
+                uint32_t (&v1)[16] = *reinterpret_cast<uint32_t (*)[16]>(&v[16]);
+                tmem_ld_x16(col + 16, v1);
             }
-            const float sc = __shfl_sync(0xffffffffu, sc_cur, i & 31);
-            if (!warp_wait(dfull(a), ra.phase, wc)) break;
+        };
+        int ps = 0;
+        int kb0 = static_cast<int>(u0 % p.KB);
+        for (int pc = 0; ps < nunits; ++pc) {
+            const int tile = first_tile + pc;
+            const int b = pc & 1;
+            int pe = ps + (p.KB - kb0) - 1;   // last unit of the piece
+            if (pe > nunits - 1) pe = nunits - 1;
+            const int kb_end = kb0 + (pe - ps);
+            const bool two = pe > ps;
+            const int j0 = ps & 1;
+            if (!warp_wait(dfull(b, j0), done[b][j0] & 1u, wc)) break;
+            ++done[b][j0];
+            if (two) {
+                if (!warp_wait(dfull(b, j0 ^ 1), done[b][j0 ^ 1] & 1u, wc)) break;
+                ++done[b][j0 ^ 1];
+            }
             tc_fence_after();
-            uint32_t v0[16], v1[16];
-            tmem_ld_x16(tl + kDCol0 + a * NMMA, v0);
-            if constexpr (NMMA == 32) tmem_ld_x16(tl + kDCol0 + a * NMMA + 16, v1);
+            uint32_t v[NMMA], w[NMMA];
+            load_acc(b, j0, v);
+            if (two) load_acc(b, j0 ^ 1, w);
             tmem_wait_ld();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(dempty(a));
-            // the unit's MMAs are complete, so its X slot can be refilled (one
-            // arrival suffices; a commit in the MMA stream would cost about as
-            // much as another MMA)
-            if (warp == kWarpFold0 && lane == 0) mbar_arrive(xempty(rx.slot));
+            if (lane == 0) mbar_arrive(dempty(b));
+            float outer[NMMA];
 #pragma unroll
-            for (int m = 0; m < 16; ++m) outer[m] = F::fold(outer[m], __uint_as_float(v0[m]), sc);
-            if constexpr (NMMA == 32) {
-#pragma unroll
-                for (int m = 0; m < 16; ++m) outer[16 + m] = F::fold(outer[16 + m], __uint_as_float(v1[m]), sc);
-            }
-
-            if (kb != p.KB - 1 && u != u1 - 1) continue;
-            end_piece<NMMA, F>(p, outer, tile, kb, u, u0, first_tile, split_info, q, lane);
-#pragma unroll
-            for (int m = 0; m < NMMA; ++m) outer[m] = 0.0f;
+            for (int m = 0; m < NMMA; ++m)
+                outer[m] = two ? __fadd_rn(__uint_as_float(v[m]), __uint_as_float(w[m])) : __uint_as_float(v[m]);
+            end_piece<NMMA, F>(p, outer, tile, kb_end, u0 + pe, u0, first_tile, split_info, q, lane);
+            ps = pe + 1;
+            kb0 = 0;
         }
     } else {
         // ------------------------------------------------------------ dequant
@@ -537,7 +565,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool more = inext < nunits;
             if (more && !issue(inext, nslot)) return false;
             // unit i - kNA (this group's) is done with its A buffer once its MMAs are
-            if (i >= kNA && !warp_wait(dfull(a), aph ^ 1u, wc)) return false;
+            if (i >= kNA && !warp_wait(afree(a), aph ^ 1u, wc)) return false;
             __syncwarp();
             tc_fence_after();
 #pragma unroll

@@ -29,9 +29,6 @@ struct Lut3Fmt {
         const size_t off = (static_cast<size_t>(tile) * p.KT + (kb >> 1)) * 16384 + (kb & 1) * kWBytes;
         bulk_load(dst, p.Wq + off, kWBytes, bar, pol);
     }
-    static constexpr bool kHasFoldScale = false;
-    __device__ static const float* fold_scale_ptr(const gemm::Params&, int, int) { return nullptr; }
-    __device__ static float fold(float outer, float inner, float) { return __fadd_rn(outer, inner); }
     __device__ static void store(void* Y, int64_t idx, float v) {
         static_cast<__half*>(Y)[idx] = __float2half_rn(v);
     }
