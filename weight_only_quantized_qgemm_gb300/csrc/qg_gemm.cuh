@@ -51,11 +51,20 @@
 namespace qg {
 namespace gemm {
 
-constexpr int kThreads = 512;
 constexpr int kWarpFold0 = 2;
 constexpr int kWarpDeq0 = 6;
-constexpr int kWarpMma2 = 14;
-constexpr int kWarpXProd = 15;
+
+// Warp roles for an MMA width: dequant groups of four warps (one per TMEM lane
+// quadrant) taking every kDeqGroups-th unit, then the second MMA issuer and the
+// X producer.  Three groups at N = 16 (20 warps); two at N = 32, whose wider
+// fold needs the registers of a 16-warp CTA.
+template <int NMMA>
+struct Roles {
+    static constexpr int kDeqGroups = NMMA == 16 ? 3 : 2;
+    static constexpr int kWarpMma2 = kWarpDeq0 + 4 * kDeqGroups;
+    static constexpr int kWarpXProd = kWarpMma2 + 1;
+    static constexpr int kThreads = 32 * (kWarpXProd + 1);
+};
 constexpr int kIssuers = 2;
 constexpr int kTmemCols = 512;
 
@@ -101,13 +110,15 @@ struct Layout {
     // far enough ahead of the MMA to hide their latency behind the weight stream)
     static constexpr int kXStages = (NMMA == 16 ? 3 : 2) * kNA;
     static constexpr int kWBudget = 212992 - kXStages * kXSlot;   // 208 KB in all
-    // Even, so that every use of a weight stage falls to the same dequant group
-    // (units i and i + kWStages have the same parity).  A group's parity wait
-    // on a stage is then always for the phase right after one it has already
-    // seen; with an odd count it could be for a phase after the other group's
-    // still-pending one, and a parity wait cannot tell those two apart.
+    // A multiple of the dequant group count, so that every use of a weight stage
+    // falls to the same dequant group (units i and i + kWStages are taken by
+    // the same group).  A group's parity wait on a stage is then always for the
+    // phase right after one it has already seen; otherwise it could be for a
+    // phase after another group's still-pending one, and a parity wait cannot
+    // tell those two apart.
+    static constexpr int kG = Roles<NMMA>::kDeqGroups;
     static constexpr int kWFit = (kWBudget / WBYTES) < 24 ? (kWBudget / WBYTES) : 24;
-    static constexpr int kWStages = kWFit & ~1;
+    static constexpr int kWStages = kWFit / kG * kG;
     static constexpr int kXOff = kWStages * WBYTES;
     static constexpr int kBarOff = kXOff + kXStages * kXSlot;
     static constexpr int kNumBars = 2 * kWStages + 2 * kXStages + 2 * kNA + 6;
@@ -117,9 +128,9 @@ struct Layout {
     static_assert(kXStages >= kNA, "X copies run at least as far ahead as the dequant");
     // the same ownership rule for the other rings: an X stage and an A buffer
     // are always used by the same MMA issuer and the same dequant group
-    static_assert(kXStages % kIssuers == 0 && kNA % kIssuers == 0 && kNA % 2 == 0, "ring ownership");
+    static_assert(kXStages % kIssuers == 0 && kNA % kIssuers == 0 && kNA % kG == 0, "ring ownership");
     static_assert(kWStages >= 8, "the weight ring must cover HBM latency");
-    static_assert(kWStages % 2 == 0, "a weight stage must belong to one dequant group");
+    static_assert(kWStages % kG == 0, "a weight stage must belong to one dequant group");
     static_assert(kSmemBytes <= 232448, "shared memory");
 };
 
@@ -228,7 +239,7 @@ __device__ __forceinline__ int split_info_lane(const Params& p, long long u0, lo
 // workspace, and the last of the tile's CTAs to arrive sums every piece in
 // ascending K order and stores the tile.  Store::store(Y, index, value)
 // writes one output element.
-template <int NOUT, class Store>
+template <int NOUT, class Store, int kBatch = (NOUT == 16 ? 2 : 1)>
 __device__ __forceinline__ void end_piece(const Params& p, const float (&outer)[NOUT], int tile, int kb,
                                           long long u, long long u0, int first_tile, int split_info, int q,
                                           int lane) {
@@ -268,7 +279,6 @@ __device__ __forceinline__ void end_piece(const Params& p, const float (&outer)[
     // piece included (just stored above), loading kBatch pieces at a time so
     // that their latencies overlap.
     __threadfence();
-    constexpr int kBatch = NOUT == 16 ? 2 : 1;
     float acc[NOUT];
 #pragma unroll
     for (int m = 0; m < NOUT; ++m) acc[m] = 0.0f;
@@ -304,10 +314,13 @@ __device__ __forceinline__ void end_piece(const Params& p, const float (&outer)[
 }
 
 template <int NMMA, class F>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Roles<NMMA>::kThreads, 1)
     qgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                  const Params p) {
     using L = Layout<NMMA, F::kWBytes>;
+    constexpr int kDeqGroups = Roles<NMMA>::kDeqGroups;
+    constexpr int kWarpMma2 = Roles<NMMA>::kWarpMma2;
+    constexpr int kWarpXProd = Roles<NMMA>::kWarpXProd;
     constexpr int kWStages = L::kWStages;
     constexpr int kXStages = L::kXStages;
     constexpr int kNA = L::kNA;
@@ -533,12 +546,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ------------------------------------------------------------ dequant
         const int q = warp & 3;
-        const int grp = (warp - kWarpDeq0) >> 2;   // takes units i with i % 2 == grp
+        const int grp = (warp - kWarpDeq0) >> 2;   // takes units i with i % kDeqGroups == grp
         const int row = q * 32 + lane;
         const uint32_t tl = tmem + (static_cast<uint32_t>(q * 32) << 16);
-        typename F::Deq dq(p, u0, grp, nunits, row);
+        typename F::Deq dq(p, u0, grp, kDeqGroups, nunits, row);
         // Rings of the unit being converted (weight stage, A buffer) and of the
-        // next unit issued (weight stage); the group's units are 2 apart.
+        // next unit issued (weight stage); the group's units are kDeqGroups apart.
         Ring<kWStages> rw(grp);
         Ring<kWStages> rwn(grp);
         Ring<kNA> ra(grp);
@@ -548,7 +561,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto issue = [&](int i, int slot) -> bool {
             const int s = rwn.slot;
             const uint32_t ph = rwn.phase;
-            rwn.step(2);
+            rwn.step(kDeqGroups);
             dq.prepare(p, i, nunits, row, slot);
             if (!warp_wait(wfull(s), ph, wc)) return false;
             dq.load(slot, gbase + s * F::kWBytes, row);
@@ -559,9 +572,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int a = ra.slot;
             const uint32_t aph = ra.phase;
             const int sw = rw.slot;
-            ra.step(2);
-            rw.step(2);
-            const int inext = i + 2;
+            ra.step(kDeqGroups);
+            rw.step(kDeqGroups);
+            const int inext = i + kDeqGroups;
             const bool more = inext < nunits;
             if (more && !issue(inext, nslot)) return false;
             // unit i - kNA (this group's) is done with its A buffer once its MMAs are
@@ -594,10 +607,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         constexpr int kU = F::Deq::kUnroll;
         static_assert(kU % 2 == 0, "two register slots alternate");
         bool ok = grp < nunits && issue(grp, 0);
-        for (int i0 = grp; i0 < nunits && ok; i0 += 2 * kU) {
+        for (int i0 = grp; i0 < nunits && ok; i0 += kDeqGroups * kU) {
 #pragma unroll
             for (int j = 0; j < kU; ++j) {
-                const int i = i0 + 2 * j;
+                const int i = i0 + kDeqGroups * j;
                 if (i < nunits && ok) ok = unit(i, j, (j + 1) % kU);
             }
         }
@@ -628,7 +641,7 @@ cudaError_t launch(const Params& prm, const Schedule& s, const CUtensorMap& tmW,
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(s.G));
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(Roles<NMMA>::kThreads);
     cfg.dynamicSmemBytes = L::kSmemBytes;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];

@@ -12,8 +12,9 @@
 // two FP16 byte planes in registers and looks codes up with byte permutes
 // whose selector is the code word itself (8 values = 1 shift + 8 permutes; no
 // shared-memory table).  The scale is applied once per table entry, which
-// gives the same FP16 values as scaling every weight.  Per-unit accumulators
-// are summed in FP32 by the fold warps (fold scale 1).
+// gives the same FP16 values as scaling every weight.  There is no per-block
+// fold scale: the MMAs of a tile piece accumulate in TMEM (FP32) and the fold
+// warps add the two MMA issuers' accumulators once per piece.
 #include "qg_gemm.cuh"
 
 namespace qg {
@@ -48,28 +49,30 @@ struct Lut3Fmt {
         uint32_t scq[kUnroll];
         LutPlanes t[2];
         gemm::Cursor ahead;   // the unit whose scale is fetched next
+        int G;                // dequant groups: this thread's units are G apart
         __device__ static uint32_t scale_of(const gemm::Params& p, const gemm::Cursor& c, int row) {
             const int n = c.tile * 128 + row;
             return n < p.N ? static_cast<uint32_t>(__ldg(p.lut_scales + static_cast<int64_t>(n) * p.ld_lut_scales + c.kr))
                            : 0u;
         }
-        // this thread handles units grp, grp + 2, grp + 4, ...; slot j holds the
+        // this thread handles units grp, grp + G, grp + 2 G, ... (G dequant
+        // groups); slot j holds the
         // scale of its j-th unit modulo kUnroll
-        __device__ Deq(const gemm::Params& p, long long u0, int grp, int nunits, int row)
-            : qm(__ldg(p.qmap)), ahead(u0 + grp, p.KB) {
+        __device__ Deq(const gemm::Params& p, long long u0, int grp, int groups, int nunits, int row)
+            : qm(__ldg(p.qmap)), ahead(u0 + grp, p.KB), G(groups) {
 #pragma unroll
             for (int j = 0; j < kUnroll; ++j) {
-                const int i = grp + 2 * j;
+                const int i = grp + G * j;
                 scq[j] = i < nunits ? scale_of(p, ahead, row) : 0u;
-                ahead.step(2, p.KB);
+                ahead.step(G, p.KB);
             }
         }
         // called for each of the group's units in order, just before load()
         __device__ void prepare(const gemm::Params& p, int i, int nunits, int row, int slot) {
             sc[slot & 1] = scq[slot];
-            const int inext = i + 2 * kUnroll;
+            const int inext = i + G * kUnroll;
             scq[slot] = inext < nunits ? scale_of(p, ahead, row) : 0u;
-            ahead.step(2, p.KB);
+            ahead.step(G, p.KB);
         }
         __device__ void load(int slot, const uint8_t* stage, int row) {
             const int b = slot & 1;
