@@ -117,7 +117,11 @@ struct Layout {
     // phase after another group's still-pending one, and a parity wait cannot
     // tell those two apart.
     static constexpr int kG = Roles<NMMA>::kDeqGroups;
-    static constexpr int kWFit = (kWBudget / WBYTES) < 24 ? (kWBudget / WBYTES) : 24;
+    // Not deeper: the X copies queue behind the code copies in flight (one TMA
+    // queue per SM), so every extra stage delays X by as much.  Measured on
+    // the 28672 x 8192 shape: 9 stages 37.9 us, 12 38.9, 15 39.0, 6 48 (the
+    // code stream starves).
+    static constexpr int kWFit = (kWBudget / WBYTES) < 9 ? (kWBudget / WBYTES) : 9;
     static constexpr int kWStages = kWFit / kG * kG;
     static constexpr int kXOff = kWStages * WBYTES;
     static constexpr int kBarOff = kXOff + kXStages * kXSlot;

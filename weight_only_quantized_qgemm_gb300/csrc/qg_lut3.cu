@@ -42,7 +42,7 @@ struct Lut3Fmt {
     // group's next unit into one while it converts the current unit from the
     // other.
     struct Deq {
-        static constexpr int kUnroll = 4;
+        static constexpr int kUnroll = 2;
         uint4 qm;
         uint4 c[2][4];
         uint32_t sc[2];
