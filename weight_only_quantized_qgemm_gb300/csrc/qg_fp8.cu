@@ -31,9 +31,8 @@
 //                that free the unit's weight stage and X planes and mark its
 //                accumulator ready once the MMAs complete.
 //   warps 3-6    fold / epilogue, one per TMEM lane quadrant (warp % 4).
-//   warps 7-14   X split: four groups of 2 warps taking every fourth unit (two
-//                groups of 4 warps, alternate units, for 32 rows), 32
-//                elements of a row per thread.  Each
+//   warps 7-14   X split: four groups of 2 warps taking every fourth unit, 32
+//                (64 for 32 rows) elements of a row per thread.  Each
 //                thread copies its own share of a unit's BF16 X slice several
 //                units ahead (cp.async through the load/store path: a TMA copy
 //                would queue behind the weight tiles already in flight and
@@ -57,14 +56,16 @@ constexpr int kWarpMma0 = 1;      // warps 1, 2
 constexpr int kIssuers = 2;
 constexpr int kWarpFold0 = 3;     // warps 3..6: TMEM lane quadrant warp % 4
 constexpr int kFoldWarps = 4;
-constexpr int kWarpConv0 = 7;     // then two groups of split warps
-constexpr int kEpt = 32;          // X elements per split thread and unit
-constexpr int kLpr = 128 / kEpt;  // split lanes per row
+constexpr int kWarpConv0 = 7;     // then the split warps
 
+// X split: four groups of two warps, taking units i with i % 4 == g; a
+// thread owns kEpt elements of one row (32 at up to 16 rows, 64 at 32).
 template <int NX>
 struct Split {
-    static constexpr int kWarps = NX * kLpr / 32;   // per group: 2 or 4
-    static constexpr int kGroups = NX == 16 ? 4 : 2; // taking units i with i % kGroups == g
+    static constexpr int kEpt = NX == 16 ? 32 : 64;   // X elements per split thread and unit
+    static constexpr int kLpr = 128 / kEpt;           // split lanes per row
+    static constexpr int kWarps = NX * kLpr / 32;     // per group: 2
+    static constexpr int kGroups = 4;
     static constexpr int kThreads = 32 * (kWarpConv0 + kGroups * kWarps);
 };
 
@@ -74,7 +75,7 @@ struct Fp8Layout {
     static constexpr int kWBytes = 128 * 128;    // one E4M3 unit
     static constexpr int kXbSlot = NX * 256;     // BF16 X slice, [16-byte chunk j][split thread of the group]
     static constexpr int kX8Slot = kN * 128;     // both planes, 128-byte rows
-    static constexpr int kXAhead = NX == 16 ? 1 : 2;   // a group's units of X copied ahead
+    static constexpr int kXAhead = 1;                  // a group's units of X copied ahead
     static constexpr int kXbStages = kXAhead + 1;      // per group
     // X plane slots: a slot is refilled once the MMAs that read it complete, so
     // the ring has to cover the split latency plus the MMA latency
@@ -86,7 +87,7 @@ struct Fp8Layout {
     // i - kX8Stages completed, which were issued after the fold released unit
     // i - kX8Stages - kNA's accumulator, having read its factors; so the fold is
     // done with every unit before i - kX8Stages - kNA >= i - kFacStages.
-    static constexpr int kFacStages = 16;
+    static constexpr int kFacStages = NX == 16 ? 16 : 8;
     static constexpr int kFacBytes = kFacStages * NX * 4;
     static constexpr int kMaxWStages = 16;
     static constexpr int kFixed = Split<NX>::kGroups * kXbStages * kXbSlot + kX8Stages * kX8Slot + kFacBytes +
@@ -204,10 +205,12 @@ __global__ void __launch_bounds__(Split<NX>::kThreads, 1)
     } else if (warp >= kWarpConv0) {
         // ------------------------------------------------------------ X split
         // Group g takes units i with i % kG == g.  Thread (r, c) of a group:
-        // row r, elements [32 c, 32 c + 32) of the unit's 128-wide slice; the
-        // four lanes of a row are adjacent lanes.  Each thread copies and reads
+        // row r, elements [kEpt c, kEpt c + kEpt) of the unit's 128-wide slice;
+        // the kLpr lanes of a row are adjacent lanes.  Each thread copies and reads
         // back only its own chunks, so the staging ring needs no barrier: a
         // thread's wait on its own copy groups is enough.
+        constexpr int kEpt = Split<NX>::kEpt;
+        constexpr int kLpr = Split<NX>::kLpr;
         constexpr int CH_IN = kEpt / 8;        // 16-byte BF16 chunks read
         constexpr int CH_OUT = kEpt / 16;      // 16-byte E4M3 chunks written per plane
         constexpr int kGT = 32 * Split<NX>::kWarps;   // threads per group
