@@ -126,6 +126,36 @@ qg_status qgemm_fp8_block_noalloc(const void *X, int64_t ldx,
                                   struct CUstream_st *stream);
 
 /*
+ * The W8A16 FP8 block-scaled GEMM with X and Y in host memory -- for a
+ * caller whose activations arrive from, and whose results go back to, the
+ * host every call.  (The paper has no counterpart of this entry point; it is
+ * an addition of this library.)
+ *
+ * Arguments and results are those of qgemm_fp8_block, except:
+ *   X_host   pinned (page-locked) host memory, BF16 [M, ldx], 16-byte
+ *            aligned, ldx >= K, ldx % 8 == 0; device or managed memory also
+ *            works
+ *   Y_host   pinned host memory, BF16 [M, ldy], ldy >= N; device or managed
+ *            memory also works
+ *   X_stage  device, at least M * K * 2 bytes, 16-byte aligned: scratch the
+ *            call copies X into (row stride K); owned by the caller and
+ *            serving one in-flight call at a time, like the workspace
+ * A staging kernel reads X_host over the host link into X_stage, and the
+ * GEMM stores Y directly into Y_host; no copy call is enqueued.  Pageable
+ * (unregistered) host memory, or a pointer the runtime does not know,
+ * returns QG_ERR_INVALID_ARG before anything is enqueued.  Y_host is
+ * complete once `stream` has been synchronised; the call is asynchronous
+ * like the others, so neither host buffer may be touched before that.
+ */
+qg_status qgemm_fp8_block_host(const void *X_host, int64_t ldx,
+                               const uint8_t *W, const float *W_scale,
+                               void *Y_host, int64_t ldy,
+                               int M, int N, int K,
+                               void *X_stage,
+                               void *workspace, size_t workspace_bytes,
+                               struct CUstream_st *stream);
+
+/*
  * W3A16 learned-LUT GEMM.
  *   X        device, FP16 [M, ldx], 16-byte aligned, ldx >= K, ldx % 8 == 0
  *   Wq       device, pack_lut3() output for an [N, K] code matrix

@@ -80,6 +80,21 @@ def test_fp8_argument_validation(qg, args, expect):
 
 
 @pytest.mark.parametrize("args,expect", [
+    # X_host, ldx, W, S, Y_host, ldy, M, N, K, X_stage
+    ((FAKE, 512, FAKE, FAKE, FAKE, 256, 0, 256, 512, FAKE), 0),       # M == 0: no-op
+    ((FAKE, 512, FAKE, FAKE, FAKE, 256, 4, 256, 512, None), 1),       # null staging buffer
+    ((FAKE, 512, FAKE, FAKE, FAKE, 256, 33, 256, 512, FAKE), 2),      # M > 32
+    ((FAKE, 512, FAKE, FAKE, FAKE, 256, 4, 256, 512, FAKE + 8), 3),   # staging not 16-byte aligned
+    ((FAKE + 8, 512, FAKE, FAKE, FAKE, 256, 4, 256, 512, FAKE), 3),   # X not 16-byte aligned
+    # pointers the runtime does not know as pinned or device memory
+    ((FAKE, 512, FAKE, FAKE, FAKE, 256, 4, 256, 512, FAKE), 1),
+])
+def test_fp8_host_entry_argument_validation(qg, args, expect):
+    X, ldx, W, S, Y, ldy, M, N, K, stage = args
+    assert qg.lib.qgemm_fp8_block_host(X, ldx, W, S, Y, ldy, M, N, K, stage, None, 0, None) == expect
+
+
+@pytest.mark.parametrize("args,expect", [
     # X, ldx, Wq, qmap, scales, Y, ldy, M, N, K
     ((FAKE, 512, FAKE, FAKE, FAKE, FAKE, 256, 0, 256, 512), 0),
     ((None, 512, FAKE, FAKE, FAKE, FAKE, 256, 4, 256, 512), 1),

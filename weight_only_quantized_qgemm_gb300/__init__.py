@@ -9,6 +9,8 @@ The names follow the C ABI in ``include/qgemm.h``:
 
 * :func:`qgemm_fp8_block` -- W8A16 FP8 E4M3 weights with [128 x 128] FP32
   block scales, BF16 activations and output, two-level FP32 fold.
+* :func:`qgemm_fp8_block_host` -- the same GEMM with X and Y in pinned host
+  memory (staged in and stored out by the library's kernels).
 * :func:`qgemm_lut3` -- 3-bit learned-LUT weights (see :func:`pack_lut3`),
   FP16 activations and output.
 * :func:`pack_lut3` / :func:`unpack_lut3` -- offline nibble packer (host).
@@ -24,7 +26,7 @@ import numpy as np
 
 __all__ = [
     "QgemmError", "LIB_PATH", "lib", "status_string", "workspace_bytes", "Workspace",
-    "qgemm_fp8_block", "qgemm_lut3", "pack_lut3", "unpack_lut3", "lut3_packed_bytes",
+    "qgemm_fp8_block", "qgemm_fp8_block_host", "qgemm_lut3", "pack_lut3", "unpack_lut3", "lut3_packed_bytes",
     "dequant_e4m3_bf16", "dequant_lut3", "last_device_status", "set_wait_timeout_ns",
     "set_fault_injection", "set_weight_prefetch_overlap", "KIND_FP8_BLOCK", "KIND_LUT3", "STATUS",
 ]
@@ -60,6 +62,7 @@ lib = ctypes.CDLL(LIB_PATH)
 _SIGS = {
     "qg_workspace_bytes": (_S, [_I, _I, _I, _I]),
     "qgemm_fp8_block": (_I, [_P, _L, _P, _P, _P, _L, _I, _I, _I, _P, _S, _P]),
+    "qgemm_fp8_block_host": (_I, [_P, _L, _P, _P, _P, _L, _I, _I, _I, _P, _P, _S, _P]),
     "qgemm_lut3": (_I, [_P, _L, _P, _P, _P, _P, _L, _I, _I, _I, _P, _S, _P]),
     "qg_lut3_packed_bytes": (_S, [_I, _I]),
     "pack_lut3": (_I, [_P, _P, _I, _I]),
@@ -131,8 +134,14 @@ class Workspace:
 _default_ws = {}
 
 
+_ws_need = {}
+
+
 def _workspace_for(kind, M, N, K, workspace, device):
-    need = workspace_bytes(kind, M, N, K)
+    key = (kind, M, N, K, device)
+    need = _ws_need.get(key)
+    if need is None:
+        need = _ws_need[key] = workspace_bytes(kind, M, N, K)
     if need == 0:
         return None, 0
     if workspace is None:
@@ -170,6 +179,51 @@ def qgemm_fp8_block(X, W, W_scale, Y=None, workspace=None, stream=None):
     ws, wsb = _workspace_for(KIND_FP8_BLOCK, M, N, K, workspace, X.device)
     _check(lib.qgemm_fp8_block(X.data_ptr(), _ld(X), W.data_ptr(), W_scale.data_ptr(), Y.data_ptr(),
                                _ld(Y), M, N, K, ws, wsb, _stream_ptr(stream)), "qgemm_fp8_block")
+    return Y
+
+
+_default_stage = {}
+
+
+def qgemm_fp8_block_host(X, W, W_scale, Y=None, X_stage=None, workspace=None, stream=None):
+    """:func:`qgemm_fp8_block` with X and Y in pinned host memory.
+
+    X: bf16 CPU [M, K], pinned (``tensor.pin_memory()``), row stride a
+    multiple of 8; Y (optional, allocated pinned if absent): bf16 CPU [M, N],
+    pinned, unit column stride.  W and W_scale are on the device as for
+    :func:`qgemm_fp8_block`.  X_stage (optional): a device buffer of at least
+    M*K bf16 elements that the call copies X into; a per-device buffer is
+    kept when absent.  The call is asynchronous: Y is complete after the
+    stream is synchronised.
+    """
+    torch = _torch()
+    if X.dtype != torch.bfloat16:
+        raise TypeError("X must be bfloat16")
+    if W.dtype not in (torch.uint8, torch.float8_e4m3fn):
+        raise TypeError("W must hold E4M3 codes (uint8 or float8_e4m3fn)")
+    if W_scale.dtype != torch.float32 or not W_scale.is_contiguous() or not W.is_contiguous():
+        raise TypeError("W must be contiguous and W_scale contiguous float32")
+    if X.is_cuda or not X.is_pinned():
+        raise ValueError("X must be a pinned host tensor")
+    M, K = X.shape
+    N = W.shape[0]
+    if W.shape[1] != K or tuple(W_scale.shape) != (-(-N // 128), -(-K // 128)):
+        raise ValueError("shape mismatch between X, W and W_scale")
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
+    elif Y.dtype != torch.bfloat16 or Y.is_cuda or not Y.is_pinned():
+        raise ValueError("Y must be a pinned bfloat16 host tensor")
+    if X_stage is None:
+        X_stage = _default_stage.get(W.device)
+        if X_stage is None or X_stage.numel() < M * K:
+            X_stage = _default_stage[W.device] = torch.empty(max(M * K, 1 << 16), dtype=torch.bfloat16,
+                                                             device=W.device)
+    elif not X_stage.is_cuda or X_stage.numel() * X_stage.element_size() < M * K * 2:
+        raise ValueError("X_stage must be a device buffer of at least M*K bfloat16 elements")
+    ws, wsb = _workspace_for(KIND_FP8_BLOCK, M, N, K, workspace, W.device)
+    _check(lib.qgemm_fp8_block_host(X.data_ptr(), _ld(X), W.data_ptr(), W_scale.data_ptr(), Y.data_ptr(),
+                                    _ld(Y), M, N, K, X_stage.data_ptr(), ws, wsb, _stream_ptr(stream)),
+           "qgemm_fp8_block_host")
     return Y
 
 

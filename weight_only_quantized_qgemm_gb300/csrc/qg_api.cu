@@ -89,6 +89,12 @@ LaunchCtl launch_ctl(const DeviceInfo* d) {
     return c;
 }
 
+}  // namespace
+
+bool overlap_enabled() { return g_overlap.load() != 0; }
+
+namespace {
+
 // ----------------------------------------------------------------- dispatch
 // Per-(kind, M, N, K) choice of MMA width and grid.  The MMA N side is 16 for
 // M <= 16 and 32 above (one weight pass for every M <= 32).  Two grids are
@@ -135,25 +141,86 @@ Schedule choose_schedule(int kind, int M, int N, int K, int sms) {
 // True when some tile's units are spread over more than one CTA.
 bool schedule_splits(const Schedule& s) { return splits(s.U, s.KU, s.G); }
 
+// Per-thread caches of the last few schedules (keyed by kind, shape and SM
+// count) and weight tensor maps (keyed by address and shape, which determine
+// the map): the schedule search walks every CTA boundary and the map encoding
+// is a driver call, both otherwise paid on every GEMM call.
+constexpr int kCacheWays = 8;
+
+struct SchedEntry {
+    int kind = -1, M = 0, N = 0, K = 0, sms = 0;
+    Schedule s;
+    size_t ws = 0;
+};
+
+size_t workspace_bytes_uncached(const Schedule& s);
+
+const SchedEntry& cached_schedule(int kind, int M, int N, int K, int sms) {
+    thread_local SchedEntry cache[kCacheWays];
+    thread_local int next = 0;
+    for (const SchedEntry& e : cache)
+        if (e.kind == kind && e.M == M && e.N == N && e.K == K && e.sms == sms) return e;
+    SchedEntry& e = cache[next];
+    next = (next + 1) % kCacheWays;
+    e.kind = kind;
+    e.M = M;
+    e.N = N;
+    e.K = K;
+    e.sms = sms;
+    e.s = choose_schedule(kind, M, N, K, sms);
+    e.ws = workspace_bytes_uncached(e.s);
+    return e;
+}
+
+struct MapEntry {
+    const void* ptr = nullptr;
+    uint64_t cols = 0, rows = 0;
+    CUtensorMap map;
+};
+
+// The E4M3 weight map of W [rows, cols] (128 x 128 boxes), from the
+// per-thread cache; null if the driver refused it.
+const CUtensorMap* weight_tmap(const void* W, uint64_t cols, uint64_t rows) {
+    thread_local MapEntry cache[kCacheWays];
+    thread_local int next = 0;
+    for (MapEntry& e : cache)
+        if (e.ptr == W && e.cols == cols && e.rows == rows) return &e.map;
+    MapEntry& e = cache[next];
+    if (!make_tmap(&e.map, W, CU_TENSOR_MAP_DATA_TYPE_UINT8, cols, rows, cols, 128, 128)) {
+        e.ptr = nullptr;
+        return nullptr;
+    }
+    next = (next + 1) % kCacheWays;
+    e.ptr = W;
+    e.cols = cols;
+    e.rows = rows;
+    return &e.map;
+}
+
 }  // namespace
 
 size_t workspace_partial_bytes(const Schedule& s) {
     return static_cast<size_t>(s.max_ctas) * 2 * 32 * 128 * sizeof(float);
 }
 
-size_t workspace_bytes(const Schedule& s) {
+namespace {
+size_t workspace_bytes_uncached(const Schedule& s) {
     if (!schedule_splits(s)) return 0;
     const size_t cnt = (static_cast<size_t>(s.T) * 4 * sizeof(uint32_t) + 255) & ~static_cast<size_t>(255);
     return workspace_partial_bytes(s) + cnt;
 }
+}  // namespace
+
+size_t workspace_bytes(const Schedule& s) { return workspace_bytes_uncached(s); }
 
 void workspace_counters(int kind, int M, int N, int K, size_t* offset, size_t* bytes) {
     *offset = 0;
     *bytes = 0;
     DeviceInfo* d = device_info();
     if (!d || M <= 0 || N <= 0 || K <= 0) return;
-    const Schedule s = choose_schedule(kind, M, N, K, d->sms);
-    const size_t total = workspace_bytes(s);
+    const SchedEntry& e = cached_schedule(kind, M, N, K, d->sms);
+    const Schedule& s = e.s;
+    const size_t total = e.ws;
     if (total == 0) return;
     *offset = workspace_partial_bytes(s);
     *bytes = total - *offset;
@@ -265,7 +332,7 @@ size_t qg_workspace_bytes(int kind, int M, int N, int K) {
     if (kind != QG_KIND_FP8_BLOCK && kind != QG_KIND_LUT3) return 0;
     DeviceInfo* d = device_info();
     if (!d) return 0;
-    return workspace_bytes(choose_schedule(kind, M, N, K, d->sms));
+    return cached_schedule(kind, M, N, K, d->sms).ws;
 }
 
 qg_status qgemm_fp8_block(const void* X, int64_t ldx, const uint8_t* W, const float* W_scale, void* Y, int64_t ldy,
@@ -281,14 +348,13 @@ qg_status qgemm_fp8_block(const void* X, int64_t ldx, const uint8_t* W, const fl
     DeviceInfo* d = device_info();
     if (!d) return QG_ERR_CUDA;
     if (K == 0) return launch_zero_rows(Y, ldy, M, N, stream) == cudaSuccess ? QG_OK : QG_ERR_CUDA;
-    const Schedule s = choose_schedule(QG_KIND_FP8_BLOCK, M, N, K, d->sms);
-    const size_t need = workspace_bytes(s);
+    const SchedEntry& se = cached_schedule(QG_KIND_FP8_BLOCK, M, N, K, d->sms);
+    const Schedule s = se.s;
+    const size_t need = se.ws;
     if (need > 0 && (!workspace || workspace_bytes_ < need || (reinterpret_cast<uintptr_t>(workspace) & 255u)))
         return QG_ERR_WORKSPACE;
-    CUtensorMap tmW;
-    if (!make_tmap(&tmW, W, CU_TENSOR_MAP_DATA_TYPE_UINT8, static_cast<uint64_t>(K), static_cast<uint64_t>(N),
-                   static_cast<uint64_t>(K), 128, 128))
-        return QG_ERR_CUDA;
+    const CUtensorMap* tmW = weight_tmap(W, static_cast<uint64_t>(K), static_cast<uint64_t>(N));
+    if (!tmW) return QG_ERR_CUDA;
     Fp8Args a;
     a.X = X;
     a.ldx = ldx;
@@ -301,7 +367,7 @@ qg_status qgemm_fp8_block(const void* X, int64_t ldx, const uint8_t* W, const fl
     a.N = N;
     a.K = K;
     a.ws = need > 0 ? workspace : nullptr;
-    return launch_fp8(a, s, tmW, launch_ctl(d), stream) == cudaSuccess ? QG_OK : QG_ERR_CUDA;
+    return launch_fp8(a, s, *tmW, launch_ctl(d), stream) == cudaSuccess ? QG_OK : QG_ERR_CUDA;
 }
 
 qg_status qgemm_lut3(const void* X, int64_t ldx, const void* Wq, const void* qmap, const void* scales, void* Y,
@@ -318,8 +384,9 @@ qg_status qgemm_lut3(const void* X, int64_t ldx, const void* Wq, const void* qma
     DeviceInfo* d = device_info();
     if (!d) return QG_ERR_CUDA;
     if (K == 0) return launch_zero_rows(Y, ldy, M, N, stream) == cudaSuccess ? QG_OK : QG_ERR_CUDA;
-    const Schedule s = choose_schedule(QG_KIND_LUT3, M, N, K, d->sms);
-    const size_t need = workspace_bytes(s);
+    const SchedEntry& se = cached_schedule(QG_KIND_LUT3, M, N, K, d->sms);
+    const Schedule s = se.s;
+    const size_t need = se.ws;
     if (need > 0 && (!workspace || workspace_bytes_ < need || (reinterpret_cast<uintptr_t>(workspace) & 255u)))
         return QG_ERR_WORKSPACE;
     CUtensorMap tmX;

@@ -80,4 +80,10 @@ cudaError_t launch_zero_rows(void* Y, int64_t ldy, int M, int N, cudaStream_t st
 
 uint32_t* device_status_ptr();
 
+// True when calls launch with programmatic stream serialization
+// (qg_set_weight_prefetch_overlap).
+bool overlap_enabled();
+
+inline bool aligned_16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
 }  // namespace qg
