@@ -1,38 +1,32 @@
-// The weight-only decode GEMM pipeline for sm_103a, shared by both weight
-// formats (a format supplies the weight copy, the register dequantiser and
-// the per-block scale of the fold).
+// The 3-bit learned-LUT decode GEMM pipeline for sm_103a (the FP8 format has
+// its own kernel in qg_fp8.cu and shares only the parameter block, the work
+// decomposition and the split-K epilogue defined here).
 //
-//   Y[m, n] = out( sum_kb  fold_scale(n, kb) * ( sum_{k in kb} x[m,k] * deq(W)[n,k] ) )
+//   Y[m, n] = fp16( sum_k x[m,k] * deq(W)[n,k] )
 //
 // Swap-AB: a 128-row slice of W is the MMA's M side (TMEM lanes), the M <= 32
 // activation rows are the MMA's narrow N side (16 or 32).  A work unit is one
-// 128-row tile x one 128-wide K block; its MMAs accumulate into a TMEM
-// accumulator of its own, which the fold warps multiply by the block scale
-// and add into FP32 registers (the two-level fold of the FP8 format; the LUT
-// format's scale is inside the weights and its fold scale is 1).
+// 128-row tile x one 128-wide K block.  The MMAs of a tile piece (the units of
+// one tile in a CTA's range) accumulate in TMEM; the fold warps read each
+// piece once.
 //
-// One persistent CTA per SM, 512 threads (16 warps; registers are granted in
-// 4-warp steps, so a 17th warp would cut every thread to 96 registers):
-//   warp 0        weight producer: one copy per unit (evict-first L2 hint) into
-//                 a deep ring.  A weight stage is released as soon as the
-//                 dequant warps hold it in registers, so nearly the whole ring
-//                 (up to ~176 KB per SM) is in flight against HBM latency.
-//   warp 15       X producer: the unit's 128-wide X slice (two 64-element TMA
-//                 boxes, 128-byte swizzle) into a smaller ring; a slice is held
+// One persistent CTA per SM; warps by role (N = 16: 20 warps, 96 registers
+// each; N = 32: 16 warps, 128 registers):
+//   warp 0        code producer: 4 lanes in step, one bulk copy per unit
+//                 (evict-first L2 hint) into a ring of up to 15 stages.  A
+//                 stage is released when the dequant group has converted it.
+//   last warp     X producer: 4 lanes in step, the unit's 128-wide X slice
+//                 (two 64-element TMA boxes, 128-byte swizzle) into a ring held
 //                 until the unit's MMAs complete.
-//   warps 1,14    MMA issuers, unit i taken by issuer i % 2: 8 tcgen05.mma
+//   warp 1 and the one before the X producer
+//                 MMA issuers, unit i taken by issuer i % 2: 8 tcgen05.mma
 //                 kind::f16 (M=128, N=16|32, K=16), A from TMEM, B (X) from
-//                 shared memory, then one tcgen05.commit, from one elected
-//                 lane.  A single issuing thread gets an MMA accepted only
-//                 every ~55-120 cycles, while the tensor core takes one every
-//                 ~30 at this shape, so two issuers share the units.
+//                 shared memory, then the commits, from one elected lane.
 //   warps 2-5     fold / epilogue, one per TMEM lane quadrant.
-//   warps 6-13    dequant, two groups of four warps taking alternate units:
-//                 shared memory -> registers -> exact BF16/FP16 -> tcgen05.st
-//                 into a ring of A buffers in TMEM (6 deep at N=16, 4 at N=32).
-// The per-unit commit marks the unit's accumulator ready, which also frees its
-// A buffer for the dequant group; the first fold warp to see it then returns
-// the unit's X slot to the X producer.
+//   warps 6-      dequant: 3 groups (2 at N = 32) of four warps, group g
+//                 taking units i with i % groups == g: shared memory ->
+//                 registers -> FP16 by byte-permute lookups -> tcgen05.st into
+//                 a ring of 6 A buffers in TMEM.
 //
 // Work units are split evenly over the CTAs in tile-major order (stream-K);
 // a tile shared by several CTAs is summed, in ascending K order of its
@@ -66,6 +60,8 @@ struct Roles {
     static constexpr int kThreads = 32 * (kWarpXProd + 1);
 };
 constexpr int kIssuers = 2;
+constexpr int kProdLanes = 4;   // lanes of a producer warp that issue copies
+constexpr unsigned kProdMask = (1u << kProdLanes) - 1u;
 constexpr int kTmemCols = 512;
 
 struct Params {
@@ -106,9 +102,9 @@ struct Layout {
     static_assert(kDCol0 + 4 * NMMA <= kTmemCols, "TMEM columns");
     static constexpr int kXSlot = NMMA * 256;             // two 64-element X boxes
     static constexpr int kXBox = NMMA * 128;
-    // X slots: as many as leave the weight ring 8 stages (the X copies then run
-    // far enough ahead of the MMA to hide their latency behind the weight stream)
-    static constexpr int kXStages = (NMMA == 16 ? 3 : 2) * kNA;
+    // X slots: two per A buffer, enough for the X copies (L2 hits) to run
+    // ahead of the MMAs; the rest of the budget goes to the weight ring.
+    static constexpr int kXStages = 2 * kNA;
     static constexpr int kWBudget = 212992 - kXStages * kXSlot;   // 208 KB in all
     // A multiple of the dequant group count, so that every use of a weight stage
     // falls to the same dequant group (units i and i + kWStages are taken by
@@ -117,11 +113,10 @@ struct Layout {
     // phase after another group's still-pending one, and a parity wait cannot
     // tell those two apart.
     static constexpr int kG = Roles<NMMA>::kDeqGroups;
-    // Not deeper: the X copies queue behind the code copies in flight (one TMA
-    // queue per SM), so every extra stage delays X by as much.  Measured on
-    // the 28672 x 8192 shape: 9 stages 37.9 us, 12 38.9, 15 39.0, 6 48 (the
-    // code stream starves).
-    static constexpr int kWFit = (kWBudget / WBYTES) < 9 ? (kWBudget / WBYTES) : 9;
+    // At most 15 stages.  Measured on the 28672 x 8192 shape at M = 16 (code
+    // stages x X slots): 15 x 12 32.7 us, 12 x 12 32.9, 18 x 12 32.9, 15 x 6
+    // 33.0, 18 x 6 33.1, 21 x 6 33.1, 9 x 18 34.8.
+    static constexpr int kWFit = (kWBudget / WBYTES) < 15 ? (kWBudget / WBYTES) : 15;
     static constexpr int kWStages = kWFit / kG * kG;
     static constexpr int kXOff = kWStages * WBYTES;
     static constexpr int kBarOff = kXOff + kXStages * kXSlot;
@@ -135,6 +130,7 @@ struct Layout {
     static_assert(kXStages % kIssuers == 0 && kNA % kIssuers == 0 && kNA % kG == 0, "ring ownership");
     static_assert(kWStages >= 8, "the weight ring must cover HBM latency");
     static_assert(kWStages % kG == 0, "a weight stage must belong to one dequant group");
+    static_assert(kWStages > kProdLanes && kXStages > kProdLanes, "a stage's previous unit is issued in an earlier pass");
     static_assert(kSmemBytes <= 232448, "shared memory");
 };
 
@@ -389,46 +385,69 @@ __global__ void __launch_bounds__(Roles<NMMA>::kThreads, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------------ weight producer
-        if (lane == 0) {
-            if (F::kUsesTensorMapW) prefetch_tmap(&tmW);
+        // kProdLanes lanes issue kProdLanes consecutive units per pass of the
+        // loop, so one pass of its bookkeeping starts kProdLanes copies: a
+        // single producing thread, sharing its scheduler with three dequant
+        // warps, could not issue a copy as often as the dequant consumes one.
+        // The lanes move in step.  A lane waiting for the release of unit
+        // i - kWStages then knows that unit i - 2 kWStages was released (unit
+        // i - kWStages was issued in an earlier pass, after that release), so
+        // the parity of its wait cannot match an older phase of the stage.
+        if (lane < kProdLanes) {
+            if (F::kUsesTensorMapW && lane == 0) prefetch_tmap(&tmW);
             const uint64_t pol_w = policy_evict_first();
-            int issued = 0;
-            Cursor cur(u0, p.KB);
-            Ring<kWStages> rw(0);
-            for (int i = 0; i < nunits; ++i, cur.step(p.KB), rw.step(1)) {
+            int last = -1;   // the last unit this lane issued
+            Cursor cur(u0 + lane, p.KB);
+            Ring<kWStages> rw(lane);
+            for (int i0 = 0; i0 < nunits; i0 += kProdLanes, cur.step(kProdLanes, p.KB), rw.step(kProdLanes)) {
+                const int i = i0 + lane;
                 const int s = rw.slot;
-                if (i >= kWStages && !wait_bounded(wempty(s), rw.phase ^ 1u, wc)) break;
-                if (cta == 0 && i == p.fault_unit) continue;   // failure-path test hook
-                mbar_arrive_expect_tx(wfull(s), F::kWBytes);
-                F::load_w(base + s * F::kWBytes, &tmW, p, wfull(s), cur.tile, cur.kr, pol_w);
-                issued = i + 1;
+                const bool mine = i < nunits;
+                const bool ok = !mine || i < kWStages || wait_bounded(wempty(s), rw.phase ^ 1u, wc);
+                if (!__all_sync(kProdMask, ok)) break;
+                if (mine && !(cta == 0 && i == p.fault_unit)) {   // failure-path test hook
+                    mbar_arrive_expect_tx(wfull(s), F::kWBytes);
+                    F::load_w(base + s * F::kWBytes, &tmW, p, wfull(s), cur.tile, cur.kr, pol_w);
+                    last = i;
+                }
             }
-            // Every copy this thread started must land before the CTA can exit.
-            for (int i = issued - kWStages < 0 ? 0 : issued - kWStages; i < issued; ++i) {
-                if (cta == 0 && i == p.fault_unit) continue;
-                drain_wait(wfull(i % kWStages), (i / kWStages) & 1, p.timeout_ns);
-            }
+            // Every copy started must land before the CTA can exit.  Only the
+            // last kWStages units issued can be in flight: each older unit's
+            // stage was consumed before it was filled again.  Those units sit in
+            // distinct stages with nothing issued after them, so the parity of
+            // each one's wait is unambiguous.
+            const int newest = __reduce_max_sync(kProdMask, last);
+            for (int i = last; i >= 0 && i > newest - kWStages; i -= kProdLanes)
+                if (!(cta == 0 && i == p.fault_unit)) drain_wait(wfull(i % kWStages), (i / kWStages) & 1, p.timeout_ns);
         }
     } else if (warp == kWarpXProd) {
         // ------------------------------------------------------------ X producer
-        if (lane == 0) {
-            prefetch_tmap(&tmX);
+        // kProdLanes lanes in step, as for the weights.
+        if (lane < kProdLanes) {
+            if (lane == 0) prefetch_tmap(&tmX);
             // X may be the output of the preceding grid on the stream
             grid_dependency_wait();
             const uint64_t pol_x = policy_evict_last();
-            int issued = 0;
-            Cursor cur(u0, p.KB);
-            Ring<kXStages> rx(0);
-            for (int i = 0; i < nunits; ++i, cur.step(p.KB), rx.step(1)) {
+            int last = -1;
+            Cursor cur(u0 + lane, p.KB);
+            Ring<kXStages> rx(lane);
+            for (int i0 = 0; i0 < nunits; i0 += kProdLanes, cur.step(kProdLanes, p.KB), rx.step(kProdLanes)) {
+                const int i = i0 + lane;
                 const int s = rx.slot;
-                if (i >= kXStages && !wait_bounded(xempty(s), rx.phase ^ 1u, wc)) break;
-                const uint32_t st = base + L::kXOff + s * L::kXSlot;
-                mbar_arrive_expect_tx(xfull(s), L::kXSlot);
-                tma_load_2d(st, &tmX, xfull(s), cur.kr * 128, 0, pol_x);
-                tma_load_2d(st + L::kXBox, &tmX, xfull(s), cur.kr * 128 + 64, 0, pol_x);
-                issued = i + 1;
+                const bool mine = i < nunits;
+                const bool ok = !mine || i < kXStages || wait_bounded(xempty(s), rx.phase ^ 1u, wc);
+                if (!__all_sync(kProdMask, ok)) break;
+                if (mine) {
+                    const uint32_t st = base + L::kXOff + s * L::kXSlot;
+                    mbar_arrive_expect_tx(xfull(s), L::kXSlot);
+                    tma_load_2d(st, &tmX, xfull(s), cur.kr * 128, 0, pol_x);
+                    tma_load_2d(st + L::kXBox, &tmX, xfull(s), cur.kr * 128 + 64, 0, pol_x);
+                    last = i;
+                }
             }
-            for (int i = issued - kXStages < 0 ? 0 : issued - kXStages; i < issued; ++i)
+            // the last kXStages units issued, as for the weights
+            const int newest = __reduce_max_sync(kProdMask, last);
+            for (int i = last; i >= 0 && i > newest - kXStages; i -= kProdLanes)
                 drain_wait(xfull(i % kXStages), (i / kXStages) & 1, p.timeout_ns);
         }
     } else if (warp == 1 || warp == kWarpMma2) {
@@ -554,33 +573,21 @@ __global__ void __launch_bounds__(Roles<NMMA>::kThreads, 1)
         const int row = q * 32 + lane;
         const uint32_t tl = tmem + (static_cast<uint32_t>(q * 32) << 16);
         typename F::Deq dq(p, u0, grp, kDeqGroups, nunits, row);
-        // Rings of the unit being converted (weight stage, A buffer) and of the
-        // next unit issued (weight stage); the group's units are kDeqGroups apart.
+        // Rings of the unit being converted (weight stage, A buffer); the
+        // group's units are kDeqGroups apart.
         Ring<kWStages> rw(grp);
-        Ring<kWStages> rwn(grp);
         Ring<kNA> ra(grp);
-        // The group's next unit is loaded from shared memory into the other
-        // register slot before the current one is converted, so the load
-        // latency overlaps the conversion.  Unit i's weights into `slot`:
-        auto issue = [&](int i, int slot) -> bool {
-            const int s = rwn.slot;
-            const uint32_t ph = rwn.phase;
-            rwn.step(kDeqGroups);
-            dq.prepare(p, i, nunits, row, slot);
-            if (!warp_wait(wfull(s), ph, wc)) return false;
-            dq.load(slot, gbase + s * F::kWBytes, row);
-            return true;
-        };
-        // unit i (already loaded into `slot`); false when a wait gave up
-        auto unit = [&](int i, int slot, int nslot) -> bool {
+        // unit i, whose scale sits in queue slot `slot`; false when a wait gave up
+        auto unit = [&](int i, int slot) -> bool {
             const int a = ra.slot;
             const uint32_t aph = ra.phase;
             const int sw = rw.slot;
+            const uint32_t wph = rw.phase;
             ra.step(kDeqGroups);
             rw.step(kDeqGroups);
-            const int inext = i + kDeqGroups;
-            const bool more = inext < nunits;
-            if (more && !issue(inext, nslot)) return false;
+            dq.prepare(p, i, nunits, row, slot);
+            if (!warp_wait(wfull(sw), wph, wc)) return false;
+            dq.load(gbase + sw * F::kWBytes, row);
             // unit i - kNA (this group's) is done with its A buffer once its MMAs are
             if (i >= kNA && !warp_wait(afree(a), aph ^ 1u, wc)) return false;
             __syncwarp();
@@ -588,7 +595,7 @@ __global__ void __launch_bounds__(Roles<NMMA>::kThreads, 1)
 #pragma unroll
             for (int qtr = 0; qtr < 4; ++qtr) {
                 uint32_t o[16];
-                dq.convert(slot, qtr, o);
+                dq.convert(qtr, o);
                 tmem_st_x16(tl + a * 64 + qtr * 16, o);
             }
             // Unit i's weight stage is refilled as soon as it is released, so the
@@ -606,16 +613,14 @@ __global__ void __launch_bounds__(Roles<NMMA>::kThreads, 1)
             if (lane == 0) mbar_arrive(afull(a));
             return true;
         };
-        // unrolled so that every register slot index is a constant (no moves
-        // between slots that would wait for a load)
+        // unrolled so that every scale-queue slot index is a constant
         constexpr int kU = F::Deq::kUnroll;
-        static_assert(kU % 2 == 0, "two register slots alternate");
-        bool ok = grp < nunits && issue(grp, 0);
+        bool ok = true;
         for (int i0 = grp; i0 < nunits && ok; i0 += kDeqGroups * kU) {
 #pragma unroll
             for (int j = 0; j < kU; ++j) {
                 const int i = i0 + kDeqGroups * j;
-                if (i < nunits && ok) ok = unit(i, j, (j + 1) % kU);
+                if (i < nunits && ok) ok = unit(i, j);
             }
         }
     }

@@ -37,17 +37,17 @@ struct Lut3Fmt {
     // One thread dequantises one weight row (128 codes, one scale group) of a
     // unit.  The thread's scale for a unit is fetched kUnroll of its units in
     // advance into a fixed slot of scq (the caller unrolls its loop by
-    // kUnroll), so the load latency stays off the dequant.  Codes and the
-    // scaled table have two register slots (slot & 1): the pipeline loads the
-    // group's next unit into one while it converts the current unit from the
-    // other.
+    // kUnroll), so the load latency stays off the dequant.  The codes of one
+    // unit and its scaled table are held at a time: loading the next unit's
+    // codes early would need a second set of registers, and at this kernel's
+    // register budget that set spills.
     struct Deq {
         static constexpr int kUnroll = 2;
         uint4 qm;
-        uint4 c[2][4];
-        uint32_t sc[2];
+        uint4 c[4];
+        uint32_t sc;
         uint32_t scq[kUnroll];
-        LutPlanes t[2];
+        LutPlanes t;
         gemm::Cursor ahead;   // the unit whose scale is fetched next
         int G;                // dequant groups: this thread's units are G apart
         __device__ static uint32_t scale_of(const gemm::Params& p, const gemm::Cursor& c, int row) {
@@ -56,8 +56,7 @@ struct Lut3Fmt {
                            : 0u;
         }
         // this thread handles units grp, grp + G, grp + 2 G, ... (G dequant
-        // groups); slot j holds the
-        // scale of its j-th unit modulo kUnroll
+        // groups); slot j of scq holds the scale of its j-th unit modulo kUnroll
         __device__ Deq(const gemm::Params& p, long long u0, int grp, int groups, int nunits, int row)
             : qm(__ldg(p.qmap)), ahead(u0 + grp, p.KB), G(groups) {
 #pragma unroll
@@ -67,30 +66,28 @@ struct Lut3Fmt {
                 ahead.step(G, p.KB);
             }
         }
-        // called for each of the group's units in order, just before load()
+        // called for each of the group's units in order, before load(); slot is
+        // the unit's place in the scale queue (a compile-time constant)
         __device__ void prepare(const gemm::Params& p, int i, int nunits, int row, int slot) {
-            sc[slot & 1] = scq[slot];
+            sc = scq[slot];
             const int inext = i + G * kUnroll;
             scq[slot] = inext < nunits ? scale_of(p, ahead, row) : 0u;
             ahead.step(G, p.KB);
         }
-        __device__ void load(int slot, const uint8_t* stage, int row) {
-            const int b = slot & 1;
+        __device__ void load(const uint8_t* stage, int row) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) c[b][j] = *reinterpret_cast<const uint4*>(stage + ((j * 128 + row) << 4));
-            const uint32_t sc2 = sc[b] | (sc[b] << 16);
-            t[b] = lut_planes(f16x2_mul(qm.x, sc2), f16x2_mul(qm.y, sc2), f16x2_mul(qm.z, sc2),
-                              f16x2_mul(qm.w, sc2));
+            for (int j = 0; j < 4; ++j) c[j] = *reinterpret_cast<const uint4*>(stage + ((j * 128 + row) << 4));
+            const uint32_t sc2 = sc | (sc << 16);
+            t = lut_planes(f16x2_mul(qm.x, sc2), f16x2_mul(qm.y, sc2), f16x2_mul(qm.z, sc2), f16x2_mul(qm.w, sc2));
         }
         // columns 16*qtr .. 16*qtr+15 of the row's A fragment (K 32*qtr .. 32*qtr+31)
-        __device__ void convert(int slot, int qtr, uint32_t (&o)[16]) const {
-            const int b = slot & 1;
-            const uint4 cw = c[b][qtr];
+        __device__ void convert(int qtr, uint32_t (&o)[16]) const {
+            const uint4 cw = c[qtr];
             const uint32_t w4[4] = {cw.x, cw.y, cw.z, cw.w};
 #pragma unroll
             for (int w = 0; w < 4; ++w) {
                 uint32_t r4[4];
-                lut3x8_to_f16(w4[w], t[b], r4);
+                lut3x8_to_f16(w4[w], t, r4);
 #pragma unroll
                 for (int e = 0; e < 4; ++e) o[4 * w + e] = r4[e];
             }
