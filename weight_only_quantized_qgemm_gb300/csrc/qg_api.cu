@@ -65,7 +65,8 @@ EncodeTiledFn encode_fn() {
 // 2-D row-major tensor map: `rows` x `cols` elements, row stride `ld_bytes`,
 // box `box_cols` x `box_rows`, 128-byte swizzle, out-of-range reads as zero.
 bool make_tmap(CUtensorMap* m, const void* ptr, CUtensorMapDataType dt, uint64_t cols, uint64_t rows,
-               uint64_t ld_bytes, uint32_t box_cols, uint32_t box_rows) {
+               uint64_t ld_bytes, uint32_t box_cols, uint32_t box_rows,
+               CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[2] = {cols, rows};
@@ -73,7 +74,7 @@ bool make_tmap(CUtensorMap* m, const void* ptr, CUtensorMapDataType dt, uint64_t
     const cuuint32_t box[2] = {box_cols, box_rows};
     const cuuint32_t estr[2] = {1, 1};
     return fn(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -172,28 +173,40 @@ const SchedEntry& cached_schedule(int kind, int M, int N, int K, int sms) {
     return e;
 }
 
+// Tensor maps of operands that stay put between calls, keyed by what the map
+// encodes (address, shape and kind).
+enum MapKind { kMapFp8Weights = 0, kMapLut3Scales = 1 };
+
 struct MapEntry {
     const void* ptr = nullptr;
     uint64_t cols = 0, rows = 0;
+    int kind = -1;
     CUtensorMap map;
 };
 
-// The E4M3 weight map of W [rows, cols] (128 x 128 boxes), from the
-// per-thread cache; null if the driver refused it.
-const CUtensorMap* weight_tmap(const void* W, uint64_t cols, uint64_t rows) {
+// The cached map of a [rows, cols] operand, encoded on a miss; null if the
+// driver refused it.
+//   kMapFp8Weights: E4M3 weights, 128 x 128 boxes, 128-byte swizzle.
+//   kMapLut3Scales: FP16 LUT3 scales [N, K/128], boxes of 8 groups x 128 rows.
+const CUtensorMap* cached_tmap(const void* ptr, uint64_t cols, uint64_t rows, MapKind kind) {
     thread_local MapEntry cache[kCacheWays];
     thread_local int next = 0;
     for (MapEntry& e : cache)
-        if (e.ptr == W && e.cols == cols && e.rows == rows) return &e.map;
+        if (e.ptr == ptr && e.cols == cols && e.rows == rows && e.kind == kind) return &e.map;
     MapEntry& e = cache[next];
-    if (!make_tmap(&e.map, W, CU_TENSOR_MAP_DATA_TYPE_UINT8, cols, rows, cols, 128, 128)) {
+    const bool ok = kind == kMapFp8Weights
+                        ? make_tmap(&e.map, ptr, CU_TENSOR_MAP_DATA_TYPE_UINT8, cols, rows, cols, 128, 128)
+                        : make_tmap(&e.map, ptr, CU_TENSOR_MAP_DATA_TYPE_UINT16, cols, rows, cols * 2, 8, 128,
+                                    CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (!ok) {
         e.ptr = nullptr;
         return nullptr;
     }
     next = (next + 1) % kCacheWays;
-    e.ptr = W;
+    e.ptr = ptr;
     e.cols = cols;
     e.rows = rows;
+    e.kind = kind;
     return &e.map;
 }
 
@@ -353,7 +366,7 @@ qg_status qgemm_fp8_block(const void* X, int64_t ldx, const uint8_t* W, const fl
     const size_t need = se.ws;
     if (need > 0 && (!workspace || workspace_bytes_ < need || (reinterpret_cast<uintptr_t>(workspace) & 255u)))
         return QG_ERR_WORKSPACE;
-    const CUtensorMap* tmW = weight_tmap(W, static_cast<uint64_t>(K), static_cast<uint64_t>(N));
+    const CUtensorMap* tmW = cached_tmap(W, static_cast<uint64_t>(K), static_cast<uint64_t>(N), kMapFp8Weights);
     if (!tmW) return QG_ERR_CUDA;
     Fp8Args a;
     a.X = X;
@@ -393,6 +406,14 @@ qg_status qgemm_lut3(const void* X, int64_t ldx, const void* Wq, const void* qma
     if (!make_tmap(&tmX, X, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, static_cast<uint64_t>(K), static_cast<uint64_t>(M),
                    static_cast<uint64_t>(ldx) * 2, 64, static_cast<uint32_t>(s.nmma)))
         return QG_ERR_CUDA;
+    // The scales go through the weight stage when their rows can be copied
+    // by a tensor map (16-byte row pitch and base); otherwise the dequant
+    // warps load them.
+    const CUtensorMap* tmS = nullptr;
+    if ((K / 128) % 8 == 0 && aligned16(scales)) {
+        tmS = cached_tmap(scales, static_cast<uint64_t>(K / 128), static_cast<uint64_t>(N), kMapLut3Scales);
+        if (!tmS) return QG_ERR_CUDA;
+    }
     Lut3Args a;
     a.X = X;
     a.ldx = ldx;
@@ -406,7 +427,7 @@ qg_status qgemm_lut3(const void* X, int64_t ldx, const void* Wq, const void* qma
     a.N = N;
     a.K = K;
     a.ws = need > 0 ? workspace : nullptr;
-    return launch_lut3(a, s, tmX, launch_ctl(d), stream) == cudaSuccess ? QG_OK : QG_ERR_CUDA;
+    return launch_lut3(a, s, tmX, tmS, launch_ctl(d), stream) == cudaSuccess ? QG_OK : QG_ERR_CUDA;
 }
 
 size_t qg_lut3_packed_bytes(int N, int K) {

@@ -317,7 +317,7 @@ template <int NMMA, class F>
 __global__ void __launch_bounds__(Roles<NMMA>::kThreads, 1)
     qgemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                  const Params p) {
-    using L = Layout<NMMA, F::kWBytes>;
+    using L = Layout<NMMA, F::kStageBytes>;
     constexpr int kDeqGroups = Roles<NMMA>::kDeqGroups;
     constexpr int kWarpMma2 = Roles<NMMA>::kWarpMma2;
     constexpr int kWarpXProd = Roles<NMMA>::kWarpXProd;
@@ -396,6 +396,7 @@ __global__ void __launch_bounds__(Roles<NMMA>::kThreads, 1)
         if (lane < kProdLanes) {
             if (F::kUsesTensorMapW && lane == 0) prefetch_tmap(&tmW);
             const uint64_t pol_w = policy_evict_first();
+            const uint64_t pol_s = policy_evict_last();   // a scale box serves 8 units
             int last = -1;   // the last unit this lane issued
             Cursor cur(u0 + lane, p.KB);
             Ring<kWStages> rw(lane);
@@ -406,8 +407,8 @@ __global__ void __launch_bounds__(Roles<NMMA>::kThreads, 1)
                 const bool ok = !mine || i < kWStages || wait_bounded(wempty(s), rw.phase ^ 1u, wc);
                 if (!__all_sync(kProdMask, ok)) break;
                 if (mine && !(cta == 0 && i == p.fault_unit)) {   // failure-path test hook
-                    mbar_arrive_expect_tx(wfull(s), F::kWBytes);
-                    F::load_w(base + s * F::kWBytes, &tmW, p, wfull(s), cur.tile, cur.kr, pol_w);
+                    mbar_arrive_expect_tx(wfull(s), F::kStageBytes);
+                    F::load_w(base + s * F::kStageBytes, &tmW, p, wfull(s), cur.tile, cur.kr, pol_w, pol_s);
                     last = i;
                 }
             }
@@ -587,7 +588,7 @@ __global__ void __launch_bounds__(Roles<NMMA>::kThreads, 1)
             rw.step(kDeqGroups);
             dq.prepare(p, i, nunits, row, slot);
             if (!warp_wait(wfull(sw), wph, wc)) return false;
-            dq.load(gbase + sw * F::kWBytes, row);
+            dq.load(gbase + sw * F::kStageBytes, row);
             // unit i - kNA (this group's) is done with its A buffer once its MMAs are
             if (i >= kNA && !warp_wait(afree(a), aph ^ 1u, wc)) return false;
             __syncwarp();
@@ -637,7 +638,7 @@ __global__ void __launch_bounds__(Roles<NMMA>::kThreads, 1)
 template <int NMMA, class F>
 cudaError_t launch(const Params& prm, const Schedule& s, const CUtensorMap& tmW, const CUtensorMap& tmX,
                    bool overlap, cudaStream_t st) {
-    using L = Layout<NMMA, F::kWBytes>;
+    using L = Layout<NMMA, F::kStageBytes>;
     static int configured_device = -1;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);

@@ -70,7 +70,9 @@ struct LaunchCtl {
 
 cudaError_t launch_fp8(const Fp8Args& a, const Schedule& s, const CUtensorMap& tmW, const LaunchCtl& c,
                        cudaStream_t st);
-cudaError_t launch_lut3(const Lut3Args& a, const Schedule& s, const CUtensorMap& tmX,
+// tmS: the scale-matrix tensor map ([N, K/128] FP16, boxes of 128 rows x 8
+// groups), or null to have the kernel load scales from global memory.
+cudaError_t launch_lut3(const Lut3Args& a, const Schedule& s, const CUtensorMap& tmX, const CUtensorMap* tmS,
                         const LaunchCtl& c, cudaStream_t st);
 
 cudaError_t launch_dequant_e4m3(const uint8_t* codes, void* out, int64_t n, cudaStream_t st);
