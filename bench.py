@@ -392,6 +392,9 @@ def main():
     ap.add_argument("--quick", action="store_true", help="headline only, no secondary configs or CPU baseline")
     ap.add_argument("--overlap", type=int, choices=[0, 1], default=1,
                     help="launch with weight-prefetch overlap of consecutive calls (default 1)")
+    ap.add_argument("--only", choices=["lut3"], default=None,
+                    help="time one secondary workload alone (3-bit LUT, M=16, N=28672, K=8192) and print "
+                         "its line; for profiling that kernel")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -411,6 +414,19 @@ def main():
         import torch.distributed as dist
         dist.barrier()
     import weight_only_quantized_qgemm_gb300 as qg
+
+    if args.only == "lut3":
+        stream = torch.cuda.Stream()
+        qg.set_weight_prefetch_overlap(bool(args.overlap))
+        c = Lut3Case(torch, qg, 16, 28672, 8192)
+        ms = c.time(16, stream, args.steps, args.warmup)
+        nbytes = lut3_bytes(16, 28672, 8192)
+        peak, peak_kind = measured_peaks()
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        print(json.dumps({"workload": "lut3 M=16 N=28672 K=8192", "us_per_call": round(ms * 1e3, 3),
+                          "GBps": round(gbs, 1), "frac": round(gbs / peak, 4), "peak": peak,
+                          "peak_kind": peak_kind, "steps": args.steps, "warmup": args.warmup}))
+        return 0
 
     M, N, K, cid = HEAD["M"], HEAD["N"], HEAD["K"], HEAD["config_id"]
     stream = torch.cuda.Stream()
