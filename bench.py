@@ -154,6 +154,18 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(x, world, device="cuda"):
+    """The maximum of x over all ranks of the default process group (x itself
+    for one rank): the job's time is its slowest rank's."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def gpu_uuid(torch, dev):
     try:
         u = str(torch.cuda.get_device_properties(dev).uuid)
@@ -468,11 +480,9 @@ def main():
     st = qg.last_device_status(stream)
     if st:
         raise RuntimeError(f"device status {qg.status_string(st)}")
+    ms_total = max_over_ranks(ms_total, world)
     if world > 1:
         import torch.distributed as dist
-        t = torch.tensor([ms_total], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
         dist.barrier()
     ms = ms_total / args.steps
     per_call_bytes = fp8_bytes(M, N, K)
@@ -482,6 +492,7 @@ def main():
 
     e2e_ms, h2d, d2h = e2e_fp8(torch, qg, stream, case, M, steps=max(200, min(args.steps, 5000)),
                                warmup=args.warmup)
+    e2e_ms = max_over_ranks(e2e_ms, world)
     case.free()
     torch.cuda.empty_cache()
     if rank != 0:
@@ -527,7 +538,7 @@ def main():
                      "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
                      "bytes_per_launch": per_call_bytes,
                      "traffic": profiled_traffic("fp8_gateup_m16", per_call_bytes)},
-        "e2e": {"value": round(per_call_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+        "e2e": {"value": round(per_call_bytes * world / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "us_per_step": round(e2e_ms * 1e3, 3),
                 "path": "qgemm_fp8_block_host: pinned host X read by a staging kernel, "
