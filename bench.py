@@ -412,9 +412,9 @@ def main():
     ap.add_argument("--quick", action="store_true", help="headline only, no secondary configs or CPU baseline")
     ap.add_argument("--overlap", type=int, choices=[0, 1], default=1,
                     help="launch with weight-prefetch overlap of consecutive calls (default 1)")
-    ap.add_argument("--only", choices=["lut3"], default=None,
-                    help="time one secondary workload alone (3-bit LUT, M=16, N=28672, K=8192) and print "
-                         "its line; for profiling that kernel")
+    ap.add_argument("--only", choices=["lut3", "fp8_down_m32"], default=None,
+                    help="time one secondary workload alone and print its line, for profiling its kernel: "
+                         "lut3 = 3-bit LUT, M=16, N=28672, K=8192; fp8_down_m32 = FP8 M=32, N=5120, K=17408")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -435,15 +435,20 @@ def main():
         dist.barrier()
     import weight_only_quantized_qgemm_gb300 as qg
 
-    if args.only == "lut3":
+    if args.only is not None:
         stream = torch.cuda.Stream()
         qg.set_weight_prefetch_overlap(bool(args.overlap))
-        c = Lut3Case(torch, qg, 16, 28672, 8192)
-        ms = c.time(16, stream, args.steps, args.warmup)
-        nbytes = lut3_bytes(16, 28672, 8192)
+        if args.only == "lut3":
+            c = Lut3Case(torch, qg, 16, 28672, 8192)
+            ms = c.time(16, stream, args.steps, args.warmup)
+            nbytes, name = lut3_bytes(16, 28672, 8192), "lut3 M=16 N=28672 K=8192"
+        else:
+            c = Fp8Case(torch, qg, 32, 5120, 17408, 2)
+            ms = c.time(32, stream, args.steps, args.warmup)
+            nbytes, name = fp8_bytes(32, 5120, 17408), "fp8_block down M=32 N=5120 K=17408"
         peak, peak_kind = measured_peaks()
         gbs = nbytes / (ms * 1e-3) / 1e9
-        print(json.dumps({"workload": "lut3 M=16 N=28672 K=8192", "us_per_call": round(ms * 1e3, 3),
+        print(json.dumps({"workload": name, "us_per_call": round(ms * 1e3, 3),
                           "GBps": round(gbs, 1), "frac": round(gbs / peak, 4), "peak": peak,
                           "peak_kind": peak_kind, "steps": args.steps, "warmup": args.warmup}))
         return 0
