@@ -280,28 +280,107 @@ def e2e_fp8(torch, qg, stream, case, M, steps, warmup):
     """Through the public Python API with host buffers: X in pinned host
     memory, Y into pinned host memory, every step.  qgemm_fp8_block_host
     moves both inside the timed region: its staging kernel reads X over the
-    host link, and the GEMM's epilogue stores Y to the host."""
-    X = case.X[:M]
-    Xh = torch.empty(X.shape, dtype=X.dtype).pin_memory()
-    Xh.copy_(X.cpu())
-    Yh = torch.empty((M, case.N), dtype=torch.bfloat16).pin_memory()
-    stage = torch.empty(X.numel(), dtype=X.dtype, device="cuda")
+    host link, and the GEMM's epilogue stores Y to the host.  Each step reads
+    a different X: the steps rotate over host X buffers of distinct contents
+    that together exceed twice the L2 size, so no step's X can come from a
+    cache."""
+    K, N = case.K, case.N
+    slots = -(-2 * L2_BYTES // (M * K * 2)) + 1
+    Xh = torch.empty((slots, M, K), dtype=torch.bfloat16).pin_memory()
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(0x51A7E000 + 7)
+    for s0 in range(0, slots, 256):
+        s1 = min(slots, s0 + 256)
+        Xh[s0:s1].copy_(torch.randn((s1 - s0, M, K), generator=gen, device="cuda").to(torch.bfloat16).cpu())
+    Yh = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
+    stage = torch.empty(M * K, dtype=torch.bfloat16, device="cuda")
     W, S, ws, copies = case.W, case.S, case.ws, case.copies
 
     def step(i):
-        qg.qgemm_fp8_block_host(Xh, W[i % copies], S, Y=Yh, X_stage=stage, workspace=ws, stream=stream)
+        qg.qgemm_fp8_block_host(Xh[i % slots], W[i % copies], S, Y=Yh, X_stage=stage, workspace=ws, stream=stream)
 
     ms = time_calls(torch, stream, step, steps, warmup)
     st = qg.last_device_status(stream)
     if st:
         raise RuntimeError(f"device status {qg.status_string(st)}")
     # the last step's Y, read on the host, must be the device path's result
-    ref = torch.empty((M, case.N), dtype=torch.bfloat16, device="cuda")
-    qg.qgemm_fp8_block(case.X[:M], W[(steps + warmup - 1) % copies], S, Y=ref, workspace=ws, stream=stream)
+    last = steps - 1
+    ref = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    qg.qgemm_fp8_block(Xh[last % slots].cuda(), W[last % copies], S, Y=ref, workspace=ws, stream=stream)
     torch.cuda.synchronize()
     if not torch.equal(ref.cpu().view(torch.int16), Yh.view(torch.int16)):
         raise RuntimeError("host-buffer path differs from the device path")
-    return ms, Xh.numel() * Xh.element_size(), Yh.numel() * Yh.element_size()
+    return ms, M * K * 2, Yh.numel() * Yh.element_size(), slots
+
+
+def time_halves(torch, qg, stream, case, steps, warmup):
+    """M = 32 as two calls on contiguous 16-row halves of X and Y (plain row
+    offsets), one step = both calls."""
+    qg_, N, K = qg, case.N, case.K
+    buf = case.ws.get(qg_.workspace_bytes(qg_.KIND_FP8_BLOCK, 16, N, K))
+    ws_ptr = buf.data_ptr() if buf is not None else None
+    ws_n = buf.numel() if buf is not None else 0
+    lib, sptr, copies = qg_.lib, stream.cuda_stream, case.copies
+    xp, yp, sp = case.X.data_ptr(), case.Y.data_ptr(), case.S.data_ptr()
+    wps = [w.data_ptr() for w in case.W]
+
+    def step(i):
+        w = wps[i % copies]
+        for h in (0, 1):
+            r = lib.qgemm_fp8_block(xp + h * 16 * K * 2, K, w, sp, yp + h * 16 * N * 2, N, 16, N, K, ws_ptr, ws_n,
+                                    sptr)
+            if r:
+                raise RuntimeError(qg_.status_string(r))
+    ms = time_calls(torch, stream, step, steps, warmup)
+    st = qg_.last_device_status(stream)
+    if st:
+        raise RuntimeError(f"device status {qg_.status_string(st)}")
+    return ms
+
+
+class QkvCase:
+    """The attention projections Q (N=6144), K and V (N=1024 each) at
+    K=5120 sharing X, weights rotated over copies (>= 2x L2)."""
+
+    NS = (6144, 1024, 1024)
+
+    def __init__(self, torch, qg, M_max, K=5120):
+        import workloads as wl
+        self.torch, self.qg, self.K = torch, qg, K
+        ps = [wl.make_fp8_problem(M_max, N, K, config_id=80 + j) for j, N in enumerate(self.NS)]
+        per_set = sum(N for N in self.NS) * K
+        self.copies = -(-2 * L2_BYTES // per_set) + 1
+        self.sets = [[(torch.from_numpy(p.W).cuda(), torch.from_numpy(p.S).cuda()) for p in ps]
+                     for _ in range(self.copies)]
+        self.X = torch.from_numpy(ps[0].X.view(np.int16)).view(torch.bfloat16).cuda()
+        self.Y = [torch.empty((M_max, N), dtype=torch.bfloat16, device="cuda") for N in self.NS]
+        self.ws = qg.Workspace()
+
+    def nbytes(self, M):
+        """Algorithmic bytes of the three GEMMs with X counted once."""
+        return sum(fp8_bytes(M, N, self.K) for N in self.NS) - 2 * M * self.K * 2
+
+    def time(self, M, stream, steps, warmup, fused):
+        qg, K = self.qg, self.K
+        X = self.X[:M]
+        Ys = [Y[:M] for Y in self.Y]
+        ws = self.ws
+
+        def step(i):
+            ws_set = self.sets[i % self.copies]
+            if fused:
+                qg.qgemm_fp8_block_multi(X, ws_set, Ys=Ys, workspace=ws, stream=stream)
+            else:
+                for (W, S), Y in zip(ws_set, Ys):
+                    qg.qgemm_fp8_block(X, W, S, Y=Y, workspace=ws, stream=stream)
+        ms = time_calls(self.torch, stream, step, steps, warmup)
+        st = qg.last_device_status(stream)
+        if st:
+            raise RuntimeError(f"device status {qg.status_string(st)}")
+        return ms
+
+    def free(self):
+        self.sets = self.X = self.Y = self.ws = None
 
 
 def secondary_lines(torch, qg, stream, peak, steps=2000, warmup=50):
@@ -320,6 +399,9 @@ def secondary_lines(torch, qg, stream, peak, steps=2000, warmup=50):
     c = Fp8Case(torch, qg, 32, 5120, 17408, 2)
     for m in (1, 16, 32):
         rec(f"fp8_down_M{m}", c.time(m, stream, steps, warmup), fp8_bytes(m, 5120, 17408))
+    # the same 32 rows as two 16-row calls (the weights stream twice; the
+    # fraction is taken against the one-call algorithmic bytes)
+    rec("fp8_down_M32_halves", time_halves(torch, qg, stream, c, steps, warmup), fp8_bytes(32, 5120, 17408))
     c.free()
     for n in (1024, 5120, 6144):
         c = Fp8Case(torch, qg, 32, n, 5120, 3)
@@ -329,6 +411,12 @@ def secondary_lines(torch, qg, stream, peak, steps=2000, warmup=50):
     c = Fp8Case(torch, qg, 1, 256, 512, 0)
     rec("fp8_small_M1", c.time(1, stream, steps, warmup), fp8_bytes(1, 256, 512))
     c.free()
+    # Q, K and V in one launch against the three calls one after another
+    c = QkvCase(torch, qg, 32)
+    for m in (1, 16, 32):
+        rec(f"fp8_qkv_fused_M{m}", c.time(m, stream, steps, warmup, True), c.nbytes(m))
+        rec(f"fp8_qkv_separate_M{m}", c.time(m, stream, steps, warmup, False), c.nbytes(m))
+    c.free()
     c = Lut3Case(torch, qg, 16, 28672, 8192)
     for m in (1, 4, 8, 16):
         rec(f"lut3_M{m}", c.time(m, stream, steps, warmup), lut3_bytes(m, 28672, 8192))
@@ -337,30 +425,39 @@ def secondary_lines(torch, qg, stream, peak, steps=2000, warmup=50):
     return out
 
 
-def cpu_baseline(M, N, K, config_id, budget_s=12.0):
-    """The oracle as it stands, on the host cores, over a column sample of the
-    same workload sized to roughly `budget_s` seconds."""
-    import oracle
-    import workloads as wl
-    p = wl.make_fp8_problem(M, N, K, config_id=config_id)
-    nt = oracle.max_threads()
-    cols = 512
+def _oracle_rate(oracle, p, M, K, nthreads, budget_s):
+    """GB/s of the oracle on a column sample of the problem sized to about
+    `budget_s` seconds, and a description of the sample."""
+    N = p.W.shape[0]
+    cols = 128 if nthreads == 1 else 512
     t0 = time.perf_counter()
-    oracle.qgemm_fp8_block(p.X, p.W[:cols], p.S[: -(-cols // 128)], nthreads=nt)
+    oracle.qgemm_fp8_block(p.X, p.W[:cols], p.S[: -(-cols // 128)], nthreads=nthreads)
     dt = time.perf_counter() - t0
     n_s = int(min(N, max(128, (budget_s / max(dt, 1e-6)) * cols)) // 128 * 128)
-    # whole passes over the sample until the budget is spent (the full
-    # workload takes well under a second on many cores)
+    # whole passes over the sample until the budget is spent
     passes, t0 = 0, time.perf_counter()
     while True:
-        oracle.qgemm_fp8_block(p.X, p.W[:n_s], p.S[: -(-n_s // 128)], nthreads=nt)
+        oracle.qgemm_fp8_block(p.X, p.W[:n_s], p.S[: -(-n_s // 128)], nthreads=nthreads)
         passes += 1
         dt = time.perf_counter() - t0
         if dt >= budget_s or passes >= 1000:
             break
     gbs = fp8_bytes(M, n_s, K) * passes / dt / 1e9
-    return {"value": round(gbs, 4), "unit": "GB/s", "cores": nt, "kind": "oracle",
-            "sample": f"columns 0..{n_s - 1} of {N} (all {M} rows, full K={K}), {passes} passes; {dt:.2f} s"}, p
+    return gbs, f"columns 0..{n_s - 1} of {N} (all {M} rows, full K={K}), {passes} passes; {dt:.2f} s"
+
+
+def cpu_baseline(M, N, K, config_id, budget_s=10.0):
+    """The oracle as it stands, on the host cores (all of them, and one),
+    over a column sample of the same workload sized to roughly `budget_s`
+    seconds each."""
+    import oracle
+    import workloads as wl
+    p = wl.make_fp8_problem(M, N, K, config_id=config_id)
+    nt = oracle.max_threads()
+    gbs, sample = _oracle_rate(oracle, p, M, K, nt, budget_s)
+    gbs1, sample1 = _oracle_rate(oracle, p, M, K, 1, budget_s)
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": nt, "kind": "oracle", "sample": sample,
+            "single_thread": {"value": round(gbs1, 5), "unit": "GB/s", "cores": 1, "sample": sample1}}, p
 
 
 def run_reference(args):
@@ -495,9 +592,17 @@ def main():
     achieved = per_call_bytes / (ms * 1e-3) / 1e9
     copies = case.copies
 
-    e2e_ms, h2d, d2h = e2e_fp8(torch, qg, stream, case, M, steps=max(200, min(args.steps, 5000)),
-                               warmup=args.warmup)
+    e2e_ms, h2d, d2h, e2e_slots = e2e_fp8(torch, qg, stream, case, M, steps=max(200, min(args.steps, 5000)),
+                                          warmup=args.warmup)
     e2e_ms = max_over_ranks(e2e_ms, world)
+    # the same calls strictly one after another (no launch overlap): what one
+    # call costs on its own
+    iso_ms = None
+    if args.overlap:
+        qg.set_weight_prefetch_overlap(False)
+        iso_ms = case.time(M, stream, max(200, min(args.steps, 5000)), args.warmup)
+        qg.set_weight_prefetch_overlap(True)
+        iso_ms = max_over_ranks(iso_ms, world)
     case.free()
     torch.cuda.empty_cache()
     if rank != 0:
@@ -543,11 +648,17 @@ def main():
                      "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
                      "bytes_per_launch": per_call_bytes,
                      "traffic": profiled_traffic("fp8_gateup_m16", per_call_bytes)},
+        "isolated": None if iso_ms is None else {
+            "us_per_call": round(iso_ms * 1e3, 3), "GBps": round(per_call_bytes / (iso_ms * 1e-3) / 1e9, 2),
+            "frac": round(per_call_bytes / (iso_ms * 1e-3) / 1e9 / peak, 4),
+            "how": "same workload, calls launched without weight-prefetch overlap (each waits for the one before)"},
         "e2e": {"value": round(per_call_bytes * world / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "us_per_step": round(e2e_ms * 1e3, 3),
                 "path": "qgemm_fp8_block_host: pinned host X read by a staging kernel, "
-                        "Y stored to pinned host memory by the GEMM epilogue (2 kernels per step)"},
+                        "Y stored to pinned host memory by the GEMM epilogue (2 kernels per step)",
+                "x_buffers": f"{e2e_slots} pinned host X buffers of distinct contents rotated "
+                             f"({e2e_slots * h2d / 1e6:.0f} MB > 2x L2)"},
         "gpu_launches": args.steps,
         "clocks": clocks,
         "cpu_baseline": cpu,

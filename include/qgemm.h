@@ -98,6 +98,42 @@ qg_status qgemm_fp8_block(const void *X, int64_t ldx,
                           struct CUstream_st *stream);
 
 /*
+ * Several FP8 block-scaled GEMMs that share X, in one launch: for each
+ * segment j, Y_j = X . dequant(W_j)^T -- e.g. the Q, K and V projections of
+ * one attention layer ("atlas" m16_tc page, the section on splitting the
+ * lever per projection family; its w8a16_gemm_m16_strided kernel).  The
+ * segments' 128-row tiles are concatenated into one grid, so the shapes
+ * share one launch, one split-K schedule and one per-call start-up cost, and
+ * each segment's rows are stored into its own Y with its own row stride.
+ * Every segment's result is what qgemm_fp8_block gives for it alone, within
+ * the same comparison rule (only the split-K order of the sums can differ).
+ *
+ *   X, ldx, M, K   as for qgemm_fp8_block, shared by every segment
+ *   segments[j]    W, W_scale, Y, ldy and N (>= 1) of segment j, each as
+ *                  for qgemm_fp8_block; 1 <= nseg <= QG_MAX_SEGMENTS
+ *   workspace      at least qg_workspace_bytes(QG_KIND_FP8_BLOCK, M, R, K)
+ *                  bytes, R = the sum over segments of 128 * ceil(N_j / 128);
+ *                  the dispatch table is consulted with that same R
+ * Arguments are checked segment by segment, in order, before anything is
+ * enqueued; the first failing check's status is returned.
+ */
+#define QG_MAX_SEGMENTS 4
+
+typedef struct qg_fp8_segment {
+    const uint8_t *W;       /* device, E4M3 [N, K] row-major, 16-byte aligned */
+    const float *W_scale;   /* device, FP32 [ceil(N/128), ceil(K/128)] row-major */
+    void *Y;                /* device, BF16 [M, ldy] */
+    int64_t ldy;            /* >= N */
+    int N;                  /* >= 1 */
+} qg_fp8_segment;
+
+qg_status qgemm_fp8_block_multi(const void *X, int64_t ldx,
+                                const qg_fp8_segment *segments, int nseg,
+                                int M, int K,
+                                void *workspace, size_t workspace_bytes,
+                                struct CUstream_st *stream);
+
+/*
  * The W8A16 FP8 block-scaled GEMM for callers that cannot allocate device
  * memory -- for example a plug-in running inside a host framework that owns
  * all device memory and hands it no allocator, or code that must not allocate
@@ -107,15 +143,20 @@ qg_status qgemm_fp8_block(const void *X, int64_t ldx,
  * Arguments and results are those of qgemm_fp8_block without the workspace:
  * the split-K scratch is a fixed 8 MiB array inside the library, which every
  * GPU that loads the library holds until the process exits.  The call
- * allocates nothing.
- *  - A shape whose scratch need (qg_workspace_bytes) exceeds 8 MiB returns
- *    QG_ERR_WORKSPACE before anything is enqueued.
- *  - The first call on a device looks up the array's device address (one
- *    runtime query, with that device current); make that first call before
- *    any stream capture.
+ * allocates nothing and enqueues nothing but the GEMM kernel.
+ *  - Arguments are checked as qgemm_fp8_block checks them, before anything
+ *    is enqueued; then a shape whose scratch need (qg_workspace_bytes)
+ *    exceeds 8 MiB returns QG_ERR_WORKSPACE, also before anything is enqueued.
+ *  - The first call on a device that needs scratch looks up the array's
+ *    device address (one runtime query, with that device current); make
+ *    that first call before any stream capture.
  *  - Every call on a device shares the one array, which keeps the previous
- *    call's contents; each call clears the part it uses on `stream` first.
- *    Calls whose execution overlaps on the GPU (different streams, or
+ *    call's contents.  Its arrival counters start at zero and every
+ *    successful call leaves them at zero.  A call that runs out of time
+ *    (QG_ERR_TIMEOUT) leaves some set: qg_last_device_status, which reports
+ *    that timeout, also clears them (on its stream, synchronously), so read
+ *    the status after an error before the next call.
+ *  - Calls whose execution overlaps on the GPU (different streams, or
  *    concurrent host threads) race on the array and give wrong results:
  *    serialise them.
  */
@@ -202,13 +243,22 @@ qg_status pack_lut3(const uint8_t *codes, void *packed, int N, int K);
 qg_status unpack_lut3(const void *packed, uint8_t *codes, int N, int K);
 
 /*
- * Dequantise n E4M3 codes to BF16 on the device with exactly the conversion
- * the FP8 GEMM uses (no scale applied).  codes and out_bf16 are device
- * pointers; n >= 0.  Exposed so that the conversion can be checked code by
- * code.
+ * Test aid: the FP8 GEMM's activation split on its own, through the same
+ * device functions as the GEMM's split warps.  The weights are never
+ * converted (E4M3 goes to the tensor core as stored); instead every
+ * (row, 128-wide K block) of BF16 X is scaled by a power of two and split
+ * into two E4M3 planes:
+ *   e  = min(126, 134 - biased BF16 exponent of the block's largest |x|)
+ *        (so the largest |x| * 2^e lies in [128, 256)),
+ *   x * 2^e = hi + lo / 16,
+ * exactly whenever |x * 2^e| >= 2^-6, and to within 2^-14 below that.
+ *   X         device, BF16 [blocks, 128] (one block per row), 16-byte aligned
+ *   hi, lo    device, E4M3 codes [blocks, 128], 16-byte aligned
+ *   exponent  device, int32 [blocks]: e of each block
+ * Non-finite X gives unspecified codes.
  */
-qg_status qg_dequant_e4m3_bf16(const uint8_t *codes, void *out_bf16, int64_t n,
-                               struct CUstream_st *stream);
+qg_status qg_debug_fp8_split(const void *X, int64_t blocks, void *hi, void *lo, int *exponent,
+                             struct CUstream_st *stream);
 
 /*
  * Dequantise a packed LUT3 matrix to FP16 D[N, K] (row-major, device) with
@@ -219,9 +269,51 @@ qg_status qg_dequant_lut3(const void *Wq, const void *qmap, const void *scales,
                           void *D, int N, int K, struct CUstream_st *stream);
 
 /*
+ * Dispatch table.  Each call picks its grid (the number of persistent CTAs,
+ * at most one per SM) per (kind, M, N, K): from this process-wide table when
+ * it holds an entry for the shape, else from a built-in cost rule (one CTA
+ * per 128-row tile when the tiles fit on the SMs and that is cheaper, else
+ * stream-K over the SMs).  Any grid gives a result within the comparison rule
+ * of the header (only the order of the FP32 split-K sum changes), and a given
+ * grid gives the same bits on every call.  Entries are set by a caller that
+ * measured the candidates (a tuner, or a test forcing split-K and unsplit
+ * runs of one shape).  A changed entry can change qg_workspace_bytes for the
+ * shape; the table is shared by all threads and devices.
+ *
+ * qg_dispatch_set: ctas in 1 .. SM count of the current device sets the
+ *   entry (a grid larger than the shape's work units is cut to their
+ *   number); ctas == 0 removes it.  M in 1..32.
+ * qg_dispatch_get: the grid the next call of the shape launches on the
+ *   current device (0 for invalid arguments).
+ * qg_dispatch_clear: removes every entry.
+ */
+qg_status qg_dispatch_set(int kind, int M, int N, int K, int ctas);
+int qg_dispatch_get(int kind, int M, int N, int K);
+void qg_dispatch_clear(void);
+
+/*
+ * Test aid: the work split of a shape's schedule, computed on the device by
+ * the same functions the GEMM kernels use.  Work units are (128-row tile,
+ * 128-wide K block) pairs numbered tile-major, ceil(N/128) * ceil(K/128) in
+ * all.  Writes the CTA count to *ctas (host); then, unless ranges or info is
+ * null, launches one small kernel on `stream` that writes, for every CTA g:
+ *   ranges[2g], ranges[2g+1]   device int64: its units [first, end)
+ *   info[6g .. 6g+2]           device int32: for its first tile, the first
+ *                              and last CTA holding units of the tile and the
+ *                              partial-sum slot (0 or 1) of the first one
+ *   info[6g+3 .. 6g+5]         the same for its last tile
+ * capacity: the number of CTAs the arrays hold.
+ */
+qg_status qg_debug_schedule(int kind, int M, int N, int K, int *ctas, int64_t *ranges, int *info, int capacity,
+                            struct CUstream_st *stream);
+
+/*
  * Synchronises `stream`, returns the device status word recorded by kernels
  * since the last call (QG_OK if none failed), and clears it.  The word is per
- * process and device, shared by all streams.
+ * process and device, shared by all streams.  On QG_ERR_TIMEOUT it also
+ * zeroes the arrival counters of qgemm_fp8_block_noalloc's scratch array on
+ * the current device (a caller-owned workspace must be zero-filled by its
+ * owner).
  */
 qg_status qg_last_device_status(struct CUstream_st *stream);
 

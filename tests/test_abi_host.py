@@ -110,9 +110,10 @@ def test_lut3_argument_validation(qg, args, expect):
 
 
 def test_dequant_entry_validation(qg):
-    assert qg.lib.qg_dequant_e4m3_bf16(FAKE, FAKE, 0, None) == 0
-    assert qg.lib.qg_dequant_e4m3_bf16(None, FAKE, 4, None) == 1
-    assert qg.lib.qg_dequant_e4m3_bf16(FAKE, FAKE, -1, None) == 1
+    assert qg.lib.qg_debug_fp8_split(FAKE, 0, FAKE, FAKE, FAKE, None) == 0
+    assert qg.lib.qg_debug_fp8_split(None, 4, FAKE, FAKE, FAKE, None) == 1
+    assert qg.lib.qg_debug_fp8_split(FAKE, -1, FAKE, FAKE, FAKE, None) == 1
+    assert qg.lib.qg_debug_fp8_split(FAKE + 8, 4, FAKE, FAKE, FAKE, None) == 3
     assert qg.lib.qg_dequant_lut3(FAKE, FAKE, FAKE, FAKE, 128, 200, None) == 2
     assert qg.lib.qg_dequant_lut3(None, FAKE, FAKE, FAKE, 128, 256, None) == 1
 
@@ -136,27 +137,41 @@ def test_pack_rejects_wide_codes(qg):
     assert e.value.code == 1
 
 
-def _begin(c, U, G):
-    return c * U // G
+def test_dispatch_and_schedule_argument_validation(qg):
+    """The dispatch table and the schedule probe check their arguments before
+    touching a device."""
+    assert qg.lib.qg_dispatch_set(7, 16, 1024, 5120, 8) == 1       # unknown kind
+    assert qg.lib.qg_dispatch_set(0, 0, 1024, 5120, 8) == 1        # M < 1
+    assert qg.lib.qg_dispatch_set(0, 33, 1024, 5120, 8) == 1       # M > 32
+    assert qg.lib.qg_dispatch_set(0, 16, 0, 5120, 8) == 1          # N < 1
+    assert qg.lib.qg_dispatch_set(0, 16, 1024, 5120, -1) == 1      # negative grid
+    assert qg.lib.qg_dispatch_get(7, 16, 1024, 5120) == 0
+    assert qg.lib.qg_dispatch_get(0, 40, 1024, 5120) == 0
+    g = ctypes.c_int(-1)
+    assert qg.lib.qg_debug_schedule(0, 16, 1024, 5120, None, None, None, 0, None) == 1   # no count pointer
+    assert qg.lib.qg_debug_schedule(0, 16, 1024, 5128, ctypes.byref(g), None, None, 0, None) == 2   # K % 16
+    assert qg.lib.qg_debug_schedule(1, 16, 1024, 5120 + 64, ctypes.byref(g), None, None, 0, None) == 2
+    qg.dispatch_clear()
 
 
-def _owner(x, U, G):
-    return ((x + 1) * G - 1) // U
-
-
-@pytest.mark.parametrize("U", [1, 7, 8, 40, 152, 153, 320, 5440, 7168, 14336, 99991])
-@pytest.mark.parametrize("G", [1, 2, 7, 148, 152])
-def test_stream_k_partition_rule(U, G):
-    """The kernels split U work units over G CTAs as [c*U/G, (c+1)*U/G) and find
-    a unit's owner as ((x+1)*G-1)/U; the two must agree for every unit."""
-    if G > U:
-        return
-    starts = [_begin(c, U, G) for c in range(G + 1)]
-    assert starts[0] == 0 and starts[-1] == U
-    sizes = np.diff(starts)
-    assert sizes.min() >= 1 and sizes.max() - sizes.min() <= 1
-    xs = np.unique(np.concatenate([np.arange(min(U, 3000)), np.array(starts[:-1]),
-                                   np.array(starts[1:]) - 1]))
-    for x in xs:
-        c = _owner(int(x), U, G)
-        assert starts[c] <= x < starts[c + 1]
+def test_multi_argument_validation(qg):
+    """qgemm_fp8_block_multi checks every segment before anything is enqueued."""
+    segs = (qg.Fp8Segment * 5)()
+    for j in range(5):
+        segs[j] = qg.Fp8Segment(FAKE, FAKE, FAKE, 256, 256)
+    ptr = ctypes.cast(segs, ctypes.c_void_p)
+    fn = qg.lib.qgemm_fp8_block_multi
+    assert fn(FAKE, 512, ptr, 0, 4, 512, None, 0, None) == 1      # no segments
+    assert fn(FAKE, 512, ptr, 5, 4, 512, None, 0, None) == 1      # more than QG_MAX_SEGMENTS
+    assert fn(FAKE, 512, None, 2, 4, 512, None, 0, None) == 1     # null table
+    segs[1] = qg.Fp8Segment(None, FAKE, FAKE, 256, 256)
+    assert fn(FAKE, 512, ptr, 3, 4, 512, None, 0, None) == 1      # null W in segment 1
+    segs[1] = qg.Fp8Segment(FAKE + 4, FAKE, FAKE, 256, 256)
+    assert fn(FAKE, 512, ptr, 3, 4, 512, None, 0, None) == 3      # misaligned W in segment 1
+    segs[1] = qg.Fp8Segment(FAKE, FAKE, FAKE, 100, 256)
+    assert fn(FAKE, 512, ptr, 3, 4, 512, None, 0, None) == 1      # ldy < N in segment 1
+    segs[1] = qg.Fp8Segment(FAKE, FAKE, FAKE, 256, 0)
+    assert fn(FAKE, 512, ptr, 3, 4, 512, None, 0, None) == 1      # empty segment
+    segs[1] = qg.Fp8Segment(FAKE, FAKE, FAKE, 256, 256)
+    assert fn(FAKE, 512, ptr, 3, 33, 512, None, 0, None) == 2     # M > 32
+    assert fn(FAKE, 512, ptr, 3, 0, 512, None, 0, None) == 0      # M == 0: no-op

@@ -1,6 +1,12 @@
-"""The kernels' own dequantisers, checked value by value against the oracle
-(bit-exact: the E4M3 -> BF16 and LUT -> FP16 conversions have one correct
-answer)."""
+"""The kernels' own conversions, checked value by value.
+
+* The FP8 GEMM feeds E4M3 weights to the tensor core as stored and splits
+  BF16 activations instead: per (row, 128-wide K block) an exponent e brings
+  the largest |x| into [128, 256), and each x * 2^e becomes two E4M3 codes
+  with x * 2^e = hi + lo / 16.  Every finite BF16 pattern is checked under
+  every exponent the rule can give it.
+* The LUT3 dequantiser is bit-exact against the oracle (one correct answer).
+"""
 import numpy as np
 import pytest
 import torch
@@ -12,19 +18,52 @@ from gpu_util import qg, to_bits
 pytestmark = pytest.mark.gpu
 
 
-def test_e4m3_to_bf16_all_codes_exact():
+def _split_blocks():
+    """Blocks of 128 BF16 patterns covering, for every block-maximum exponent
+    E (biased, 0 = zero/subnormal .. 254), every finite pattern of magnitude
+    at most that maximum, both signs; element 0 holds the maximum (negative in
+    every other block).  Also one all-zero block and one all -0 block."""
+    blocks, expect_e = [], []
+    for E in range(255):
+        mags = np.arange(0, (E + 1) << 7, dtype=np.uint32)
+        pats = np.concatenate([mags, mags | 0x8000]).astype(np.uint16)
+        per = 127
+        nrow = -(-pats.size // per)
+        pats = np.concatenate([pats, np.zeros(nrow * per - pats.size, np.uint16)])
+        blk = np.empty((nrow, 128), np.uint16)
+        blk[:, 0] = (E << 7) | 0x7F
+        blk[1::2, 0] |= 0x8000
+        blk[:, 1:] = pats.reshape(nrow, per)
+        blocks.append(blk)
+        expect_e.append(np.full(nrow, min(126, 134 - E), np.int32))
+    blocks.append(np.zeros((1, 128), np.uint16))
+    blocks.append(np.full((1, 128), 0x8000, np.uint16))
+    expect_e += [np.array([126], np.int32)] * 2
+    return np.concatenate(blocks), np.concatenate(expect_e)
+
+
+def test_fp8_activation_split_exhaustive():
+    """x * 2^e = hi + lo/16 exactly for |x * 2^e| >= 2^-6 and within 2^-14
+    below; e = min(126, 134 - exponent of the block maximum)."""
     q = qg()
-    codes = np.arange(256, dtype=np.uint8)
-    finite = np.array([c for c in codes if c not in (0x7F, 0xFF)], dtype=np.uint8)
-    # every code, in every position of a 4-byte word, plus a ragged tail
-    arr = np.concatenate([np.repeat(finite, 4), np.roll(np.repeat(finite, 4), 1),
-                          np.roll(np.repeat(finite, 4), 2), finite[:3]])
-    out = q.dequant_e4m3_bf16(torch.from_numpy(arr).cuda())
+    X, expect_e = _split_blocks()
+    Xd = torch.from_numpy(X.view(np.int16)).view(torch.bfloat16).cuda()
+    hi, lo, e = q.debug_fp8_split(Xd)
     assert q.last_device_status() == 0
-    got = to_bits(out)
-    ref = oracle.float_to_bf16(oracle.e4m3_to_float(arr))
-    bad = np.nonzero(got != ref)[0]
-    assert bad.size == 0, [(hex(arr[i]), hex(got[i]), hex(ref[i])) for i in bad[:10]]
+    hi, lo, e = hi.cpu().numpy(), lo.cpu().numpy(), e.cpu().numpy()
+    np.testing.assert_array_equal(e, expect_e)
+    table = oracle.e4m3_to_float(np.arange(256, dtype=np.uint8)).astype(np.float64)
+    assert not np.isnan(table[hi]).any() and not np.isnan(table[lo]).any()
+    x = (X.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    target = x * np.exp2(e.astype(np.float64))[:, None]
+    got = table[hi] + table[lo] / 16.0
+    assert np.abs(target).max() < 256.0
+    exact = np.abs(target) >= 2.0 ** -6
+    bad = exact & (got != target)
+    assert not bad.any(), [(hex(int(X[i, j])), int(e[i]), float(target[i, j]), float(got[i, j]))
+                           for i, j in zip(*np.nonzero(bad))][:8]
+    err = np.abs(got - target)[~exact]
+    assert err.max() <= 2.0 ** -14, float(err.max())
 
 
 @pytest.mark.parametrize("N,K", [(128, 256), (200, 384), (384, 1024)])

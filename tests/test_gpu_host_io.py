@@ -99,3 +99,42 @@ def test_host_entry_refuses_pageable_memory():
         q.qgemm_fp8_block_host(Xpage, W, S)
     torch.cuda.synchronize()
     assert q.last_device_status() == 0
+
+
+def test_host_entry_chained_through_host_memory():
+    """With launch overlap on, one call's Y_host is the next call's X_host:
+    the second call's staging kernel must read the first call's finished
+    result (it waits for the preceding grid before it reads X_host), so the
+    chain gives exactly the bits of the same chain on device buffers."""
+    q = qg()
+    q.set_weight_prefetch_overlap(1)
+    try:
+        M = 16
+        pa = cached(("fp8host", M, 5120, 5120), lambda: wl.make_fp8_problem(M, 5120, 5120, config_id=64))
+        pb = cached(("fp8host", M, 1024, 5120), lambda: wl.make_fp8_problem(M, 1024, 5120, config_id=65))
+        Wa, Sa = _device_inputs(pa)
+        Wb, Sb = _device_inputs(pb)
+        ws = q.Workspace()
+        Xd = torch.from_numpy(pa.X.view(np.int16)).view(torch.bfloat16).cuda()
+        ya = q.qgemm_fp8_block(Xd, Wa, Sa, workspace=ws)
+        yb = to_bits(q.qgemm_fp8_block(ya, Wb, Sb, workspace=ws))
+        ya = to_bits(ya)
+        stage = torch.empty(M * 5120, dtype=torch.bfloat16, device="cuda")
+        Xh = _pinned_bf16(pa.X)
+        outs = []
+        for _ in range(3):
+            Yh1 = torch.empty((M, 5120), dtype=torch.int16).pin_memory()
+            Yh1.fill_(0x7FC1)
+            Yh2 = torch.empty((M, 1024), dtype=torch.int16).pin_memory()
+            Yh2.fill_(0x7FC1)
+            q.qgemm_fp8_block_host(Xh, Wa, Sa, Y=Yh1.view(torch.bfloat16), X_stage=stage, workspace=ws)
+            q.qgemm_fp8_block_host(Yh1.view(torch.bfloat16), Wb, Sb, Y=Yh2.view(torch.bfloat16), X_stage=stage,
+                                   workspace=ws)
+            outs.append((Yh1, Yh2))
+        torch.cuda.synchronize()
+        assert q.last_device_status() == 0
+        for Yh1, Yh2 in outs:
+            np.testing.assert_array_equal(Yh1.numpy().view(np.uint16), ya)
+            np.testing.assert_array_equal(Yh2.numpy().view(np.uint16), yb)
+    finally:
+        q.set_weight_prefetch_overlap(0)

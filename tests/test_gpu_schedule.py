@@ -1,0 +1,115 @@
+"""The work decomposition on the device and the dispatch table.
+
+* The unit ranges and split-K bookkeeping the kernels compute (read back with
+  the schedule probe, which runs the kernels' own device functions) are
+  checked against what they must be: a contiguous cover of all units split
+  evenly, and, per tile, the first and last CTA holding its units and the
+  slot of the first one's piece, found by brute force from the ranges.
+* The same shape run split-K and unsplit (grids forced through the dispatch
+  table) gives results within the oracle's budget both ways, each
+  deterministic call after call.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads as wl
+from gpu_util import Fp8Device, Lut3Device, cached, grade_fp8, grade_lut3, qg, to_bits
+
+pytestmark = pytest.mark.gpu
+
+SHAPES = [(16, 17408, 5120), (16, 5120, 17408), (32, 5120, 17408), (1, 1024, 5120), (16, 5120, 5120),
+          (32, 6144, 5120), (7, 200, 336), (1, 256, 512), (20, 3000, 1040)]
+
+
+def _check_schedule(ranges, info, U, KB):
+    G = ranges.shape[0]
+    assert ranges[0, 0] == 0 and ranges[-1, 1] == U
+    assert np.all(ranges[1:, 0] == ranges[:-1, 1]), "ranges are not contiguous"
+    sizes = ranges[:, 1] - ranges[:, 0]
+    assert sizes.min() >= 1 and sizes.max() - sizes.min() <= 1, "units are not split evenly"
+    for g in range(G):
+        for w, u in ((0, ranges[g, 0]), (1, ranges[g, 1] - 1)):
+            t = u // KB
+            lo, hi = t * KB, (t + 1) * KB
+            holders = np.nonzero((ranges[:, 0] < hi) & (ranges[:, 1] > lo))[0]
+            cf, cl = int(holders.min()), int(holders.max())
+            slot = 0 if ranges[cf, 0] == lo else 1
+            assert tuple(info[g, 3 * w:3 * w + 3]) == (cf, cl, slot), (g, w, t)
+
+
+@pytest.mark.parametrize("M,N,K", SHAPES)
+def test_device_work_split(M, N, K):
+    q = qg()
+    KB = -(-K // 128)
+    U = (-(-N // 128)) * KB
+    ranges, info = q.debug_schedule(q.KIND_FP8_BLOCK, M, N, K)
+    assert q.last_device_status() == 0
+    assert ranges.shape[0] == q.dispatch_get(q.KIND_FP8_BLOCK, M, N, K)
+    _check_schedule(ranges, info, U, KB)
+
+
+@pytest.mark.parametrize("G", [1, 3, 40, 41, 77, 152])
+def test_device_work_split_forced_grids(G):
+    q = qg()
+    M, N, K = 16, 5120, 5120
+    try:
+        q.dispatch_set(q.KIND_FP8_BLOCK, M, N, K, G)
+        assert q.dispatch_get(q.KIND_FP8_BLOCK, M, N, K) == G
+        ranges, info = q.debug_schedule(q.KIND_FP8_BLOCK, M, N, K)
+        _check_schedule(ranges, info, 40 * 40, 40)
+    finally:
+        q.dispatch_clear()
+    assert q.dispatch_get(q.KIND_FP8_BLOCK, M, N, K) != 1
+
+
+def _fp8_runs(q, p, dev, Xd, reps=3):
+    ws = q.Workspace()
+    outs = [to_bits(q.qgemm_fp8_block(Xd, dev.W[0], dev.S, workspace=ws)) for _ in range(reps)]
+    assert q.last_device_status() == 0
+    for o in outs[1:]:
+        assert np.array_equal(o, outs[0])
+    return outs[0]
+
+
+@pytest.mark.parametrize("M,N,K,grids", [(16, 5120, 5120, [152, 40, 80, 120]), (32, 5120, 5120, [152, 40, 100]),
+                                         (16, 17408, 5120, [136, 152, 68]), (5, 1024, 5120, [32, 8, 152])])
+def test_fp8_split_and_unsplit_agree(M, N, K, grids):
+    """Split-K over many CTAs, one CTA per tile, and grids in between: every
+    one within the oracle's budget and deterministic."""
+    q = qg()
+    p = cached(("fp8", M, N, K, 70), lambda: wl.make_fp8_problem(M, N, K, config_id=70))
+    dev = Fp8Device(p)
+    Xd = torch.from_numpy(p.X.view(np.int16)).view(torch.bfloat16).cuda()
+    T = -(-N // 128)
+    try:
+        for G in grids:
+            q.dispatch_set(q.KIND_FP8_BLOCK, M, N, K, G)
+            assert q.dispatch_get(q.KIND_FP8_BLOCK, M, N, K) == G
+            if G == T:
+                assert q.workspace_bytes(q.KIND_FP8_BLOCK, M, N, K) == 0
+            y = _fp8_runs(q, p, dev, Xd)
+            ok, rep = grade_fp8(p, y)
+            assert rep.ok, (G, rep)
+    finally:
+        q.dispatch_clear()
+
+
+@pytest.mark.parametrize("grids", [[152, 8, 64]])
+def test_lut3_split_and_unsplit_agree(grids):
+    q = qg()
+    M, N, K = 8, 1024, 4096
+    p = cached(("lut3", M, N, K, 71), lambda: wl.make_lut3_problem(M, N, K, config_id=71))
+    dev = Lut3Device(p)
+    Xd = torch.from_numpy(p.X.view(np.int16)).view(torch.float16).cuda()
+    try:
+        for G in grids:
+            q.dispatch_set(q.KIND_LUT3, M, N, K, G)
+            ws = q.Workspace()
+            outs = [to_bits(q.qgemm_lut3(Xd, dev.Wq, dev.qmap, dev.scales, N, workspace=ws)) for _ in range(3)]
+            assert q.last_device_status() == 0
+            assert all(np.array_equal(o, outs[0]) for o in outs[1:])
+            ok, rep = grade_lut3(p, outs[0])
+            assert rep.ok, (G, rep)
+    finally:
+        q.dispatch_clear()

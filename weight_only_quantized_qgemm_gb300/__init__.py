@@ -9,13 +9,16 @@ The names follow the C ABI in ``include/qgemm.h``:
 
 * :func:`qgemm_fp8_block` -- W8A16 FP8 E4M3 weights with [128 x 128] FP32
   block scales, BF16 activations and output, two-level FP32 fold.
+* :func:`qgemm_fp8_block_multi` -- several of those GEMMs sharing X (e.g. the
+  Q, K and V projections) in one launch, each with its own output.
 * :func:`qgemm_fp8_block_host` -- the same GEMM with X and Y in pinned host
   memory (staged in and stored out by the library's kernels).
 * :func:`qgemm_lut3` -- 3-bit learned-LUT weights (see :func:`pack_lut3`),
   FP16 activations and output.
 * :func:`pack_lut3` / :func:`unpack_lut3` -- offline nibble packer (host).
-* :func:`dequant_e4m3_bf16` / :func:`dequant_lut3` -- the kernels' own
-  dequantisers, exposed for code-by-code checks.
+* :func:`debug_fp8_split` / :func:`dequant_lut3` -- test aids: the FP8
+  kernel's activation split and the LUT3 kernel's dequantiser on their own,
+  exposed for value-by-value checks.
 """
 from __future__ import annotations
 
@@ -26,9 +29,10 @@ import numpy as np
 
 __all__ = [
     "QgemmError", "LIB_PATH", "lib", "status_string", "workspace_bytes", "Workspace",
-    "qgemm_fp8_block", "qgemm_fp8_block_host", "qgemm_lut3", "pack_lut3", "unpack_lut3", "lut3_packed_bytes",
-    "dequant_e4m3_bf16", "dequant_lut3", "last_device_status", "set_wait_timeout_ns",
-    "set_fault_injection", "set_weight_prefetch_overlap", "KIND_FP8_BLOCK", "KIND_LUT3", "STATUS",
+    "qgemm_fp8_block", "qgemm_fp8_block_multi", "qgemm_fp8_block_host", "Fp8Segment", "MAX_SEGMENTS", "qgemm_lut3", "pack_lut3", "unpack_lut3", "lut3_packed_bytes",
+    "debug_fp8_split", "dequant_lut3", "last_device_status", "set_wait_timeout_ns",
+    "set_fault_injection", "set_weight_prefetch_overlap", "dispatch_set", "dispatch_get", "dispatch_clear",
+    "debug_schedule", "KIND_FP8_BLOCK", "KIND_LUT3", "STATUS",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -62,12 +66,17 @@ lib = ctypes.CDLL(LIB_PATH)
 _SIGS = {
     "qg_workspace_bytes": (_S, [_I, _I, _I, _I]),
     "qgemm_fp8_block": (_I, [_P, _L, _P, _P, _P, _L, _I, _I, _I, _P, _S, _P]),
+    "qgemm_fp8_block_multi": (_I, [_P, _L, _P, _I, _I, _I, _P, _S, _P]),
     "qgemm_fp8_block_host": (_I, [_P, _L, _P, _P, _P, _L, _I, _I, _I, _P, _P, _S, _P]),
     "qgemm_lut3": (_I, [_P, _L, _P, _P, _P, _P, _L, _I, _I, _I, _P, _S, _P]),
     "qg_lut3_packed_bytes": (_S, [_I, _I]),
     "pack_lut3": (_I, [_P, _P, _I, _I]),
     "unpack_lut3": (_I, [_P, _P, _I, _I]),
-    "qg_dequant_e4m3_bf16": (_I, [_P, _P, _L, _P]),
+    "qg_debug_fp8_split": (_I, [_P, _L, _P, _P, _P, _P]),
+    "qg_debug_schedule": (_I, [_I, _I, _I, _I, _P, _P, _P, _I, _P]),
+    "qg_dispatch_set": (_I, [_I, _I, _I, _I, _I]),
+    "qg_dispatch_get": (_I, [_I, _I, _I, _I]),
+    "qg_dispatch_clear": (None, []),
     "qg_dequant_lut3": (_I, [_P, _P, _P, _P, _I, _I, _P]),
     "qg_last_device_status": (_I, [_P]),
     "qg_set_wait_timeout_ns": (None, [ctypes.c_uint64]),
@@ -182,6 +191,46 @@ def qgemm_fp8_block(X, W, W_scale, Y=None, workspace=None, stream=None):
     return Y
 
 
+MAX_SEGMENTS = 4
+
+
+class Fp8Segment(ctypes.Structure):
+    """qg_fp8_segment of include/qgemm.h."""
+    _fields_ = [("W", ctypes.c_void_p), ("W_scale", ctypes.c_void_p), ("Y", ctypes.c_void_p),
+                ("ldy", ctypes.c_int64), ("N", ctypes.c_int)]
+
+
+def qgemm_fp8_block_multi(X, weights, Ys=None, workspace=None, stream=None):
+    """Y_j = X . dequant(W_j)^T for every (W_j, W_scale_j) in `weights`
+    (1 to MAX_SEGMENTS of them, sharing X), in one launch; returns the list of
+    Y_j (BF16 [M, N_j]).  Ys (optional): the output tensors, each with unit
+    column stride."""
+    torch = _torch()
+    if X.dtype != torch.bfloat16:
+        raise TypeError("X must be bfloat16")
+    if not 1 <= len(weights) <= MAX_SEGMENTS:
+        raise ValueError(f"between 1 and {MAX_SEGMENTS} weight matrices")
+    M, K = X.shape
+    segs = (Fp8Segment * len(weights))()
+    outs = []
+    rows = 0
+    for j, (W, S) in enumerate(weights):
+        if W.dtype not in (torch.uint8, torch.float8_e4m3fn) or not W.is_contiguous():
+            raise TypeError("W must hold contiguous E4M3 codes (uint8 or float8_e4m3fn)")
+        N = W.shape[0]
+        if W.shape[1] != K or tuple(S.shape) != (-(-N // 128), -(-K // 128)) or S.dtype != torch.float32 \
+                or not S.is_contiguous():
+            raise ValueError(f"segment {j}: shape mismatch between X, W and W_scale")
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device=X.device) if Ys is None else Ys[j]
+        outs.append(Y)
+        segs[j] = Fp8Segment(W.data_ptr(), S.data_ptr(), Y.data_ptr(), _ld(Y), N)
+        rows += -(-N // 128) * 128
+    ws, wsb = _workspace_for(KIND_FP8_BLOCK, M, rows, K, workspace, X.device)
+    _check(lib.qgemm_fp8_block_multi(X.data_ptr(), _ld(X), ctypes.cast(segs, ctypes.c_void_p), len(weights), M, K,
+                                     ws, wsb, _stream_ptr(stream)), "qgemm_fp8_block_multi")
+    return outs
+
+
 _default_stage = {}
 
 
@@ -271,14 +320,20 @@ def unpack_lut3(packed: np.ndarray, N: int, K: int) -> np.ndarray:
     return out
 
 
-def dequant_e4m3_bf16(codes, out=None, stream=None):
-    """E4M3 codes (uint8 CUDA tensor) -> BF16, with the FP8 GEMM's own conversion."""
+def debug_fp8_split(X, stream=None):
+    """The FP8 GEMM's activation split of BF16 X [B, 128] (one 128-wide K
+    block per row): returns (hi, lo, e) with hi, lo uint8 E4M3 codes [B, 128]
+    and e int32 [B], such that x * 2^e = hi + lo / 16 (see include/qgemm.h)."""
     torch = _torch()
-    if out is None:
-        out = torch.empty(codes.shape, dtype=torch.bfloat16, device=codes.device)
-    _check(lib.qg_dequant_e4m3_bf16(codes.data_ptr(), out.data_ptr(), codes.numel(), _stream_ptr(stream)),
-           "qg_dequant_e4m3_bf16")
-    return out
+    if X.dtype != torch.bfloat16 or X.dim() != 2 or X.shape[1] != 128 or not X.is_contiguous():
+        raise ValueError("X must be a contiguous bfloat16 [B, 128] tensor")
+    B = X.shape[0]
+    hi = torch.empty((B, 128), dtype=torch.uint8, device=X.device)
+    lo = torch.empty((B, 128), dtype=torch.uint8, device=X.device)
+    e = torch.empty((B,), dtype=torch.int32, device=X.device)
+    _check(lib.qg_debug_fp8_split(X.data_ptr(), B, hi.data_ptr(), lo.data_ptr(), e.data_ptr(), _stream_ptr(stream)),
+           "qg_debug_fp8_split")
+    return hi, lo, e
 
 
 def dequant_lut3(Wq, qmap, scales, N: int, K: int, out=None, stream=None):
@@ -308,3 +363,34 @@ def set_weight_prefetch_overlap(enable: bool) -> None:
     """Let consecutive GEMMs on a stream overlap (weights stream early); see
     include/qgemm.h for the condition under which this is safe."""
     lib.qg_set_weight_prefetch_overlap(1 if enable else 0)
+
+
+def dispatch_set(kind: int, M: int, N: int, K: int, ctas: int) -> None:
+    """Set (ctas > 0) or remove (ctas == 0) the dispatch-table grid of a shape."""
+    _check(lib.qg_dispatch_set(kind, M, N, K, ctas), "qg_dispatch_set")
+    _ws_need.clear()   # a shape's workspace need follows its grid
+
+
+def dispatch_get(kind: int, M: int, N: int, K: int) -> int:
+    """The grid (CTA count) the next call of this shape launches."""
+    return int(lib.qg_dispatch_get(kind, M, N, K))
+
+
+def dispatch_clear() -> None:
+    lib.qg_dispatch_clear()
+    _ws_need.clear()
+
+
+def debug_schedule(kind: int, M: int, N: int, K: int, stream=None):
+    """The device's work split of a shape: (ranges int64 [G, 2], info int32
+    [G, 6]) as numpy arrays (see include/qgemm.h)."""
+    torch = _torch()
+    g = ctypes.c_int(0)
+    _check(lib.qg_debug_schedule(kind, M, N, K, ctypes.byref(g), None, None, 0, None), "qg_debug_schedule")
+    G = g.value
+    ranges = torch.empty((G, 2), dtype=torch.int64, device="cuda")
+    info = torch.empty((G, 6), dtype=torch.int32, device="cuda")
+    _check(lib.qg_debug_schedule(kind, M, N, K, ctypes.byref(g), ranges.data_ptr(), info.data_ptr(), G,
+                                 _stream_ptr(stream)), "qg_debug_schedule")
+    torch.cuda.synchronize()
+    return ranges.cpu().numpy(), info.cpu().numpy()

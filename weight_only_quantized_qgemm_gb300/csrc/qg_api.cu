@@ -1,6 +1,7 @@
 // C ABI of libqgemm: argument validation, the per-shape dispatch table,
-// tensor-map encoding, the device status word, the code-by-code dequant
-// kernels and the offline LUT3 packer.  See include/qgemm.h for the contract.
+// tensor-map encoding, the device status word, the test-aid kernels (the
+// FP8 activation split, the LUT3 dequantiser) and the offline LUT3 packer.
+// See include/qgemm.h for the contract.
 #include <atomic>
 #include <cstring>
 #include <mutex>
@@ -9,7 +10,7 @@
 #include <cuda_fp16.h>
 
 #include "../../include/qgemm.h"
-#include "qg_device.cuh"
+#include "qg_gemm.cuh"
 #include "qg_internal.h"
 
 namespace qg {
@@ -98,8 +99,10 @@ namespace {
 
 // ----------------------------------------------------------------- dispatch
 // Per-(kind, M, N, K) choice of MMA width and grid.  The MMA N side is 16 for
-// M <= 16 and 32 above (one weight pass for every M <= 32).  Two grids are
-// weighed by the work units (128 rows x 128 K) of their busiest CTA:
+// M <= 16 and 32 above (one weight pass for every M <= 32).  The grid comes
+// from the dispatch table when it holds an entry for the shape (set by a
+// caller, e.g. after measuring candidates), else from a cost rule weighing
+// two grids by the work units (128 rows x 128 K) of their busiest CTA:
 //  - one CTA per 128-row tile, when the tiles fit on the SMs: no tile is
 //    split, so no partial sums and no reduction;
 //  - stream-K: one CTA per SM, the units split evenly, capped so that a tile
@@ -121,19 +124,43 @@ bool splits(long long U, int KU, int G) {
     return false;
 }
 
+// The dispatch table: process-wide, shared by all devices and threads.  A
+// generation counter tells the per-thread schedule caches to look again.
+struct TableEntry {
+    int kind, M, N, K, ctas;
+};
+std::mutex g_table_mu;
+TableEntry g_table[256];
+int g_table_n = 0;
+std::atomic<uint64_t> g_table_gen{1};
+
+int table_lookup(int kind, int M, int N, int K) {
+    std::lock_guard<std::mutex> lk(g_table_mu);
+    for (int i = 0; i < g_table_n; ++i) {
+        const TableEntry& e = g_table[i];
+        if (e.kind == kind && e.M == M && e.N == N && e.K == K) return e.ctas;
+    }
+    return 0;
+}
+
 Schedule choose_schedule(int kind, int M, int N, int K, int sms) {
-    (void)kind;
     Schedule s;
     s.nmma = M <= 16 ? 16 : 32;
     s.T = (N + 127) / 128;
     s.KU = (K + 127) / 128;   // one unit = 128 rows x one 128-wide K block
     s.U = static_cast<long long>(s.T) * s.KU;
+    const int forced = table_lookup(kind, M, N, K);
     long long g = sms;
-    if (g > s.U) g = s.U;
-    if (g > static_cast<long long>(kMaxPiecesPerTile) * s.T) g = static_cast<long long>(kMaxPiecesPerTile) * s.T;
-    if (g < 1) g = 1;
-    long long cost = ceil_div(s.U, g) + (splits(s.U, s.KU, static_cast<int>(g)) ? kSplitCostUnits : 0);
-    if (s.T <= sms && static_cast<long long>(s.KU) <= cost) g = s.T;
+    if (forced > 0) {
+        g = forced;
+        if (g > s.U) g = s.U;
+    } else {
+        if (g > s.U) g = s.U;
+        if (g > static_cast<long long>(kMaxPiecesPerTile) * s.T) g = static_cast<long long>(kMaxPiecesPerTile) * s.T;
+        if (g < 1) g = 1;
+        long long cost = ceil_div(s.U, g) + (splits(s.U, s.KU, static_cast<int>(g)) ? kSplitCostUnits : 0);
+        if (s.T <= sms && static_cast<long long>(s.KU) <= cost) g = s.T;
+    }
     s.G = static_cast<int>(g);
     s.max_ctas = sms > s.G ? sms : s.G;
     return s;
@@ -142,14 +169,16 @@ Schedule choose_schedule(int kind, int M, int N, int K, int sms) {
 // True when some tile's units are spread over more than one CTA.
 bool schedule_splits(const Schedule& s) { return splits(s.U, s.KU, s.G); }
 
-// Per-thread caches of the last few schedules (keyed by kind, shape and SM
-// count) and weight tensor maps (keyed by address and shape, which determine
-// the map): the schedule search walks every CTA boundary and the map encoding
-// is a driver call, both otherwise paid on every GEMM call.
+// Per-thread caches of the last few schedules (keyed by kind, shape, SM
+// count and dispatch-table generation) and weight tensor maps (keyed by
+// address and shape, which determine the map): the schedule search walks
+// every CTA boundary and the map encoding is a driver call, both otherwise
+// paid on every GEMM call.
 constexpr int kCacheWays = 8;
 
 struct SchedEntry {
     int kind = -1, M = 0, N = 0, K = 0, sms = 0;
+    uint64_t gen = 0;
     Schedule s;
     size_t ws = 0;
 };
@@ -159,8 +188,9 @@ size_t workspace_bytes_uncached(const Schedule& s);
 const SchedEntry& cached_schedule(int kind, int M, int N, int K, int sms) {
     thread_local SchedEntry cache[kCacheWays];
     thread_local int next = 0;
+    const uint64_t gen = g_table_gen.load(std::memory_order_acquire);
     for (const SchedEntry& e : cache)
-        if (e.kind == kind && e.M == M && e.N == N && e.K == K && e.sms == sms) return e;
+        if (e.kind == kind && e.M == M && e.N == N && e.K == K && e.sms == sms && e.gen == gen) return e;
     SchedEntry& e = cache[next];
     next = (next + 1) % kCacheWays;
     e.kind = kind;
@@ -168,6 +198,7 @@ const SchedEntry& cached_schedule(int kind, int M, int N, int K, int sms) {
     e.N = N;
     e.K = K;
     e.sms = sms;
+    e.gen = gen;
     e.s = choose_schedule(kind, M, N, K, sms);
     e.ws = workspace_bytes_uncached(e.s);
     return e;
@@ -247,20 +278,27 @@ uint32_t* device_status_ptr() {
 // ----------------------------------------------------------------- small kernels
 namespace {
 
-__global__ void dequant_e4m3_kernel(const uint8_t* __restrict__ codes, uint32_t* __restrict__ out, int64_t n) {
-    const int64_t nq = (n + 3) / 4;
-    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < nq;
-         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        uint32_t r = 0;
-        for (int b = 0; b < 4; ++b)
-            if (4 * i + b < n) r |= static_cast<uint32_t>(codes[4 * i + b]) << (8 * b);
-        uint32_t lo, hi;
-        e4m3x4_to_bf16(r, lo, hi);
-        const uint32_t v[4] = {lo & 0xFFFFu, lo >> 16, hi & 0xFFFFu, hi >> 16};
-        uint16_t* o = reinterpret_cast<uint16_t*>(out);
-        for (int b = 0; b < 4; ++b)
-            if (4 * i + b < n) o[4 * i + b] = static_cast<uint16_t>(v[b]);
-    }
+// One warp per 128-element block of BF16 activations: the FP8 GEMM's
+// activation split (block exponent from the largest |x|, then the hi/lo E4M3
+// codes of every x * 2^e), through the device functions the GEMM's split
+// warps use.  Lane l handles elements 4l .. 4l+3.
+__global__ void split_probe_kernel(const uint2* __restrict__ x, int64_t blocks, uint32_t* __restrict__ hi,
+                                   uint32_t* __restrict__ lo, int* __restrict__ exponent) {
+    const int lane = threadIdx.x & 31;
+    const int64_t blk = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    if (blk >= blocks) return;
+    const uint2 v = x[blk * 32 + lane];
+    uint32_t m2 = bf16x2_absmax(v.x, v.y) & 0x7FFF7FFFu;
+    uint32_t mx = max(m2 & 0xFFFFu, m2 >> 16);
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    const int e = split_exponent(mx);
+    const uint32_t pw2 = bf16x2_pow2(e);
+    uint32_t h, l;
+    split_e4m3x4(bf16x2_mul(v.x, pw2), bf16x2_mul(v.y, pw2), h, l);
+    hi[blk * 32 + lane] = h;
+    lo[blk * 32 + lane] = l;
+    if (lane == 0) exponent[blk] = e;
 }
 
 // One thread per (row, 8-code word) of the packed LUT3 layout.
@@ -303,6 +341,27 @@ __global__ void zero_rows_kernel(uint16_t* Y, int64_t ldy, int M, int N) {
         Y[(t / N) * ldy + (t % N)] = 0;
 }
 
+// One warp per CTA of a schedule: the CTA's unit range and its split-K
+// bookkeeping (first and last contributing CTA and slot of its first and last
+// tile), through the device functions the GEMM kernels use.
+__global__ void schedule_probe_kernel(long long U, int G, int KB, long long* __restrict__ ranges,
+                                      int* __restrict__ info) {
+    const int cta = blockIdx.x;
+    const int lane = threadIdx.x;
+    gemm::Params p{};
+    p.U = U;
+    p.G = G;
+    p.KB = KB;
+    const long long u0 = gemm::unit_begin(cta, U, G);
+    const long long u1 = gemm::unit_begin(cta + 1, U, G);
+    const int v = gemm::split_info_lane(p, u0, u1, lane);
+    if (lane == 0) {
+        ranges[2 * cta] = u0;
+        ranges[2 * cta + 1] = u1;
+    }
+    if (lane < 6) info[6 * cta + lane] = v;
+}
+
 int grid_for(int64_t work, int threads) {
     int64_t g = (work + threads - 1) / threads;
     if (g > 4096) g = 4096;
@@ -312,8 +371,12 @@ int grid_for(int64_t work, int threads) {
 
 }  // namespace
 
-cudaError_t launch_dequant_e4m3(const uint8_t* codes, void* out, int64_t n, cudaStream_t st) {
-    dequant_e4m3_kernel<<<grid_for((n + 3) / 4, 256), 256, 0, st>>>(codes, static_cast<uint32_t*>(out), n);
+cudaError_t launch_split_probe(const void* X, int64_t blocks, void* hi, void* lo, int* exponent, cudaStream_t st) {
+    const int64_t threads = blocks * 32;
+    const int64_t grid = (threads + 255) / 256;
+    split_probe_kernel<<<static_cast<unsigned>(grid), 256, 0, st>>>(static_cast<const uint2*>(X), blocks,
+                                                                    static_cast<uint32_t*>(hi),
+                                                                    static_cast<uint32_t*>(lo), exponent);
     return cudaGetLastError();
 }
 
@@ -333,6 +396,21 @@ cudaError_t launch_zero_rows(void* Y, int64_t ldy, int M, int N, cudaStream_t st
     return cudaGetLastError();
 }
 
+// Argument checks of the FP8 entry points, in the order the header lists the
+// errors; M == 0 or N == 0 is valid (a no-op).
+qg_status check_fp8_args(const void* X, int64_t ldx, const void* W, const void* W_scale, const void* Y, int64_t ldy,
+                         int M, int N, int K) {
+    if (M < 0 || N < 0 || K < 0) return QG_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return QG_OK;
+    if (!X || !W || !W_scale || !Y) return QG_ERR_INVALID_ARG;
+    if (M > 32 || K % 16 != 0) return QG_ERR_UNSUPPORTED_SHAPE;
+    if (ldx < K || ldy < N) return QG_ERR_INVALID_ARG;
+    if (!aligned16(X) || !aligned16(W) || (ldx % 8) != 0) return QG_ERR_MISALIGNED;
+    if ((reinterpret_cast<uintptr_t>(W_scale) & 3u) != 0 || (reinterpret_cast<uintptr_t>(Y) & 1u) != 0)
+        return QG_ERR_MISALIGNED;
+    return QG_OK;
+}
+
 }  // namespace qg
 
 // =================================================================== C ABI
@@ -350,14 +428,8 @@ size_t qg_workspace_bytes(int kind, int M, int N, int K) {
 
 qg_status qgemm_fp8_block(const void* X, int64_t ldx, const uint8_t* W, const float* W_scale, void* Y, int64_t ldy,
                           int M, int N, int K, void* workspace, size_t workspace_bytes_, cudaStream_t stream) {
-    if (M < 0 || N < 0 || K < 0) return QG_ERR_INVALID_ARG;
-    if (M == 0 || N == 0) return QG_OK;
-    if (!X || !W || !W_scale || !Y) return QG_ERR_INVALID_ARG;
-    if (M > 32 || K % 16 != 0) return QG_ERR_UNSUPPORTED_SHAPE;
-    if (ldx < K || ldy < N) return QG_ERR_INVALID_ARG;
-    if (!aligned16(X) || !aligned16(W) || (ldx % 8) != 0) return QG_ERR_MISALIGNED;
-    if ((reinterpret_cast<uintptr_t>(W_scale) & 3u) != 0 || (reinterpret_cast<uintptr_t>(Y) & 1u) != 0)
-        return QG_ERR_MISALIGNED;
+    const qg_status v = check_fp8_args(X, ldx, W, W_scale, Y, ldy, M, N, K);
+    if (v != QG_OK || M == 0 || N == 0) return v;
     DeviceInfo* d = device_info();
     if (!d) return QG_ERR_CUDA;
     if (K == 0) return launch_zero_rows(Y, ldy, M, N, stream) == cudaSuccess ? QG_OK : QG_ERR_CUDA;
@@ -366,21 +438,66 @@ qg_status qgemm_fp8_block(const void* X, int64_t ldx, const uint8_t* W, const fl
     const size_t need = se.ws;
     if (need > 0 && (!workspace || workspace_bytes_ < need || (reinterpret_cast<uintptr_t>(workspace) & 255u)))
         return QG_ERR_WORKSPACE;
+    Fp8Args a{};
+    Fp8Maps maps{};
     const CUtensorMap* tmW = cached_tmap(W, static_cast<uint64_t>(K), static_cast<uint64_t>(N), kMapFp8Weights);
     if (!tmW) return QG_ERR_CUDA;
-    Fp8Args a;
+    maps.m[0] = *tmW;
     a.X = X;
     a.ldx = ldx;
-    a.W = W;
-    a.S = W_scale;
+    a.nseg = 1;
+    a.seg[0] = Fp8Seg{W, W_scale, Y, ldy, N};
     a.lds = (K + 127) / 128;
-    a.Y = Y;
-    a.ldy = ldy;
     a.M = M;
-    a.N = N;
     a.K = K;
     a.ws = need > 0 ? workspace : nullptr;
-    return launch_fp8(a, s, *tmW, launch_ctl(d), stream) == cudaSuccess ? QG_OK : QG_ERR_CUDA;
+    return launch_fp8(a, s, maps, launch_ctl(d), stream) == cudaSuccess ? QG_OK : QG_ERR_CUDA;
+}
+
+qg_status qgemm_fp8_block_multi(const void* X, int64_t ldx, const qg_fp8_segment* segments, int nseg, int M, int K,
+                                void* workspace, size_t workspace_bytes_, cudaStream_t stream) {
+    if (nseg < 1 || nseg > QG_MAX_SEGMENTS || !segments) return QG_ERR_INVALID_ARG;
+    int64_t rows = 0;   // the segments' tiles, concatenated
+    for (int j = 0; j < nseg; ++j) {
+        const qg_fp8_segment& g = segments[j];
+        if (g.N < 1) return QG_ERR_INVALID_ARG;
+        const qg_status v = check_fp8_args(X, ldx, g.W, g.W_scale, g.Y, g.ldy, M, g.N, K);
+        if (v != QG_OK) return v;
+        rows += (static_cast<int64_t>(g.N) + 127) / 128 * 128;
+    }
+    if (M == 0) return QG_OK;
+    if (rows > INT32_MAX) return QG_ERR_UNSUPPORTED_SHAPE;
+    DeviceInfo* d = device_info();
+    if (!d) return QG_ERR_CUDA;
+    if (K == 0) {
+        for (int j = 0; j < nseg; ++j)
+            if (launch_zero_rows(segments[j].Y, segments[j].ldy, M, segments[j].N, stream) != cudaSuccess)
+                return QG_ERR_CUDA;
+        return QG_OK;
+    }
+    const int N = static_cast<int>(rows);
+    const SchedEntry& se = cached_schedule(QG_KIND_FP8_BLOCK, M, N, K, d->sms);
+    const Schedule s = se.s;
+    const size_t need = se.ws;
+    if (need > 0 && (!workspace || workspace_bytes_ < need || (reinterpret_cast<uintptr_t>(workspace) & 255u)))
+        return QG_ERR_WORKSPACE;
+    Fp8Args a{};
+    Fp8Maps maps{};
+    for (int j = 0; j < nseg; ++j) {
+        const qg_fp8_segment& g = segments[j];
+        const CUtensorMap* tm = cached_tmap(g.W, static_cast<uint64_t>(K), static_cast<uint64_t>(g.N), kMapFp8Weights);
+        if (!tm) return QG_ERR_CUDA;
+        maps.m[j] = *tm;   // copied at once: a later lookup may reuse the cache entry
+        a.seg[j] = Fp8Seg{g.W, g.W_scale, g.Y, g.ldy, g.N};
+    }
+    a.X = X;
+    a.ldx = ldx;
+    a.nseg = nseg;
+    a.lds = (K + 127) / 128;
+    a.M = M;
+    a.K = K;
+    a.ws = need > 0 ? workspace : nullptr;
+    return launch_fp8(a, s, maps, launch_ctl(d), stream) == cudaSuccess ? QG_OK : QG_ERR_CUDA;
 }
 
 qg_status qgemm_lut3(const void* X, int64_t ldx, const void* Wq, const void* qmap, const void* scales, void* Y,
@@ -483,12 +600,15 @@ qg_status unpack_lut3(const void* packed, uint8_t* codes, int N, int K) {
     return QG_OK;
 }
 
-qg_status qg_dequant_e4m3_bf16(const uint8_t* codes, void* out_bf16, int64_t n, cudaStream_t stream) {
-    if (n < 0) return QG_ERR_INVALID_ARG;
-    if (n == 0) return QG_OK;
-    if (!codes || !out_bf16) return QG_ERR_INVALID_ARG;
-    if ((reinterpret_cast<uintptr_t>(out_bf16) & 1u) != 0) return QG_ERR_MISALIGNED;
-    return launch_dequant_e4m3(codes, out_bf16, n, stream) == cudaSuccess ? QG_OK : QG_ERR_CUDA;
+qg_status qg_debug_fp8_split(const void* X, int64_t blocks, void* hi, void* lo, int* exponent,
+                             cudaStream_t stream) {
+    if (blocks < 0) return QG_ERR_INVALID_ARG;
+    if (blocks == 0) return QG_OK;
+    if (!X || !hi || !lo || !exponent) return QG_ERR_INVALID_ARG;
+    if (blocks > (int64_t(1) << 31) / 32) return QG_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned16(X) || !aligned16(hi) || !aligned16(lo) || (reinterpret_cast<uintptr_t>(exponent) & 3u))
+        return QG_ERR_MISALIGNED;
+    return launch_split_probe(X, blocks, hi, lo, exponent, stream) == cudaSuccess ? QG_OK : QG_ERR_CUDA;
 }
 
 qg_status qg_dequant_lut3(const void* Wq, const void* qmap, const void* scales, void* D, int N, int K,
@@ -503,6 +623,64 @@ qg_status qg_dequant_lut3(const void* Wq, const void* qmap, const void* scales, 
     return launch_dequant_lut3(Wq, qmap, scales, D, N, K, stream) == cudaSuccess ? QG_OK : QG_ERR_CUDA;
 }
 
+qg_status qg_debug_schedule(int kind, int M, int N, int K, int* ctas, int64_t* ranges, int* info, int capacity,
+                            cudaStream_t stream) {
+    if (kind != QG_KIND_FP8_BLOCK && kind != QG_KIND_LUT3) return QG_ERR_INVALID_ARG;
+    if (M < 1 || M > 32 || N < 1 || K < 1 || !ctas) return QG_ERR_INVALID_ARG;
+    if (kind == QG_KIND_FP8_BLOCK ? K % 16 != 0 : K % 128 != 0) return QG_ERR_UNSUPPORTED_SHAPE;
+    DeviceInfo* d = device_info();
+    if (!d) return QG_ERR_CUDA;
+    const Schedule s = cached_schedule(kind, M, N, K, d->sms).s;
+    *ctas = s.G;
+    if (!ranges || !info) return QG_OK;   // a query of the CTA count only
+    if (capacity < s.G) return QG_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(ranges) & 7u) || (reinterpret_cast<uintptr_t>(info) & 3u)) return QG_ERR_MISALIGNED;
+    schedule_probe_kernel<<<s.G, 32, 0, stream>>>(s.U, s.G, s.KU, reinterpret_cast<long long*>(ranges), info);
+    return cudaGetLastError() == cudaSuccess ? QG_OK : QG_ERR_CUDA;
+}
+
+qg_status qg_dispatch_set(int kind, int M, int N, int K, int ctas) {
+    if (kind != QG_KIND_FP8_BLOCK && kind != QG_KIND_LUT3) return QG_ERR_INVALID_ARG;
+    if (M < 1 || M > 32 || N < 1 || K < 1 || ctas < 0) return QG_ERR_INVALID_ARG;
+    DeviceInfo* d = device_info();
+    if (!d) return QG_ERR_CUDA;
+    if (ctas > d->sms) return QG_ERR_INVALID_ARG;
+    {
+        std::lock_guard<std::mutex> lk(g_table_mu);
+        int at = -1;
+        for (int i = 0; i < g_table_n; ++i) {
+            const TableEntry& e = g_table[i];
+            if (e.kind == kind && e.M == M && e.N == N && e.K == K) at = i;
+        }
+        if (ctas == 0) {
+            if (at >= 0) g_table[at] = g_table[--g_table_n];
+        } else if (at >= 0) {
+            g_table[at].ctas = ctas;
+        } else {
+            if (g_table_n == static_cast<int>(sizeof(g_table) / sizeof(g_table[0]))) return QG_ERR_INVALID_ARG;
+            g_table[g_table_n++] = TableEntry{kind, M, N, K, ctas};
+        }
+    }
+    g_table_gen.fetch_add(1, std::memory_order_acq_rel);
+    return QG_OK;
+}
+
+int qg_dispatch_get(int kind, int M, int N, int K) {
+    if (kind != QG_KIND_FP8_BLOCK && kind != QG_KIND_LUT3) return 0;
+    if (M < 1 || M > 32 || N < 1 || K < 1) return 0;
+    DeviceInfo* d = device_info();
+    if (!d) return 0;
+    return cached_schedule(kind, M, N, K, d->sms).s.G;
+}
+
+void qg_dispatch_clear(void) {
+    {
+        std::lock_guard<std::mutex> lk(g_table_mu);
+        g_table_n = 0;
+    }
+    g_table_gen.fetch_add(1, std::memory_order_acq_rel);
+}
+
 qg_status qg_last_device_status(cudaStream_t stream) {
     DeviceInfo* d = device_info();
     if (!d) return QG_ERR_CUDA;
@@ -510,7 +688,12 @@ qg_status qg_last_device_status(cudaStream_t stream) {
     uint32_t word = 0;
     if (cudaMemcpy(&word, d->status, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return QG_ERR_CUDA;
     if (word != 0 && cudaMemset(d->status, 0, sizeof(word)) != cudaSuccess) return QG_ERR_CUDA;
-    if (word & kDevTimeout) return QG_ERR_TIMEOUT;
+    if (word & kDevTimeout) {
+        // a call that timed out may have been a no-alloc call: its arrival
+        // counters in the library's own scratch array are left set
+        if (noalloc_clear_counters(stream) != cudaSuccess) return QG_ERR_CUDA;
+        return QG_ERR_TIMEOUT;
+    }
     return word ? QG_ERR_CUDA : QG_OK;
 }
 

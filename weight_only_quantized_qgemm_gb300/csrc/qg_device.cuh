@@ -333,30 +333,6 @@ __device__ __forceinline__ uint32_t f16x2_mul(uint32_t a, uint32_t b) {
     return d;
 }
 
-// Four E4M3 codes r = [c3 c2 c1 c0] (c0 = lowest K) -> lo = BF16x2 {c0, c1},
-// hi = BF16x2 {c2, c3}; exact for every finite code, subnormals included.
-// A byte permute builds, per output pair, [sgn(c1) x 8 | c1 | sgn(c0) x 8 | c0];
-// a shift left by 4 (an integer multiply by 16, which runs on the FMA pipe
-// and leaves the ALU pipe to the permute and the mask) puts each code's 7
-// magnitude bits under the BF16 exponent/mantissa boundary with copies of its
-// sign above them, and a mask keeps the sign bit and the magnitude.  The
-// result is 2^-120 times the E4M3 value (a BF16 subnormal when the E4M3
-// exponent field is 0); one BF16 multiply by 2^120 restores the scale exactly.
-__device__ __forceinline__ uint32_t mul_lo_u32(uint32_t a, uint32_t b) {
-    uint32_t d;
-    asm("mul.lo.u32 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-    return d;
-}
-
-__device__ __forceinline__ void e4m3x4_to_bf16(uint32_t r, uint32_t& lo, uint32_t& hi) {
-    constexpr uint32_t kTwo120 = 0x7B807B80u;  // BF16x2 {2^120, 2^120}
-    constexpr uint32_t kKeep = 0x87F087F0u;    // sign + 7 magnitude bits per half
-    const uint32_t p0 = prmt(r, 0u, 0x9180u);  // [sgn(c1) | c1 | sgn(c0) | c0]
-    const uint32_t p1 = prmt(r, 0u, 0xB3A2u);  // [sgn(c3) | c3 | sgn(c2) | c2]
-    lo = bf16x2_mul(mul_lo_u32(p0, 16u) & kKeep, kTwo120);
-    hi = bf16x2_mul(mul_lo_u32(p1, 16u) & kKeep, kTwo120);
-}
-
 // ---- activation split for the E4M3 tensor-core path
 // Per-halfword unsigned maximum (used on |x| bit patterns, which order like
 // the magnitudes they encode).
@@ -386,6 +362,22 @@ __device__ __forceinline__ void split_e4m3x2(uint32_t xw, uint16_t& hi, uint16_t
     asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(h2), "r"(hh));
     asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(d), "r"(0x4C004C00u));   // x 16
     asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(lo) : "r"(d));
+}
+
+// Exponent of the activation split of one (row, 128-wide K block): with
+// `amax` the bit pattern of the block's largest |x| (sign cleared), 2^e
+// brings it into [128, 256): e = 134 - (its biased BF16 exponent).  The cap
+// at 126 keeps 2^e and 2^-e normal numbers; a block of zeros and subnormals
+// takes e = 126.
+__device__ __forceinline__ int split_exponent(uint32_t amax) {
+    const int e = 134 - static_cast<int>(amax >> 7);
+    return e > 126 ? 126 : e;
+}
+
+// BF16x2 {2^e, 2^e} for -126 <= e <= 126 (used to scale two X values at once).
+__device__ __forceinline__ uint32_t bf16x2_pow2(int e) {
+    const uint32_t pw = static_cast<uint32_t>(e + 127) << 7;
+    return pw | (pw << 16);
 }
 
 // Per half: the larger magnitude of a and b (the sign bit of the result is the

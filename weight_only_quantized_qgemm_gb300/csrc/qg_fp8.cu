@@ -33,14 +33,14 @@
 //   warps 3-6    fold / epilogue, one per TMEM lane quadrant (warp % 4).
 //   warps 7-14   X split: four groups of 2 warps taking every fourth unit, 32
 //                (64 for 32 rows) elements of a row per thread.  Each
-//                thread copies its own share of a unit's BF16 X slice several
-//                units ahead (cp.async through the load/store path: a TMA copy
-//                would queue behind the weight tiles already in flight and
-//                arrive microseconds later), takes the row maxima and
-//                exponents of its group's next unit while it converts the
-//                current one, and writes the hi/lo E4M3 planes in the
-//                swizzled K-major layout, and s * 2^-e per row beside them
-//                (s = the unit's block scale).
+//                thread copies its own share of a unit's BF16 X slice two of
+//                its group's units ahead (cp.async through the load/store
+//                path: a TMA copy would queue behind the weight tiles already
+//                in flight and arrive microseconds later), converts the
+//                current unit from registers, writes the hi/lo E4M3 planes in
+//                the swizzled K-major layout and s * 2^-e per row beside them
+//                (s = the unit's block scale), then takes the row maxima and
+//                exponents of its group's next unit.
 // A unit is 128 weight rows x one 128-wide K block.  The schedule (tiles of
 // 128 rows, split-K pieces, last-arriver reduction) is the shared one of
 // qg_gemm.cuh.
@@ -75,8 +75,10 @@ struct Fp8Layout {
     static constexpr int kWBytes = 128 * 128;    // one E4M3 unit
     static constexpr int kXbSlot = NX * 256;     // BF16 X slice, [16-byte chunk j][split thread of the group]
     static constexpr int kX8Slot = kN * 128;     // both planes, 128-byte rows
-    static constexpr int kXAhead = 1;                  // a group's units of X copied ahead
-    static constexpr int kXbStages = kXAhead + 1;      // per group
+    // per group: two BF16 X slots, so that a unit's copy is issued one of the
+    // group's units before its scan (the slot is refilled as soon as the scan
+    // has read it into registers)
+    static constexpr int kXbStages = 2;
     // X plane slots: a slot is refilled once the MMAs that read it complete, so
     // the ring has to cover the split latency plus the MMA latency
     static constexpr int kX8Stages = NX == 16 ? 8 : 4;
@@ -113,6 +115,7 @@ struct Fp8Layout {
     static_assert(kTmemCols == 256, "TMEM allocation");
     static_assert(kFacStages >= kX8Stages + kNA, "factor ring");
     static_assert(kSmemBytes <= 232448, "shared memory");
+    static_assert(kFacOff - kXbOff >= 4 * gemm::scratch_quadrant<NX>(), "reduction scratch in the X slots");
 };
 
 struct Bf16Store {
@@ -121,9 +124,20 @@ struct Bf16Store {
     }
 };
 
+static_assert(gemm::kMaxSegs == kMaxFp8Segs, "segment tables");
+
+// Index of the segment holding `tile` (constant-index selects).
+__device__ __forceinline__ int seg_index(const Params& p, int tile) {
+    int r = 0;
+#pragma unroll
+    for (int j = 1; j < gemm::kMaxSegs; ++j)
+        if (j < p.nseg && tile >= p.seg[j].tile0) r = j;
+    return r;
+}
+
 template <int NX>
 __global__ void __launch_bounds__(Split<NX>::kThreads, 1)
-    fp8_kernel(const __grid_constant__ CUtensorMap tmW, const Params p) {
+    fp8_kernel(const __grid_constant__ Fp8Maps tm, const Params p) {
     using L = Fp8Layout<NX>;
     constexpr int kN = L::kN;
     constexpr int kWStages = L::kWStages;
@@ -184,7 +198,7 @@ __global__ void __launch_bounds__(Split<NX>::kThreads, 1)
     if (warp == 0) {
         // ------------------------------------------------------------ weight producer
         if (lane == 0) {
-            prefetch_tmap(&tmW);
+            for (int j = 0; j < p.nseg; ++j) prefetch_tmap(&tm.m[j]);
             const uint64_t pol_w = policy_evict_first();
             int issued = 0;
             Cursor cur(u0, p.KB);
@@ -192,8 +206,11 @@ __global__ void __launch_bounds__(Split<NX>::kThreads, 1)
                 const int s = i % kWStages;
                 if (i >= kWStages && !wait_bounded(wempty(s), ((i / kWStages) - 1) & 1, wc)) break;
                 if (cta == 0 && i == p.fault_unit) continue;   // failure-path test hook
+                // the unit's segment: its own weight map, rows counted from its first tile
+                const int sj = seg_index(p, cur.tile);
+                const int row0 = (cur.tile - gemm::seg_of(p, cur.tile).tile0) * 128;
                 mbar_arrive_expect_tx(wfull(s), L::kWBytes);
-                tma_load_2d(base + s * L::kWBytes, &tmW, wfull(s), cur.kr * 128, cur.tile * 128, pol_w);
+                tma_load_2d(base + s * L::kWBytes, &tm.m[sj], wfull(s), cur.kr * 128, row0, pol_w);
                 issued = i + 1;
             }
             // Every copy this thread started must land before the CTA can exit.
@@ -214,7 +231,6 @@ __global__ void __launch_bounds__(Split<NX>::kThreads, 1)
         constexpr int CH_IN = kEpt / 8;        // 16-byte BF16 chunks read
         constexpr int CH_OUT = kEpt / 16;      // 16-byte E4M3 chunks written per plane
         constexpr int kGT = 32 * Split<NX>::kWarps;   // threads per group
-        constexpr int kAhead = L::kXAhead;
         constexpr int kG = Split<NX>::kGroups;
         const int g = (warp - kWarpConv0) / Split<NX>::kWarps;
         const int ct = ((warp - kWarpConv0) % Split<NX>::kWarps) * 32 + lane;
@@ -247,7 +263,8 @@ __global__ void __launch_bounds__(Split<NX>::kThreads, 1)
         // the maximum), capped so that 2^e and 2^-e stay normal; and the unit's
         // block scale.
         auto scan = [&](int i, uint4 (&xin)[CH_IN], uint32_t& pw2, int& e, float& sblk) {
-            sblk = __ldg(p.S + static_cast<int64_t>(sq.tile) * p.lds + sq.kr);
+            const gemm::Seg sg = gemm::seg_of(p, sq.tile);
+            sblk = __ldg(sg.S + static_cast<int64_t>(sq.tile - sg.tile0) * p.lds + sq.kr);
             sq.step(kG, p.KB);
             const uint8_t* xs = gbase + xring + ((i / kG) % L::kXbStages) * L::kXbSlot;
 #pragma unroll
@@ -264,32 +281,26 @@ __global__ void __launch_bounds__(Split<NX>::kThreads, 1)
             uint32_t mx = max(m2 & 0xFFFFu, m2 >> 16);
 #pragma unroll
             for (int o = 1; o < kLpr; o <<= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-            e = 134 - static_cast<int>(mx >> 7);
-            e = e > 126 ? 126 : e;
-            const uint32_t pw = static_cast<uint32_t>(e + 127) << 7;   // BF16 2^e
-            pw2 = pw | (pw << 16);
+            e = split_exponent(mx);
+            pw2 = bf16x2_pow2(e);
         };
-#pragma unroll 1
-        for (int j = 0; j < kAhead; ++j) prefetch(g + kG * j);
+        // The group's units i = g, g + kG, ...: unit i is converted from
+        // registers while the copies of units i + kG and i + 2 kG are in flight;
+        // then unit i + kG, copied one iteration earlier, is scanned.
+        prefetch(g);
+        prefetch(g + kG);
         uint4 xc[CH_IN];
         uint32_t pc = 0;
         int ec = 0;
         float scur = 0.0f;
         if (g < nunits) {
-            cp_async_wait<kAhead - 1>();
+            cp_async_wait<1>();
             scan(g, xc, pc, ec, scur);
         }
         for (int i = g; i < nunits; i += kG) {
             const int s8 = i % kX8Stages;
-            // into the slot scanned in the previous iteration
-            prefetch(i + kG * kAhead);
-            // the next unit's scan overlaps this unit's conversion
-            uint4 xn[CH_IN];
-            uint32_t pn = 0;
-            int en = 0;
-            float snext = 0.0f;
-            cp_async_wait<kAhead - 1>();
-            if (i + kG < nunits) scan(i + kG, xn, pn, en, snext);
+            // into the slot unit i was read from
+            prefetch(i + 2 * kG);
             if (i >= kX8Stages && !gemm::warp_wait(x8empty(s8), ((i / kX8Stages) - 1) & 1, wc)) break;
             uint8_t* xo = gbase + L::kX8Off + s8 * L::kX8Slot;
 #pragma unroll
@@ -318,11 +329,10 @@ __global__ void __launch_bounds__(Split<NX>::kThreads, 1)
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(x8full(s8));
-#pragma unroll
-            for (int j = 0; j < CH_IN; ++j) xc[j] = xn[j];
-            pc = pn;
-            ec = en;
-            scur = snext;
+            if (i + kG < nunits) {
+                cp_async_wait<1>();   // all but the newest copy (unit i + 2 kG) have landed
+                scan(i + kG, xc, pc, ec, scur);
+            }
         }
     } else if (warp >= kWarpMma0 && warp < kWarpMma0 + kIssuers) {
         // ------------------------------------------------------------ MMA issuers
@@ -365,6 +375,7 @@ __global__ void __launch_bounds__(Split<NX>::kThreads, 1)
         const int split_info = gemm::split_info_lane(p, u0, u1, lane);
         // Y and the workspace may still be in use by the preceding grid
         grid_dependency_wait();
+        bool deferred = false;   // the first tile's reduction waits for the end of the range
         float outer[NX];
 #pragma unroll
         for (int m = 0; m < NX; ++m) outer[m] = 0.0f;
@@ -407,7 +418,14 @@ __global__ void __launch_bounds__(Split<NX>::kThreads, 1)
             fold16(NX - 16, vh, vl);
 
             if (cur.kb != p.KB - 1 && i != nunits - 1) continue;
-            gemm::end_piece<NX, Bf16Store>(p, outer, cur.tile, cur.kb, u0 + i, u0, first_tile, split_info, q, lane);
+            // after the CTA's last unit the X staging and plane slots are idle:
+            // the reduction may use them
+            const bool last = i == nunits - 1;
+            if (gemm::end_piece<NX, Bf16Store>(p, outer, cur.tile, cur.kb, u0 + i, u0, first_tile, split_info, q,
+                                               lane, last ? gbase + L::kXbOff : nullptr))
+                deferred = true;
+            if (last && deferred)
+                gemm::finish_tile<NX, Bf16Store>(p, first_tile, 0, split_info, q, lane, gbase + L::kXbOff);
 #pragma unroll
             for (int m = 0; m < NX; ++m) outer[m] = 0.0f;
         }
@@ -423,8 +441,7 @@ __global__ void __launch_bounds__(Split<NX>::kThreads, 1)
 }
 
 template <int NX>
-cudaError_t launch_nx(const Params& prm, const Schedule& s, const CUtensorMap& tmW, bool overlap,
-                      cudaStream_t st) {
+cudaError_t launch_nx(const Params& prm, const Schedule& s, const Fp8Maps& maps, bool overlap, cudaStream_t st) {
     using L = Fp8Layout<NX>;
     static int configured_device = -1;
     int dev = 0;
@@ -447,20 +464,30 @@ cudaError_t launch_nx(const Params& prm, const Schedule& s, const CUtensorMap& t
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    return cudaLaunchKernelEx(&cfg, fp8_kernel<NX>, tmW, prm);
+    return cudaLaunchKernelEx(&cfg, fp8_kernel<NX>, maps, prm);
 }
 
 }  // namespace
 
-cudaError_t launch_fp8(const Fp8Args& a, const Schedule& s, const CUtensorMap& tmW, const LaunchCtl& c,
+cudaError_t launch_fp8(const Fp8Args& a, const Schedule& s, const Fp8Maps& maps, const LaunchCtl& c,
                        cudaStream_t st) {
-    gemm::Params p = gemm::base_params(s, a.Y, a.ldy, a.M, a.N, a.K, a.ws, c);
-    p.S = a.S;
+    gemm::Params p = gemm::base_params(s, a.seg[0].Y, a.seg[0].ldy, a.M, s.T * 128, a.K, a.ws, c);
+    p.nseg = a.nseg;
+    int tile0 = 0;
+    for (int j = 0; j < a.nseg; ++j) {
+        p.seg[j].tile0 = tile0;
+        p.seg[j].n = a.seg[j].N;
+        p.seg[j].S = a.seg[j].S;
+        p.seg[j].Y = a.seg[j].Y;
+        p.seg[j].ldy = a.seg[j].ldy;
+        tile0 += (a.seg[j].N + 127) / 128;
+    }
+    p.S = a.seg[0].S;
     p.lds = a.lds;
     p.X = a.X;
     p.ldx = a.ldx;
-    if (s.nmma == 16) return launch_nx<16>(p, s, tmW, c.overlap, st);
-    return launch_nx<32>(p, s, tmW, c.overlap, st);
+    if (s.nmma == 16) return launch_nx<16>(p, s, maps, c.overlap, st);
+    return launch_nx<32>(p, s, maps, c.overlap, st);
 }
 
 }  // namespace qg

@@ -63,6 +63,23 @@ constexpr int kIssuers = 2;
 constexpr int kProdLanes = 4;   // lanes of a producer warp that issue copies
 constexpr unsigned kProdMask = (1u << kProdLanes) - 1u;
 constexpr int kTmemCols = 512;
+// Shared memory per TMEM lane quadrant that the final split-K reduction of a
+// CTA may use (see sum_pieces): five pieces of 32 rows x NOUT FP32 values.
+template <int NOUT>
+__host__ __device__ constexpr int scratch_quadrant() { return 5 * 32 * NOUT * 4; }
+
+// Output segments: up to kMaxSegs weight matrices that share X run as one
+// grid over their concatenated 128-row tiles (e.g. the Q, K and V
+// projections); a plain call is one segment.  Segment j owns tiles
+// [tile0, next segment's tile0) and writes rows [0, n) of its own Y.
+constexpr int kMaxSegs = 4;
+struct Seg {
+    int tile0;         // first tile of the segment in the grid's tile order
+    int n;             // output rows (weight rows) of the segment
+    const float* S;    // FP8: the segment's block scales [ceil(n/128), lds]
+    void* Y;
+    int64_t ldy;
+};
 
 struct Params {
     // weights
@@ -76,9 +93,9 @@ struct Params {
     const void* X;                // activations (FP8 path: read by the split warps)
     int64_t ldx;
     // output and shape
-    void* Y;
-    int64_t ldy;
-    int M, N, K;
+    int nseg;
+    Seg seg[kMaxSegs];
+    int M, N, K;                  // N: rows of all segments' tiles (LUT3: its rows)
     int KB;                       // units (128-wide K blocks) per tile
     long long U;                  // total units
     int G;                        // CTAs
@@ -132,6 +149,7 @@ struct Layout {
     static_assert(kWStages % kG == 0, "a weight stage must belong to one dequant group");
     static_assert(kWStages > kProdLanes && kXStages > kProdLanes, "a stage's previous unit is issued in an earlier pass");
     static_assert(kSmemBytes <= 232448, "shared memory");
+    static_assert(kXStages * kXSlot >= 4 * scratch_quadrant<NMMA>(), "reduction scratch in the X ring");
 };
 
 __device__ __forceinline__ int unit_owner(long long x, long long U, int G) {
@@ -213,14 +231,7 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64
     }
 }
 
-// A CTA ends a split piece only in its first and its last tile.  For both,
-// the first and last contributing CTAs (cf, cl) and the slot holding cf's
-// piece (slot 0 when the tile is cf's first tile, i.e. when cf's range starts
-// exactly at the tile; every later contributor's range starts inside the
-// tile, so their pieces are all in slot 0) are worked out once per CTA,
-// before any unit is ready, so that the 64-bit divisions stay out of the
-// reduction.  Lane 3w + k holds value k (cf, cl, slot) of the first (w = 0) or
-// last (w = 1) tile; the reduction fetches them by shuffle.
+// The (cf, cl, slot) lanes of a CTA's first and last tile (see end_piece).
 __device__ __forceinline__ int split_info_lane(const Params& p, long long u0, long long u1, int lane) {
     int v = 0;
     if (lane < 6) {
@@ -239,29 +250,145 @@ __device__ __forceinline__ int split_info_lane(const Params& p, long long u0, lo
 // workspace, and the last of the tile's CTAs to arrive sums every piece in
 // ascending K order and stores the tile.  Store::store(Y, index, value)
 // writes one output element.
-template <int NOUT, class Store, int kBatch = (NOUT == 16 ? 2 : 1)>
-__device__ __forceinline__ void end_piece(const Params& p, const float (&outer)[NOUT], int tile, int kb,
-                                          long long u, long long u0, int first_tile, int split_info, int q,
-                                          int lane) {
+// The segment holding `tile` (constant-index selects: a dynamic index into
+// the kernel parameters would go through local memory).
+__device__ __forceinline__ Seg seg_of(const Params& p, int tile) {
+    Seg r = p.seg[0];
+#pragma unroll
+    for (int j = 1; j < kMaxSegs; ++j)
+        if (j < p.nseg && tile >= p.seg[j].tile0) r = p.seg[j];
+    return r;
+}
+
+// Rows [m < M] of output row `row` of `tile` (its segment's Y and row index).
+template <int NOUT, class Store>
+__device__ __forceinline__ void store_rows(const Params& p, int tile, int row, const float (&v)[NOUT]) {
+    const Seg sg = seg_of(p, tile);
+    const int n = (tile - sg.tile0) * 128 + row;
+    if (n < sg.n) {
+#pragma unroll
+        for (int m = 0; m < NOUT; ++m)
+            if (m < p.M) Store::store(sg.Y, static_cast<int64_t>(m) * sg.ldy + n, v[m]);
+    }
+}
+
+// Slot of CTA c2's piece of the tile: cf's piece may be in its second slot
+// (w_first), every later contributor's is in its first.
+template <int NOUT>
+__device__ __forceinline__ const float4* piece_slot(const Params& p, int row, int c2, int cf, int w_first) {
+    return reinterpret_cast<const float4*>(p.part) +
+           ((static_cast<size_t>(c2) * 2 + (c2 == cf ? w_first : 0)) * 128 + row) * (NOUT / 4);
+}
+
+// Split-K partial sums live in the workspace as [slot][column group g][row]
+// float4s (g = 4 columns): for each column group the 32 lanes of a TMEM lane
+// quadrant, one output row per lane, touch 512 contiguous bytes.  (Row-major
+// partials made every 16-byte access of a warp hit 32 different L2 lines.)
+template <int NOUT>
+__device__ __forceinline__ float4* slot_base(const Params& p, int cta, int which) {
+    return reinterpret_cast<float4*>(p.part) + (static_cast<size_t>(cta) * 2 + which) * (NOUT / 4) * 128;
+}
+
+// Slot of CTA c2's piece of the tile: cf's piece may be in its second slot
+// (w_first), every later contributor's is in its first.
+template <int NOUT>
+__device__ __forceinline__ const float4* piece_slot(const Params& p, int c2, int cf, int w_first) {
+    return slot_base<NOUT>(p, c2, c2 == cf ? w_first : 0);
+}
+
+// Sum of the pieces [cf, cl] of a split tile for the lane's output row, in
+// ascending piece order, into acc.  The pieces are staged through shared
+// memory that is idle by the end of the CTA's range (scratch_quadrant<NOUT>()
+// bytes per TMEM lane quadrant, laid out [piece][column group][lane] so that
+// a warp's accesses are conflict-free): every lane copies a batch of pieces
+// (up to five) with 16-byte cp.async copies before reading any back, so that
+// a batch costs one L2 round trip.
+template <int NOUT>
+__device__ __forceinline__ void sum_pieces_staged(const Params& p, int row, int lane, int q, int cf, int cl,
+                                                  int w_first, uint8_t* scratch, float (&acc)[NOUT]) {
+    constexpr int kF4 = NOUT / 4;
+    constexpr int kPieces = scratch_quadrant<NOUT>() / (32 * NOUT * 4);
+    const float4* mine = reinterpret_cast<const float4*>(scratch + q * scratch_quadrant<NOUT>()) + lane;
+    const uint32_t sq = smem_u32(mine);
+#pragma unroll
+    for (int m = 0; m < NOUT; ++m) acc[m] = 0.0f;
+    for (int c0 = cf; c0 <= cl; c0 += kPieces) {
+        const int nb = cl - c0 + 1 < kPieces ? cl - c0 + 1 : kPieces;
+#pragma unroll 1
+        for (int b = 0; b < nb; ++b) {
+            const float4* src = piece_slot<NOUT>(p, c0 + b, cf, w_first) + row;
+#pragma unroll
+            for (int g = 0; g < kF4; ++g) cp_async_16(sq + (b * kF4 + g) * 512, src + g * 128, 16u);
+        }
+        cp_async_commit();
+        cp_async_wait<0>();   // the lane reads back only what it copied
+#pragma unroll 1
+        for (int b = 0; b < nb; ++b) {
+#pragma unroll
+            for (int g = 0; g < kF4; ++g) {
+                const float4 x = mine[(b * kF4 + g) * 32];
+                acc[4 * g + 0] = __fadd_rn(acc[4 * g + 0], x.x);
+                acc[4 * g + 1] = __fadd_rn(acc[4 * g + 1], x.y);
+                acc[4 * g + 2] = __fadd_rn(acc[4 * g + 2], x.z);
+                acc[4 * g + 3] = __fadd_rn(acc[4 * g + 3], x.w);
+            }
+        }
+    }
+}
+
+// A CTA ends a split piece only in its first and its last tile.  For both,
+// the first and last contributing CTAs (cf, cl) and the slot holding cf's
+// piece (slot 0 when the tile is cf's first tile, i.e. when cf's range starts
+// exactly at the tile; every later contributor's range starts inside the
+// tile, so their pieces are all in slot 0) are worked out once per CTA,
+// before any unit is ready, so that the 64-bit divisions stay out of the
+// reduction.  Lane 3w + k holds value k (cf, cl, slot) of the first (w = 0) or
+// last (w = 1) tile; the reduction fetches them by shuffle.
+//
+// The last of a tile's CTAs to arrive sums every piece in ascending K order
+// and stores the tile (finish_tile).  The sum is staged through shared memory
+// that is idle only after the CTA's last unit, so a CTA that arrives last at
+// its first tile in the middle of its range defers that reduction to the end
+// of its range (the tile's pieces and counter stay as they are until then).
+
+// Sum and store of split tile `tile` (`which`: 0 = the CTA's first tile, 1 =
+// its last) by its last-arriving CTA; resets the tile's arrival counter.
+template <int NOUT, class Store>
+__device__ __forceinline__ void finish_tile(const Params& p, int tile, int which, int split_info, int q, int lane,
+                                            uint8_t* scratch) {
     const int row = q * 32 + lane;
-    const int n = tile * 128 + row;
+    const int cf = __shfl_sync(0xffffffffu, split_info, 3 * which);
+    const int cl = __shfl_sync(0xffffffffu, split_info, 3 * which + 1);
+    const int w_first = __shfl_sync(0xffffffffu, split_info, 3 * which + 2);
+    float acc[NOUT];
+    sum_pieces_staged<NOUT>(p, row, lane, q, cf, cl, w_first, scratch, acc);
+    store_rows<NOUT, Store>(p, tile, row, acc);
+    __syncwarp();
+    if (lane == 0) p.cnt[tile * 4 + q] = 0u;   // ready for the next call
+}
+
+// End of a CTA's piece of `tile` (one warp, TMEM lane quadrant q, one output
+// row per lane).  A whole tile is stored directly.  A split piece goes to the
+// workspace and counts its arrival; the last to arrive finishes the tile now
+// when `scratch` (shared memory no longer in use) is given, and otherwise
+// returns true: the caller finishes the tile at the end of its range.
+// Store::store(Y, index, value) writes one output element.
+template <int NOUT, class Store>
+__device__ __forceinline__ bool end_piece(const Params& p, const float (&outer)[NOUT], int tile, int kb,
+                                          long long u, long long u0, int first_tile, int split_info, int q,
+                                          int lane, uint8_t* scratch) {
+    const int row = q * 32 + lane;
     const int cta = blockIdx.x;
     const bool whole = (kb == p.KB - 1) && (u - kb >= u0);
     if (whole) {
-        if (n < p.N) {
-#pragma unroll
-            for (int m = 0; m < NOUT; ++m)
-                if (m < p.M) Store::store(p.Y, static_cast<int64_t>(m) * p.ldy + n, outer[m]);
-        }
-        return;
+        store_rows<NOUT, Store>(p, tile, row, outer);
+        return false;
     }
-    // Partial sums are stored row-major per thread ([slot][row][m]) so that a
-    // whole row moves with independent 16-byte accesses.
     const int which = (tile == first_tile) ? 0 : 1;
-    float4* mine = reinterpret_cast<float4*>(p.part) + ((static_cast<size_t>(cta) * 2 + which) * 128 + row) * (NOUT / 4);
+    float4* mine = slot_base<NOUT>(p, cta, which) + row;
 #pragma unroll
-    for (int m4 = 0; m4 < NOUT / 4; ++m4)
-        __stcg(mine + m4, make_float4(outer[4 * m4], outer[4 * m4 + 1], outer[4 * m4 + 2], outer[4 * m4 + 3]));
+    for (int g = 0; g < NOUT / 4; ++g)
+        __stcg(mine + g * 128, make_float4(outer[4 * g], outer[4 * g + 1], outer[4 * g + 2], outer[4 * g + 3]));
     // Every lane's partial must be visible GPU-wide before lane 0's arrival: a
     // sequentially consistent fence per writing lane (an acquire-release fence
     // is not enough, since the lanes that wrote are not the lane that performs
@@ -273,44 +400,12 @@ __device__ __forceinline__ void end_piece(const Params& p, const float (&outer)[
     prev = __shfl_sync(0xffffffffu, prev, 0);
     const int cf = __shfl_sync(0xffffffffu, split_info, 3 * which);
     const int cl = __shfl_sync(0xffffffffu, split_info, 3 * which + 1);
-    const int w_first = __shfl_sync(0xffffffffu, split_info, 3 * which + 2);
-    if (static_cast<int>(prev) != cl - cf) return;
-    // Last piece to arrive: sum all pieces in ascending K order, this CTA's own
-    // piece included (just stored above), loading kBatch pieces at a time so
-    // that their latencies overlap.
+    if (static_cast<int>(prev) != cl - cf) return false;
+    // last piece to arrive: every other piece is visible
     __threadfence();
-    float acc[NOUT];
-#pragma unroll
-    for (int m = 0; m < NOUT; ++m) acc[m] = 0.0f;
-    for (int c0 = cf; c0 <= cl; c0 += kBatch) {
-        float4 piece[kBatch][NOUT / 4];
-#pragma unroll
-        for (int b = 0; b < kBatch; ++b) {
-            const int c2 = c0 + b;
-            if (c2 > cl) break;
-            const float4* slot = reinterpret_cast<const float4*>(p.part) +
-                                 ((static_cast<size_t>(c2) * 2 + (c2 == cf ? w_first : 0)) * 128 + row) * (NOUT / 4);
-#pragma unroll
-            for (int m4 = 0; m4 < NOUT / 4; ++m4) piece[b][m4] = __ldcg(slot + m4);
-        }
-#pragma unroll
-        for (int b = 0; b < kBatch; ++b) {
-            if (c0 + b > cl) break;
-#pragma unroll
-            for (int m4 = 0; m4 < NOUT / 4; ++m4) {
-                acc[4 * m4 + 0] = __fadd_rn(acc[4 * m4 + 0], piece[b][m4].x);
-                acc[4 * m4 + 1] = __fadd_rn(acc[4 * m4 + 1], piece[b][m4].y);
-                acc[4 * m4 + 2] = __fadd_rn(acc[4 * m4 + 2], piece[b][m4].z);
-                acc[4 * m4 + 3] = __fadd_rn(acc[4 * m4 + 3], piece[b][m4].w);
-            }
-        }
-    }
-    if (n < p.N) {
-#pragma unroll
-        for (int m = 0; m < NOUT; ++m)
-            if (m < p.M) Store::store(p.Y, static_cast<int64_t>(m) * p.ldy + n, acc[m]);
-    }
-    if (lane == 0) p.cnt[tile * 4 + q] = 0u;   // ready for the next call
+    if (scratch == nullptr) return true;
+    finish_tile<NOUT, Store>(p, tile, which, split_info, q, lane, scratch);
+    return false;
 }
 
 template <int NMMA, class F>
@@ -537,6 +632,7 @@ __global__ void __launch_bounds__(Roles<NMMA>::kThreads, 1)
         };
         int ps = 0;
         int kb0 = static_cast<int>(u0 % p.KB);
+        bool deferred = false;   // the first tile's reduction waits for the end of the range
         for (int pc = 0; ps < nunits; ++pc) {
             const int tile = first_tile + pc;
             const int b = pc & 1;
@@ -563,7 +659,12 @@ __global__ void __launch_bounds__(Roles<NMMA>::kThreads, 1)
 #pragma unroll
             for (int m = 0; m < NMMA; ++m)
                 outer[m] = two ? __fadd_rn(__uint_as_float(v[m]), __uint_as_float(w[m])) : __uint_as_float(v[m]);
-            end_piece<NMMA, F>(p, outer, tile, kb_end, u0 + pe, u0, first_tile, split_info, q, lane);
+            // after the CTA's last unit the X ring is idle: the reduction may use it
+            const bool last = pe == nunits - 1;
+            if (end_piece<NMMA, F>(p, outer, tile, kb_end, u0 + pe, u0, first_tile, split_info, q, lane,
+                                   last ? gbase + L::kXOff : nullptr))
+                deferred = true;
+            if (last && deferred) finish_tile<NMMA, F>(p, first_tile, 0, split_info, q, lane, gbase + L::kXOff);
             ps = pe + 1;
             kb0 = 0;
         }
@@ -668,8 +769,12 @@ cudaError_t launch(const Params& prm, const Schedule& s, const CUtensorMap& tmW,
 inline Params base_params(const Schedule& s, void* Y, int64_t ldy, int M, int N, int K, void* ws,
                           const LaunchCtl& c) {
     Params p{};
-    p.Y = Y;
-    p.ldy = ldy;
+    p.nseg = 1;
+    p.seg[0].tile0 = 0;
+    p.seg[0].n = N;
+    p.seg[0].S = nullptr;
+    p.seg[0].Y = Y;
+    p.seg[0].ldy = ldy;
     p.M = M;
     p.N = N;
     p.K = K;

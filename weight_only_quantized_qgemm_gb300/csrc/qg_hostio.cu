@@ -16,12 +16,16 @@ constexpr int kStageThreads = 128;
 constexpr int kStagePer = 4;   // 16-byte chunks per thread
 
 // Copy `rows` rows of `row16` 16-byte chunks from src (row stride src_ld16
-// chunks) to dst (row stride dst_ld16).  The loads come before the
-// dependency wait: they read only the caller's host buffer, which no grid on
-// the stream writes, while dst may still be read by the preceding call.
+// chunks) to dst (row stride dst_ld16).  Both the loads and the stores come
+// after the dependency wait: the preceding grid on the stream may write the
+// source (a chained caller passes one call's Y_host as the next call's
+// X_host) and may still read the destination.  The next grid is released at
+// once, so the GEMM behind this kernel starts streaming its weights while X
+// crosses the host link.
 __global__ void __launch_bounds__(kStageThreads) stage_rows_kernel(const uint4* src, int64_t src_ld16, uint4* dst,
                                                                    int64_t dst_ld16, int rows, int64_t row16) {
     grid_dependents_launch();
+    grid_dependency_wait();
     const int64_t total = static_cast<int64_t>(rows) * row16;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kStageThreads;
     const int64_t i0 = static_cast<int64_t>(blockIdx.x) * kStageThreads + threadIdx.x;
@@ -34,7 +38,6 @@ __global__ void __launch_bounds__(kStageThreads) stage_rows_kernel(const uint4* 
             v[j] = src[r * src_ld16 + (i - r * row16)];
         }
     }
-    grid_dependency_wait();
 #pragma unroll
     for (int j = 0; j < kStagePer; ++j) {
         const int64_t i = i0 + j * stride;
@@ -63,27 +66,22 @@ const void* device_view(const void* p) {
 extern "C" qg_status qgemm_fp8_block_host(const void* X_host, int64_t ldx, const uint8_t* W, const float* W_scale,
                                           void* Y_host, int64_t ldy, int M, int N, int K, void* X_stage,
                                           void* workspace, size_t workspace_bytes, cudaStream_t stream) {
-    if (M < 0 || N < 0 || K < 0) return QG_ERR_INVALID_ARG;
-    if (M == 0 || N == 0) return QG_OK;
-    if (!X_host || !W || !W_scale || !Y_host || !X_stage) return QG_ERR_INVALID_ARG;
-    if (M > 32 || K % 16 != 0) return QG_ERR_UNSUPPORTED_SHAPE;
-    if (ldx < K || ldy < N) return QG_ERR_INVALID_ARG;
-    if ((reinterpret_cast<uintptr_t>(X_host) & 15u) != 0 || (ldx % 8) != 0 ||
-        (reinterpret_cast<uintptr_t>(X_stage) & 15u) != 0)
-        return QG_ERR_MISALIGNED;
+    // the GEMM's own checks, with the host buffers standing for X and Y
+    qg_status v = qg::check_fp8_args(X_host, ldx, W, W_scale, Y_host, ldy, M, N, K);
+    if (v != QG_OK || M == 0 || N == 0) return v;
+    if (!X_stage) return QG_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(X_stage) & 15u) != 0) return QG_ERR_MISALIGNED;
     const void* Xd = qg::device_view(X_host);
     void* Yd = const_cast<void*>(qg::device_view(Y_host));
     if (!Xd || !Yd) return QG_ERR_INVALID_ARG;
-    if ((reinterpret_cast<uintptr_t>(Xd) & 15u) != 0) return QG_ERR_MISALIGNED;
-    // Validate the GEMM's own arguments (with X_stage as X) before the
-    // staging kernel is enqueued, so that a refused call enqueues nothing.
+    if ((reinterpret_cast<uintptr_t>(Xd) & 15u) != 0 || (reinterpret_cast<uintptr_t>(Yd) & 1u) != 0)
+        return QG_ERR_MISALIGNED;
+    // Validate the workspace too before the staging kernel is enqueued, so
+    // that a refused call enqueues nothing.
     if (K > 0) {
         const size_t need = qg_workspace_bytes(QG_KIND_FP8_BLOCK, M, N, K);
         if (need > 0 && (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u)))
             return QG_ERR_WORKSPACE;
-        if (!qg::aligned_16(W) || (reinterpret_cast<uintptr_t>(W_scale) & 3u) != 0 ||
-            (reinterpret_cast<uintptr_t>(Yd) & 1u) != 0)
-            return QG_ERR_MISALIGNED;
         const int64_t row16 = static_cast<int64_t>(K) / 8;
         const int64_t total = static_cast<int64_t>(M) * row16;
         const int64_t per_cta = static_cast<int64_t>(qg::kStageThreads) * qg::kStagePer;

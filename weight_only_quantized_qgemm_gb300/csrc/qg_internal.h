@@ -7,6 +7,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "../../include/qgemm.h"
+
 namespace qg {
 
 // Work decomposition shared by both GEMM kernels.  The output is cut into
@@ -35,16 +37,30 @@ size_t workspace_bytes(const Schedule& s);           // 0 when no tile is split
 // workspace), for callers that must clear them.
 void workspace_counters(int kind, int M, int N, int K, size_t* offset, size_t* bytes);
 
+// One FP8 weight matrix of a call and its output (a call holds 1 to
+// kMaxFp8Segs of them sharing X; see qgemm_fp8_block_multi).
+constexpr int kMaxFp8Segs = 4;
+struct Fp8Seg {
+    const uint8_t* W;
+    const float* S;
+    void* Y;
+    int64_t ldy;
+    int N;
+};
+
 struct Fp8Args {
     const void* X;
     int64_t ldx;
-    const uint8_t* W;
-    const float* S;
-    int64_t lds;
-    void* Y;
-    int64_t ldy;
-    int M, N, K;
+    int nseg;
+    Fp8Seg seg[kMaxFp8Segs];
+    int64_t lds;      // ceil(K/128): the row pitch of every segment's scales
+    int M, K;
     void* ws;
+};
+
+// The weight tensor map of each segment (128 x 128 E4M3 boxes).
+struct Fp8Maps {
+    CUtensorMap m[kMaxFp8Segs];
 };
 
 struct Lut3Args {
@@ -68,14 +84,14 @@ struct LaunchCtl {
     bool overlap;        // launch with programmatic stream serialization
 };
 
-cudaError_t launch_fp8(const Fp8Args& a, const Schedule& s, const CUtensorMap& tmW, const LaunchCtl& c,
+cudaError_t launch_fp8(const Fp8Args& a, const Schedule& s, const Fp8Maps& maps, const LaunchCtl& c,
                        cudaStream_t st);
 // tmS: the scale-matrix tensor map ([N, K/128] FP16, boxes of 128 rows x 8
 // groups), or null to have the kernel load scales from global memory.
 cudaError_t launch_lut3(const Lut3Args& a, const Schedule& s, const CUtensorMap& tmX, const CUtensorMap* tmS,
                         const LaunchCtl& c, cudaStream_t st);
 
-cudaError_t launch_dequant_e4m3(const uint8_t* codes, void* out, int64_t n, cudaStream_t st);
+cudaError_t launch_split_probe(const void* X, int64_t blocks, void* hi, void* lo, int* exponent, cudaStream_t st);
 cudaError_t launch_dequant_lut3(const void* Wq, const void* qmap, const void* scales, void* D,
                                 int N, int K, cudaStream_t st);
 cudaError_t launch_zero_rows(void* Y, int64_t ldy, int M, int N, cudaStream_t st);
@@ -87,5 +103,15 @@ uint32_t* device_status_ptr();
 bool overlap_enabled();
 
 inline bool aligned_16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Argument checks shared by the FP8 entry points (qgemm_fp8_block, the host
+// and no-alloc variants): QG_OK or the status qgemm_fp8_block returns.
+qg_status check_fp8_args(const void* X, int64_t ldx, const void* W, const void* W_scale, const void* Y, int64_t ldy,
+                         int M, int N, int K);
+
+// Zero the arrival counters of the no-alloc entry point's scratch array on
+// the current device (if that entry point has used it there), on `st`, and
+// wait for it.  Called after a timeout is reported.
+cudaError_t noalloc_clear_counters(cudaStream_t st);
 
 }  // namespace qg
