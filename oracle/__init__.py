@@ -38,6 +38,7 @@ __all__ = [
     "qgemm_fp8_block_sample", "fp8_abs_mass", "lut3_dequant", "lut3_dequant_matrix",
     "qgemm_lut3", "qgemm_lut3_sample", "lut3_abs_mass", "pack_lut3", "unpack_lut3",
     "lut3_packed_bytes", "bf16_ord", "fp16_ord", "within_budget", "BudgetReport",
+    "gemm_bf16", "gemm_bf16_sample", "bf16_abs_mass",
     "max_threads",
 ]
 
@@ -84,6 +85,9 @@ _SIGS = {
     "oracle_qgemm_fp8_block": (None, [_I, _I, _I, _P, _L, _P, _L, _P, _L, _P, _P, _L, _I]),
     "oracle_qgemm_fp8_block_sample": (None, [_I, _I, _I, _P, _L, _P, _L, _P, _L, _P, _P, _L, _P, _P, _I]),
     "oracle_fp8_abs_mass": (None, [_I, _I, _I, _P, _L, _P, _L, _P, _L, _P, _P, _L, _P, _I]),
+    "oracle_gemm_bf16": (None, [_I, _I, _I, _P, _L, _P, _L, _P, _P, _L, _I]),
+    "oracle_gemm_bf16_sample": (None, [_I, _I, _I, _P, _L, _P, _L, _P, _P, _L, _P, _P, _I]),
+    "oracle_bf16_abs_mass": (None, [_I, _I, _I, _P, _L, _P, _L, _P, _P, _L, _P, _I]),
     "oracle_lut3_dequant": (ctypes.c_uint16, [ctypes.c_uint8, _P, ctypes.c_uint16]),
     "oracle_lut3_dequant_matrix": (None, [_I, _I, _P, _L, _P, _P, _L, _P, _L]),
     "oracle_qgemm_lut3": (None, [_I, _I, _I, _P, _L, _P, _L, _P, _P, _L, _P, _P, _L, _I]),
@@ -153,6 +157,46 @@ def float_to_fp16(x) -> np.ndarray:
     out = np.empty(v.size, dtype=np.uint16)
     lib().oracle_float_to_fp16_array(v.size, _ptr(v), _ptr(out))
     return out.reshape(np.shape(x))
+
+
+# ---------------------------------------------------------------- dense BF16 GEMM
+def gemm_bf16(X, W, nthreads: int = 0, want_f32: bool = False):
+    """Y = bf16(X[M,K] . W[N,K]^T), FP32 sums in strict K order (BF16 bits in
+    and out)."""
+    X = _c(X, np.uint16); W = _c(W, np.uint16)
+    M, K = X.shape
+    N = W.shape[0]
+    assert W.shape[1] == K
+    Y = np.empty((M, N), dtype=np.uint16)
+    Yf = np.empty((M, N), dtype=np.float32) if want_f32 else None
+    lib().oracle_gemm_bf16(M, N, K, _ptr(X), K, _ptr(W), K, _ptr(Y), _ptr(Yf), N, nthreads)
+    return (Y, Yf) if want_f32 else Y
+
+
+def gemm_bf16_sample(X, W, ms, ns, nthreads: int = 0, want_f32: bool = False):
+    X = _c(X, np.uint16); W = _c(W, np.uint16)
+    M, K = X.shape
+    N = W.shape[0]
+    ms = _c(ms, np.int32); ns = _c(ns, np.int32)
+    Y = np.empty(ms.size, dtype=np.uint16)
+    Yf = np.empty(ms.size, dtype=np.float32) if want_f32 else None
+    lib().oracle_gemm_bf16_sample(M, N, K, _ptr(X), K, _ptr(W), K, _ptr(ms), _ptr(ns), ms.size, _ptr(Y),
+                                  _ptr(Yf), nthreads)
+    return (Y, Yf) if want_f32 else Y
+
+
+def bf16_abs_mass(X, W, ms=None, ns=None, nthreads: int = 0) -> np.ndarray:
+    X = _c(X, np.uint16); W = _c(W, np.uint16)
+    M, K = X.shape
+    N = W.shape[0]
+    if ms is None:
+        A = np.empty((M, N), dtype=np.float64)
+        lib().oracle_bf16_abs_mass(M, N, K, _ptr(X), K, _ptr(W), K, None, None, 0, _ptr(A), nthreads)
+        return A
+    ms = _c(ms, np.int32); ns = _c(ns, np.int32)
+    A = np.empty(ms.size, dtype=np.float64)
+    lib().oracle_bf16_abs_mass(M, N, K, _ptr(X), K, _ptr(W), K, _ptr(ms), _ptr(ns), ms.size, _ptr(A), nthreads)
+    return A
 
 
 # ---------------------------------------------------------------- FP8 GEMM

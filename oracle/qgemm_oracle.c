@@ -20,6 +20,10 @@
  *    fp16_rne(qmap[code] * scale[n, k/128]) before accumulation, the products
  *    with the FP16 activations are summed in FP32 in strict K order, and the
  *    sum is rounded to FP16.
+ *  - The unquantised BF16 decode GEMM named beside the FP8 tier on the
+ *    "atlas" m16_tc page (the numerics contract section: the BF16 lm_head
+ *    tier graded by the same comparison): BF16 X and W, products summed in
+ *    FP32 in strict K order, the sum rounded to BF16.
  *  - The tiled nibble packing of 3-bit codes (the layout documented in
  *    include/qgemm.h), written independently from that document.
  *
@@ -314,6 +318,84 @@ void oracle_fp8_abs_mass(int M, int N, int K,
                             (double)oracle_e4m3_to_float(W[(int64_t)n * ldw + k]));
             acc += fabs((double)S[(int64_t)(n / 128) * lds + kb]) * blk;
         }
+        A[i] = acc;
+    }
+}
+
+/* ------------------------------------------------------------------ */
+/* Dense BF16 GEMM                                                      */
+/* ------------------------------------------------------------------ */
+
+/* sum_k x[k] * w[k] in FP32, strictly ascending k (each product is exact). */
+static float bf16_element(int K, const uint16_t *xrow, const uint16_t *wrow)
+{
+    int k;
+    float acc = 0.0f;
+    for (k = 0; k < K; ++k) {
+        float prod = oracle_bf16_to_float(xrow[k]) * oracle_bf16_to_float(wrow[k]);
+        acc = acc + prod;
+    }
+    return acc;
+}
+
+/* Y = bf16_rne(X[M,K] . W[N,K]^T); Yf (optional) the FP32 sums. */
+void oracle_gemm_bf16(int M, int N, int K,
+                      const uint16_t *X, int64_t ldx,
+                      const uint16_t *W, int64_t ldw,
+                      uint16_t *Y, float *Yf, int64_t ldy, int nthreads)
+{
+    int n;
+    set_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 16)
+    for (n = 0; n < N; ++n) {
+        int m;
+        for (m = 0; m < M; ++m) {
+            float v = bf16_element(K, X + (int64_t)m * ldx, W + (int64_t)n * ldw);
+            if (Y)
+                Y[(int64_t)m * ldy + n] = oracle_float_to_bf16_rne(v);
+            if (Yf)
+                Yf[(int64_t)m * ldy + n] = v;
+        }
+    }
+}
+
+void oracle_gemm_bf16_sample(int M, int N, int K,
+                             const uint16_t *X, int64_t ldx,
+                             const uint16_t *W, int64_t ldw,
+                             const int32_t *ms, const int32_t *ns, int64_t count,
+                             uint16_t *Y, float *Yf, int nthreads)
+{
+    int64_t i;
+    (void)M; (void)N;
+    set_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 64)
+    for (i = 0; i < count; ++i) {
+        float v = bf16_element(K, X + (int64_t)ms[i] * ldx, W + (int64_t)ns[i] * ldw);
+        if (Y)
+            Y[i] = oracle_float_to_bf16_rne(v);
+        if (Yf)
+            Yf[i] = v;
+    }
+}
+
+/* A[m, n] = sum_k |x[m,k] * w[n,k]| in double (full array or listed elements). */
+void oracle_bf16_abs_mass(int M, int N, int K,
+                          const uint16_t *X, int64_t ldx,
+                          const uint16_t *W, int64_t ldw,
+                          const int32_t *ms, const int32_t *ns, int64_t count,
+                          double *A, int nthreads)
+{
+    int64_t i, total = ms ? count : (int64_t)M * N;
+    set_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 64)
+    for (i = 0; i < total; ++i) {
+        int m = ms ? ms[i] : (int)(i / N);
+        int n = ms ? ns[i] : (int)(i % N);
+        int k;
+        double acc = 0.0;
+        for (k = 0; k < K; ++k)
+            acc += fabs((double)oracle_bf16_to_float(X[(int64_t)m * ldx + k]) *
+                        (double)oracle_bf16_to_float(W[(int64_t)n * ldw + k]));
         A[i] = acc;
     }
 }

@@ -464,3 +464,63 @@ def test_page_grid_counts():
     for n, ctas in g["ctas"].items():
         assert int(n) // g["n_tile"] == ctas
     assert g["sms"] * g["ctas_per_sm"] == g["resident"]
+
+
+# ------------------------------------------------------------------ dense BF16 GEMM
+def _bf16_decode(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).double().numpy()
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 128, 128), (3, 200, 512), (2, 130, 1000), (4, 64, 8)])
+def test_bf16_oracle_vs_fp64_brute_force(M, N, K):
+    """Within the FP32 recursive-summation bound of the FP64 product, and the
+    BF16 output is the rounding of the FP32 sum."""
+    p = wl.make_bf16_problem(M, N, K, config_id=11)
+    Yb, Yf = oracle.gemm_bf16(p.X, p.W, want_f32=True)
+    x, w = _bf16_decode(p.X), _bf16_decode(p.W)
+    Y64 = x @ w.T
+    A = np.abs(x) @ np.abs(w).T
+    err = np.abs(Yf.astype(np.float64) - Y64)
+    assert np.all(err <= (K + 4) * U * A * 1.01), err.max()
+    assert np.array_equal(Yb, torch.from_numpy(Yf).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16))
+    assert np.allclose(oracle.bf16_abs_mass(p.X, p.W), A, rtol=1e-12, atol=0)
+
+
+def test_bf16_oracle_small_integers_are_exact():
+    """Small integer operands: every partial sum is an exact FP32 integer, so
+    the sum is the integer matmul and only the final BF16 rounding remains."""
+    rng = np.random.default_rng(12)
+    M, N, K = 3, 40, 1024
+    xi = rng.integers(-8, 9, size=(M, K))
+    wi = rng.integers(-8, 9, size=(N, K))
+    X = wl.bf16_bits_from_f32(xi.astype(np.float32))
+    W = wl.bf16_bits_from_f32(wi.astype(np.float32))
+    Yb, Yf = oracle.gemm_bf16(X, W, want_f32=True)
+    exact = xi @ wi.T
+    assert np.array_equal(Yf.astype(np.int64), exact)
+    assert np.array_equal(Yb, wl.bf16_bits_from_f32(exact.astype(np.float32)))
+
+
+def test_bf16_oracle_sums_in_strict_k_order():
+    """x = [2^24, 1, -2^24], w = [1, 1, 1]: in strict K order 2^24 + 1 rounds to
+    2^24 (tie to even) and the sum is 0; any order that adds the 1 last gives 1."""
+    X = wl.bf16_bits_from_f32(np.array([[2.0 ** 24, 1.0, -(2.0 ** 24)]], dtype=np.float32))
+    W = wl.bf16_bits_from_f32(np.ones((1, 3), dtype=np.float32))
+    _, Yf = oracle.gemm_bf16(X, W, want_f32=True)
+    assert Yf[0, 0] == 0.0
+    X2 = wl.bf16_bits_from_f32(np.array([[2.0 ** 24, -(2.0 ** 24), 1.0]], dtype=np.float32))
+    _, Yf2 = oracle.gemm_bf16(X2, W, want_f32=True)
+    assert Yf2[0, 0] == 1.0
+
+
+def test_bf16_oracle_rows_independent_and_sampled():
+    p = wl.make_bf16_problem(5, 300, 640, config_id=13)
+    Y = oracle.gemm_bf16(p.X, p.W)
+    for m in range(5):
+        assert np.array_equal(oracle.gemm_bf16(p.X[m:m + 1], p.W)[0], Y[m])
+    rng = np.random.default_rng(3)
+    ms = rng.integers(0, 5, 200).astype(np.int32)
+    ns = rng.integers(0, 300, 200).astype(np.int32)
+    assert np.array_equal(oracle.gemm_bf16_sample(p.X, p.W, ms, ns), Y[ms, ns])
+    assert np.allclose(oracle.bf16_abs_mass(p.X, p.W, ms, ns), oracle.bf16_abs_mass(p.X, p.W)[ms, ns], rtol=0,
+                       atol=0)

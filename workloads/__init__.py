@@ -13,6 +13,8 @@ Workloads (the five configurations of the weight-only decode GEMM study):
 * ``fp8_attn``   -- small-N attention shapes N in {1024, 5120, 6144},
   K=5120, M in {1,2,4,5,8,16,17,24,32}.
 * ``lut3``       -- 3-bit learned-LUT, N=28672, K=8192, M in {1,4,8,16}.
+* ``bf16_lm_head`` -- unquantised BF16 decode GEMM of an output-projection
+  (lm_head) shape, N=32768, K=5120, M in {1,16,32}.
 
 Input recipe (identical for every consumer):
 
@@ -25,6 +27,7 @@ Input recipe (identical for every consumer):
   [-448, 448], i.e. saturating to the largest finite value.
 * Activations: X ~ N(0, 1), rounded to BF16 (FP8 path) or FP16 (LUT path)
   with round-to-nearest-even.
+* BF16 weights (dense path): W ~ N(0, 0.02) rounded to BF16.
 * LUT3: codes uniform on 0..7; the 8-entry FP16 map is the standard-normal
   quantiles at (i + 0.5) / 8, sorted ascending; per-(row, 128-K group)
   scales ~ U[0.005, 0.02] rounded to FP16.
@@ -43,7 +46,7 @@ import numpy as np
 
 __all__ = [
     "SEED_BASE", "seed_for", "uniform01", "normal", "uniform_codes", "bf16_bits_from_f32",
-    "fp16_bits_from_f32", "e4m3_codes_from_f32", "Fp8Problem", "Lut3Problem",
+    "fp16_bits_from_f32", "e4m3_codes_from_f32", "Fp8Problem", "Lut3Problem", "Bf16Problem", "make_bf16_problem",
     "make_fp8_problem", "make_lut3_problem", "lut3_qmap_bits", "WORKLOADS",
 ]
 
@@ -170,6 +173,22 @@ def make_fp8_problem(M: int, N: int, K: int, config_id: int = 0, keep_float: boo
     return Fp8Problem(M, N, K, X, codes, S, w if keep_float else None)
 
 
+@dataclass
+class Bf16Problem:
+    M: int
+    N: int
+    K: int
+    X: np.ndarray        # uint16 [M, K]  BF16 bits
+    W: np.ndarray        # uint16 [N, K]  BF16 bits
+
+
+def make_bf16_problem(M: int, N: int, K: int, config_id: int = 5, x_seed_tensor: int = 0,
+                      w_seed_tensor: int = 1) -> Bf16Problem:
+    w = (normal(seed_for(config_id, w_seed_tensor), N * K) * np.float32(0.02)).reshape(N, K)
+    x = normal(seed_for(config_id, x_seed_tensor), M * K).reshape(M, K)
+    return Bf16Problem(M, N, K, bf16_bits_from_f32(x).reshape(M, K), bf16_bits_from_f32(w).reshape(N, K))
+
+
 def lut3_qmap_bits() -> np.ndarray:
     """FP16 bits of the standard-normal quantiles at (i + 0.5)/8, i = 0..7."""
     nd = statistics.NormalDist()
@@ -198,4 +217,5 @@ WORKLOADS = {
     "fp8_attn_5120": ("fp8", 3, 5120, 5120, [1, 2, 4, 5, 8, 16, 17, 24, 32]),
     "fp8_attn_6144": ("fp8", 3, 6144, 5120, [1, 2, 4, 5, 8, 16, 17, 24, 32]),
     "lut3": ("lut3", 4, 28672, 8192, [1, 4, 8, 16]),
+    "bf16_lm_head": ("bf16", 5, 32768, 5120, [1, 16, 32]),
 }
