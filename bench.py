@@ -225,6 +225,12 @@ class Fp8Case:
                 raise RuntimeError(qg.status_string(r))
         return step
 
+    def tune(self, M, stream):
+        """The exactness-gated dispatch tuner on this shape (its grid stays in
+        the process's dispatch table); returns the grid chosen."""
+        g, _ = self.qg.tune_fp8(self.X[:M], self.W, self.S, calls=100, workspace=self.ws, stream=stream)
+        return g
+
     def time(self, M, stream, steps, warmup):
         ms = time_calls(self.torch, stream, self.stepper(M, stream), steps, warmup)
         st = self.qg.last_device_status(stream)
@@ -252,6 +258,11 @@ class Lut3Case:
         self.X = torch.from_numpy(p.X.view(np.int16)).view(torch.float16).cuda()
         self.Y = torch.empty((M_max, N), dtype=torch.float16, device="cuda")
         self.ws = qg.Workspace()
+
+    def tune(self, M, stream):
+        g, _ = self.qg.tune_lut3(self.X[:M], self.Wq, self.qm, self.sc, self.N, calls=50, workspace=self.ws,
+                                 stream=stream)
+        return g
 
     def time(self, M, stream, steps, warmup):
         qg, N, K = self.qg, self.N, self.K
@@ -338,6 +349,47 @@ def time_halves(torch, qg, stream, case, steps, warmup):
     return ms
 
 
+def bf16_bytes(M, N, K):
+    return N * K * 2 + M * K * 2 + M * N * 2
+
+
+class Bf16Case:
+    """Unquantised BF16 output-projection (lm_head) shape, weights rotated
+    over copies (>= 2x L2)."""
+
+    def __init__(self, torch, qg, M_max, N, K):
+        import workloads as wl
+        self.torch, self.qg, self.N, self.K = torch, qg, N, K
+        p = wl.make_bf16_problem(M_max, N, K, config_id=5)
+        self.copies = -(-2 * L2_BYTES // (N * K * 2)) + 1
+        self.W = [torch.from_numpy(p.W.view(np.int16)).view(torch.bfloat16).cuda() for _ in range(self.copies)]
+        self.X = torch.from_numpy(p.X.view(np.int16)).view(torch.bfloat16).cuda()
+        self.Y = torch.empty((M_max, N), dtype=torch.bfloat16, device="cuda")
+        self.ws = qg.Workspace()
+
+    def time(self, M, stream, steps, warmup):
+        qg, N, K = self.qg, self.N, self.K
+        buf = self.ws.get(qg.workspace_bytes(qg.KIND_BF16, M, N, K))
+        ws_ptr = buf.data_ptr() if buf is not None else None
+        ws_n = buf.numel() if buf is not None else 0
+        lib, sptr, copies = qg.lib, stream.cuda_stream, self.copies
+        xp, yp = self.X.data_ptr(), self.Y.data_ptr()
+        wps = [w.data_ptr() for w in self.W]
+
+        def step(i):
+            r = lib.qgemm_bf16(xp, K, wps[i % copies], yp, N, M, N, K, ws_ptr, ws_n, sptr)
+            if r:
+                raise RuntimeError(qg.status_string(r))
+        ms = time_calls(self.torch, stream, step, steps, warmup)
+        st = qg.last_device_status(stream)
+        if st:
+            raise RuntimeError(f"device status {qg.status_string(st)}")
+        return ms
+
+    def free(self):
+        self.W = self.X = self.Y = self.ws = None
+
+
 class QkvCase:
     """The attention projections Q (N=6144), K and V (N=1024 each) at
     K=5120 sharing X, weights rotated over copies (>= 2x L2)."""
@@ -383,22 +435,31 @@ class QkvCase:
         self.sets = self.X = self.Y = self.ws = None
 
 
-def secondary_lines(torch, qg, stream, peak, steps=2000, warmup=50):
+def secondary_lines(torch, qg, stream, peak, steps=2000, warmup=50, tune=True):
     """The other configurations (not the headline): us/call, GB/s, fraction
-    of the HBM peak."""
+    of the HBM peak.  With `tune`, each shape first runs the library's
+    exactness-gated dispatch tuner (outside the timed calls) and its line
+    records the grid chosen."""
     out = {}
 
-    def rec(name, ms, nbytes):
+    def rec(name, ms, nbytes, grid=None):
         gbs = nbytes / (ms * 1e-3) / 1e9
         out[name] = {"us": round(ms * 1e3, 3), "GBps": round(gbs, 1), "frac": round(gbs / peak, 4)}
+        if grid is not None:
+            out[name]["grid"] = grid
+
+    def tuned(c, m):
+        return c.tune(m, stream) if tune else None
 
     c = Fp8Case(torch, qg, 16, 17408, 5120, 1)
     for m in (1, 8):
-        rec(f"fp8_gateup_M{m}", c.time(m, stream, steps, warmup), fp8_bytes(m, 17408, 5120))
+        g = tuned(c, m)
+        rec(f"fp8_gateup_M{m}", c.time(m, stream, steps, warmup), fp8_bytes(m, 17408, 5120), g)
     c.free()
     c = Fp8Case(torch, qg, 32, 5120, 17408, 2)
     for m in (1, 16, 32):
-        rec(f"fp8_down_M{m}", c.time(m, stream, steps, warmup), fp8_bytes(m, 5120, 17408))
+        g = tuned(c, m)
+        rec(f"fp8_down_M{m}", c.time(m, stream, steps, warmup), fp8_bytes(m, 5120, 17408), g)
     # the same 32 rows as two 16-row calls (the weights stream twice; the
     # fraction is taken against the one-call algorithmic bytes)
     rec("fp8_down_M32_halves", time_halves(torch, qg, stream, c, steps, warmup), fp8_bytes(32, 5120, 17408))
@@ -406,10 +467,16 @@ def secondary_lines(torch, qg, stream, peak, steps=2000, warmup=50):
     for n in (1024, 5120, 6144):
         c = Fp8Case(torch, qg, 32, n, 5120, 3)
         for m in (1, 2, 4, 5, 8, 16, 17, 24, 32):
-            rec(f"fp8_attn_N{n}_M{m}", c.time(m, stream, steps, warmup), fp8_bytes(m, n, 5120))
+            g = tuned(c, m)
+            rec(f"fp8_attn_N{n}_M{m}", c.time(m, stream, steps, warmup), fp8_bytes(m, n, 5120), g)
         c.free()
     c = Fp8Case(torch, qg, 1, 256, 512, 0)
     rec("fp8_small_M1", c.time(1, stream, steps, warmup), fp8_bytes(1, 256, 512))
+    c.free()
+    # unquantised BF16 output projection (lm_head shape)
+    c = Bf16Case(torch, qg, 32, 32768, 5120)
+    for m in (1, 16, 32):
+        rec(f"bf16_lm_head_M{m}", c.time(m, stream, steps // 4, warmup), bf16_bytes(m, 32768, 5120))
     c.free()
     # Q, K and V in one launch against the three calls one after another
     c = QkvCase(torch, qg, 32)
@@ -419,8 +486,10 @@ def secondary_lines(torch, qg, stream, peak, steps=2000, warmup=50):
     c.free()
     c = Lut3Case(torch, qg, 16, 28672, 8192)
     for m in (1, 4, 8, 16):
-        rec(f"lut3_M{m}", c.time(m, stream, steps, warmup), lut3_bytes(m, 28672, 8192))
+        g = tuned(c, m)
+        rec(f"lut3_M{m}", c.time(m, stream, steps, warmup), lut3_bytes(m, 28672, 8192), g)
     c.free()
+    qg.dispatch_clear()
     torch.cuda.empty_cache()
     return out
 
@@ -509,9 +578,10 @@ def main():
     ap.add_argument("--quick", action="store_true", help="headline only, no secondary configs or CPU baseline")
     ap.add_argument("--overlap", type=int, choices=[0, 1], default=1,
                     help="launch with weight-prefetch overlap of consecutive calls (default 1)")
-    ap.add_argument("--only", choices=["lut3", "fp8_down_m32"], default=None,
+    ap.add_argument("--only", choices=["lut3", "fp8_down_m32", "bf16", "fp8_attn_n5120_m16"], default=None,
                     help="time one secondary workload alone and print its line, for profiling its kernel: "
-                         "lut3 = 3-bit LUT, M=16, N=28672, K=8192; fp8_down_m32 = FP8 M=32, N=5120, K=17408")
+                         "lut3 = 3-bit LUT, M=16, N=28672, K=8192; fp8_down_m32 = FP8 M=32, N=5120, K=17408; "
+                         "bf16 = dense BF16, M=16, N=32768, K=5120; fp8_attn_n5120_m16 = FP8 M=16, N=5120, K=5120")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -539,6 +609,14 @@ def main():
             c = Lut3Case(torch, qg, 16, 28672, 8192)
             ms = c.time(16, stream, args.steps, args.warmup)
             nbytes, name = lut3_bytes(16, 28672, 8192), "lut3 M=16 N=28672 K=8192"
+        elif args.only == "bf16":
+            c = Bf16Case(torch, qg, 16, 32768, 5120)
+            ms = c.time(16, stream, args.steps, args.warmup)
+            nbytes, name = bf16_bytes(16, 32768, 5120), "bf16 M=16 N=32768 K=5120"
+        elif args.only == "fp8_attn_n5120_m16":
+            c = Fp8Case(torch, qg, 16, 5120, 5120, 3)
+            ms = c.time(16, stream, args.steps, args.warmup)
+            nbytes, name = fp8_bytes(16, 5120, 5120), "fp8_block M=16 N=5120 K=5120"
         else:
             c = Fp8Case(torch, qg, 32, 5120, 17408, 2)
             ms = c.time(32, stream, args.steps, args.warmup)

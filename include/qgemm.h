@@ -23,6 +23,10 @@
  *     (row, 128-wide K group) dequantise a code as fp16_rne(qmap[c] * scale);
  *     X and Y are FP16, the sum is FP32.
  *
+ *  3. Unquantised BF16 (the BF16 lm_head tier graded by the same numerics
+ *     contract on the "atlas" m16_tc page): W, X and Y are BF16, the sum is
+ *     FP32, Y is its BF16 round-to-nearest-even.
+ *
  * Conventions shared by all GEMM entry points
  *  - All matrix pointers are device pointers; the caller owns every buffer.
  *    The library allocates nothing per call.
@@ -56,14 +60,14 @@ struct CUstream_st; /* the same type as cudaStream_t */
 typedef enum {
     QG_OK = 0,
     QG_ERR_INVALID_ARG = 1,       /* null pointer, negative size, ld < row length */
-    QG_ERR_UNSUPPORTED_SHAPE = 2, /* M > 32, K % 16 (FP8) or K % 128 (LUT3) != 0 */
+    QG_ERR_UNSUPPORTED_SHAPE = 2, /* M > 32, K % 16 (FP8), K % 128 (LUT3) or K % 8 (BF16) != 0 */
     QG_ERR_MISALIGNED = 3,        /* a pointer or row stride breaks the 16-byte rule */
     QG_ERR_CUDA = 4,              /* a CUDA runtime call or kernel launch failed */
     QG_ERR_TIMEOUT = 5,           /* a bounded in-kernel wait ran out */
     QG_ERR_WORKSPACE = 6          /* workspace missing or smaller than qg_workspace_bytes */
 } qg_status;
 
-enum { QG_KIND_FP8_BLOCK = 0, QG_KIND_LUT3 = 1 };
+enum { QG_KIND_FP8_BLOCK = 0, QG_KIND_LUT3 = 1, QG_KIND_BF16 = 2 };
 
 /*
  * Bytes of device workspace a call of the given kind and shape needs on the
@@ -215,6 +219,25 @@ qg_status qgemm_lut3(const void *X, int64_t ldx,
                      struct CUstream_st *stream);
 
 /*
+ * Dense BF16 GEMM (no quantisation), e.g. an output projection (lm_head) at
+ * decode batch sizes.
+ *   X        device, BF16 [M, ldx], 16-byte aligned, ldx >= K, ldx % 8 == 0
+ *   W        device, BF16 [N, K] row-major (row stride K elements), 16-byte
+ *            aligned
+ *   Y        device, BF16 [M, ldy], ldy >= N
+ *   M, N, K  1 <= M <= 32, N >= 1, K % 8 == 0 (ragged N and K tails are
+ *            handled)
+ *   workspace as for qgemm_fp8_block, with kind QG_KIND_BF16.
+ * Results match the strict-K-order FP32 sum within the header's comparison
+ * rule (2 BF16 ULP, or the absolute floor for outputs that cancel).
+ */
+qg_status qgemm_bf16(const void *X, int64_t ldx, const void *W,
+                     void *Y, int64_t ldy,
+                     int M, int N, int K,
+                     void *workspace, size_t workspace_bytes,
+                     struct CUstream_st *stream);
+
+/*
  * Packed size, in bytes, of an [N, K] 3-bit code matrix:
  * ceil(N/128) * ceil(K/256) * 16384.
  */
@@ -290,6 +313,46 @@ qg_status qg_dequant_lut3(const void *Wq, const void *qmap, const void *scales,
 qg_status qg_dispatch_set(int kind, int M, int N, int K, int ctas);
 int qg_dispatch_get(int kind, int M, int N, int K);
 void qg_dispatch_clear(void);
+
+/*
+ * The largest workspace any grid of a shape with N output rows may need on
+ * the current device (for a multi-segment call, N = the sum of 128 *
+ * ceil(N_j / 128)): a workspace of this size serves every dispatch-table
+ * entry of such shapes, as qg_tune_* requires.
+ */
+size_t qg_workspace_bytes_max(int N);
+
+/*
+ * Tuning of the dispatch table for one shape: an exactness-gated search
+ * (FLUTE "optimized_w3" page, Results: a candidate is accepted only after
+ * its output is checked).  The built-in schedule's output, written to Y_ref
+ * (a device buffer shaped like Y), is the reference.  Candidate grids (one CTA
+ * per 128-row tile, 2..8 CTAs per tile, and 4/8..8/8 of the SMs, each at most
+ * the SM count) then run on the caller's buffers; a candidate whose output is
+ * not finite, or differs from the reference by more than a relative
+ * Frobenius distance of 1e-3 or anywhere by more than 1e-2 of the
+ * reference's largest magnitude (a reordered FP32 sum moves results by a
+ * few units in the last place; a misplaced piece moves them by their own
+ * size), is discarded.  The others are timed over `calls` back-to-back calls
+ * (CUDA events on `stream`, current launch-overlap setting), the weights
+ * rotating over the ncopies equal copies given (copies totalling more than
+ * twice the L2 size make the timings stream from HBM), and the fastest
+ * becomes the shape's dispatch-table entry (the entry is removed when the
+ * built-in grid is the fastest).  Candidates that need more than
+ * workspace_bytes of workspace are skipped (qg_workspace_bytes_max(N) serves
+ * all).  Synchronous.  *best_ctas and *best_us (either may be NULL) receive
+ * the grid chosen and its time per call.  Arguments are those of the GEMM
+ * entry point for each W copy.
+ */
+qg_status qg_tune_fp8(const void *X, int64_t ldx, const uint8_t *const *W_copies, int ncopies,
+                      const float *W_scale, void *Y, int64_t ldy, void *Y_ref,
+                      int M, int N, int K, void *workspace, size_t workspace_bytes,
+                      int calls, int *best_ctas, float *best_us, struct CUstream_st *stream);
+
+qg_status qg_tune_lut3(const void *X, int64_t ldx, const void *const *Wq_copies, int ncopies,
+                       const void *qmap, const void *scales, void *Y, int64_t ldy, void *Y_ref,
+                       int M, int N, int K, void *workspace, size_t workspace_bytes,
+                       int calls, int *best_ctas, float *best_us, struct CUstream_st *stream);
 
 /*
  * Test aid: the work split of a shape's schedule, computed on the device by

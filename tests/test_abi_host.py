@@ -175,3 +175,35 @@ def test_multi_argument_validation(qg):
     segs[1] = qg.Fp8Segment(FAKE, FAKE, FAKE, 256, 256)
     assert fn(FAKE, 512, ptr, 3, 33, 512, None, 0, None) == 2     # M > 32
     assert fn(FAKE, 512, ptr, 3, 0, 512, None, 0, None) == 0      # M == 0: no-op
+
+
+def test_tuner_argument_validation(qg):
+    """The tuners check their arguments before touching a device."""
+    P = ctypes.c_void_p
+    ptrs = (P * 1)(FAKE)
+    pp = ctypes.cast(ptrs, P)
+    t = qg.lib.qg_tune_fp8
+    assert t(FAKE, 512, None, 1, FAKE, FAKE, 256, FAKE, 4, 256, 512, None, 0, 10, None, None, None) == 1   # no copies
+    assert t(FAKE, 512, pp, 0, FAKE, FAKE, 256, FAKE, 4, 256, 512, None, 0, 10, None, None, None) == 1     # ncopies 0
+    assert t(FAKE, 512, pp, 1, FAKE, FAKE, 256, None, 4, 256, 512, None, 0, 10, None, None, None) == 1     # no Y_ref
+    assert t(FAKE, 512, pp, 1, FAKE, FAKE, 256, FAKE, 4, 256, 512, None, 0, 0, None, None, None) == 1      # calls 0
+    assert t(FAKE, 512, pp, 1, FAKE, FAKE, 256, FAKE, 33, 256, 512, None, 0, 10, None, None, None) == 2    # M > 32
+    t3 = qg.lib.qg_tune_lut3
+    assert t3(FAKE, 512, None, 1, FAKE, FAKE, FAKE, 256, FAKE, 4, 256, 512, None, 0, 10, None, None, None) == 1
+    assert qg.lib.qg_workspace_bytes_max(0) == 0
+
+
+@pytest.mark.parametrize("args,expect", [
+    # X, ldx, W, Y, ldy, M, N, K
+    ((FAKE, 512, FAKE, FAKE, 256, 0, 256, 512), 0),        # M == 0: no-op
+    ((None, 512, FAKE, FAKE, 256, 4, 256, 512), 1),        # null X
+    ((FAKE, 512, None, FAKE, 256, 4, 256, 512), 1),        # null W
+    ((FAKE, 512, FAKE, FAKE, 256, 33, 256, 512), 2),       # M > 32
+    ((FAKE, 516, FAKE, FAKE, 256, 4, 256, 516), 2),        # K % 8
+    ((FAKE, 256, FAKE, FAKE, 256, 4, 256, 512), 1),        # ldx < K
+    ((FAKE + 8, 512, FAKE, FAKE, 256, 4, 256, 512), 3),    # X not 16-byte aligned
+    ((FAKE, 512, FAKE + 2, FAKE, 256, 4, 256, 512), 3),    # W not 16-byte aligned
+])
+def test_bf16_argument_validation(qg, args, expect):
+    X, ldx, W, Y, ldy, M, N, K = args
+    assert qg.lib.qgemm_bf16(X, ldx, W, Y, ldy, M, N, K, None, 0, None) == expect

@@ -113,3 +113,40 @@ def test_lut3_split_and_unsplit_agree(grids):
             assert rep.ok, (G, rep)
     finally:
         q.dispatch_clear()
+
+
+def test_fp8_tuner_installs_a_gated_grid():
+    """The tuner times the candidate grids that pass its gate, installs the
+    fastest in the dispatch table, and later calls use it and stay within the
+    oracle's budget."""
+    q = qg()
+    M, N, K = 16, 5120, 5120
+    p = cached(("fp8", M, N, K, 70), lambda: wl.make_fp8_problem(M, N, K, config_id=70))
+    dev = Fp8Device(p, copies=2)
+    Xd = torch.from_numpy(p.X.view(np.int16)).view(torch.bfloat16).cuda()
+    try:
+        g, us = q.tune_fp8(Xd, dev.W, dev.S, calls=40)
+        assert 1 <= g <= torch.cuda.get_device_properties(0).multi_processor_count and us > 0
+        assert q.dispatch_get(q.KIND_FP8_BLOCK, M, N, K) == g
+        y = _fp8_runs(q, p, dev, Xd)
+        ok, rep = grade_fp8(p, y)
+        assert rep.ok, rep
+    finally:
+        q.dispatch_clear()
+
+
+def test_lut3_tuner_installs_a_gated_grid():
+    q = qg()
+    M, N, K = 8, 1024, 4096
+    p = cached(("lut3", M, N, K, 71), lambda: wl.make_lut3_problem(M, N, K, config_id=71))
+    dev = Lut3Device(p)
+    Xd = torch.from_numpy(p.X.view(np.int16)).view(torch.float16).cuda()
+    try:
+        g, us = q.tune_lut3(Xd, [dev.Wq, dev.Wq.clone()], dev.qmap, dev.scales, N, calls=40)
+        assert q.dispatch_get(q.KIND_LUT3, M, N, K) == g and us > 0
+        Y = q.qgemm_lut3(Xd, dev.Wq, dev.qmap, dev.scales, N)
+        assert q.last_device_status() == 0
+        ok, rep = grade_lut3(p, to_bits(Y))
+        assert rep.ok, rep
+    finally:
+        q.dispatch_clear()

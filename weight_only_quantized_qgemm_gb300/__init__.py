@@ -15,6 +15,8 @@ The names follow the C ABI in ``include/qgemm.h``:
   memory (staged in and stored out by the library's kernels).
 * :func:`qgemm_lut3` -- 3-bit learned-LUT weights (see :func:`pack_lut3`),
   FP16 activations and output.
+* :func:`qgemm_bf16` -- unquantised BF16 weights (e.g. an lm_head), BF16
+  activations and output.
 * :func:`pack_lut3` / :func:`unpack_lut3` -- offline nibble packer (host).
 * :func:`debug_fp8_split` / :func:`dequant_lut3` -- test aids: the FP8
   kernel's activation split and the LUT3 kernel's dequantiser on their own,
@@ -32,7 +34,7 @@ __all__ = [
     "qgemm_fp8_block", "qgemm_fp8_block_multi", "qgemm_fp8_block_host", "Fp8Segment", "MAX_SEGMENTS", "qgemm_lut3", "pack_lut3", "unpack_lut3", "lut3_packed_bytes",
     "debug_fp8_split", "dequant_lut3", "last_device_status", "set_wait_timeout_ns",
     "set_fault_injection", "set_weight_prefetch_overlap", "dispatch_set", "dispatch_get", "dispatch_clear",
-    "debug_schedule", "KIND_FP8_BLOCK", "KIND_LUT3", "STATUS",
+    "debug_schedule", "tune_fp8", "tune_lut3", "workspace_bytes_max", "qgemm_bf16", "KIND_BF16", "KIND_FP8_BLOCK", "KIND_LUT3", "STATUS",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -40,6 +42,7 @@ LIB_PATH = os.path.join(_PKG, "libqgemm.so")
 
 KIND_FP8_BLOCK = 0
 KIND_LUT3 = 1
+KIND_BF16 = 2
 STATUS = {
     0: "QG_OK", 1: "QG_ERR_INVALID_ARG", 2: "QG_ERR_UNSUPPORTED_SHAPE", 3: "QG_ERR_MISALIGNED",
     4: "QG_ERR_CUDA", 5: "QG_ERR_TIMEOUT", 6: "QG_ERR_WORKSPACE",
@@ -69,6 +72,7 @@ _SIGS = {
     "qgemm_fp8_block_multi": (_I, [_P, _L, _P, _I, _I, _I, _P, _S, _P]),
     "qgemm_fp8_block_host": (_I, [_P, _L, _P, _P, _P, _L, _I, _I, _I, _P, _P, _S, _P]),
     "qgemm_lut3": (_I, [_P, _L, _P, _P, _P, _P, _L, _I, _I, _I, _P, _S, _P]),
+    "qgemm_bf16": (_I, [_P, _L, _P, _P, _L, _I, _I, _I, _P, _S, _P]),
     "qg_lut3_packed_bytes": (_S, [_I, _I]),
     "pack_lut3": (_I, [_P, _P, _I, _I]),
     "unpack_lut3": (_I, [_P, _P, _I, _I]),
@@ -77,6 +81,9 @@ _SIGS = {
     "qg_dispatch_set": (_I, [_I, _I, _I, _I, _I]),
     "qg_dispatch_get": (_I, [_I, _I, _I, _I]),
     "qg_dispatch_clear": (None, []),
+    "qg_workspace_bytes_max": (_S, [_I]),
+    "qg_tune_fp8": (_I, [_P, _L, _P, _I, _P, _P, _L, _P, _I, _I, _I, _P, _S, _I, _P, _P, _P]),
+    "qg_tune_lut3": (_I, [_P, _L, _P, _I, _P, _P, _P, _L, _P, _I, _I, _I, _P, _S, _I, _P, _P, _P]),
     "qg_dequant_lut3": (_I, [_P, _P, _P, _P, _I, _I, _P]),
     "qg_last_device_status": (_I, [_P]),
     "qg_set_wait_timeout_ns": (None, [ctypes.c_uint64]),
@@ -298,6 +305,29 @@ def qgemm_lut3(X, Wq, qmap, scales, N: int, Y=None, workspace=None, stream=None)
     return Y
 
 
+def qgemm_bf16(X, W, Y=None, workspace=None, stream=None):
+    """Y[M, N] = X[M, K] . W[N, K]^T with BF16 X, W and Y (FP32 sums).
+
+    X: bf16 CUDA [M, K] (row stride a multiple of 8); W: bf16 [N, K]
+    contiguous; Y (optional): bf16 [M, N] with unit column stride.
+    """
+    torch = _torch()
+    if X.dtype != torch.bfloat16 or W.dtype != torch.bfloat16:
+        raise TypeError("X and W must be bfloat16")
+    if not W.is_contiguous():
+        raise TypeError("W must be contiguous")
+    M, K = X.shape
+    N = W.shape[0]
+    if W.shape[1] != K:
+        raise ValueError("shape mismatch between X and W")
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
+    ws, wsb = _workspace_for(KIND_BF16, M, N, K, workspace, X.device)
+    _check(lib.qgemm_bf16(X.data_ptr(), _ld(X), W.data_ptr(), Y.data_ptr(), _ld(Y), M, N, K, ws, wsb,
+                          _stream_ptr(stream)), "qgemm_bf16")
+    return Y
+
+
 def lut3_packed_bytes(N: int, K: int) -> int:
     return int(lib.qg_lut3_packed_bytes(N, K))
 
@@ -394,3 +424,53 @@ def debug_schedule(kind: int, M: int, N: int, K: int, stream=None):
                                  _stream_ptr(stream)), "qg_debug_schedule")
     torch.cuda.synchronize()
     return ranges.cpu().numpy(), info.cpu().numpy()
+
+
+def workspace_bytes_max(N: int) -> int:
+    """The workspace any grid of a shape with N output rows may need."""
+    return int(lib.qg_workspace_bytes_max(N))
+
+
+def _tune_common(M, N, X, Y_ref, workspace):
+    torch = _torch()
+    if workspace is None:
+        workspace = Workspace(X.device)
+    buf = workspace.get(workspace_bytes_max(N)) if isinstance(workspace, Workspace) else workspace
+    return buf, (buf.numel() * buf.element_size() if buf is not None else 0)
+
+
+def tune_fp8(X, W_copies, W_scale, calls: int = 200, workspace=None, stream=None):
+    """Exactness-gated tuning of the dispatch table for the shape of X and W
+    (see qg_tune_fp8 in include/qgemm.h).  W_copies: equal E4M3 weight
+    tensors the timed calls rotate over.  Returns (grid, us per call)."""
+    torch = _torch()
+    M, K = X.shape
+    N = W_copies[0].shape[0]
+    Y = torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
+    Y_ref = torch.empty_like(Y)
+    buf, nb = _tune_common(M, N, X, Y_ref, workspace)
+    ptrs = (ctypes.c_void_p * len(W_copies))(*[w.data_ptr() for w in W_copies])
+    g, us = ctypes.c_int(0), ctypes.c_float(0)
+    _check(lib.qg_tune_fp8(X.data_ptr(), _ld(X), ctypes.cast(ptrs, ctypes.c_void_p), len(W_copies),
+                           W_scale.data_ptr(), Y.data_ptr(), N, Y_ref.data_ptr(), M, N, K,
+                           buf.data_ptr() if buf is not None else None, nb, calls, ctypes.byref(g), ctypes.byref(us),
+                           _stream_ptr(stream)), "qg_tune_fp8")
+    _ws_need.clear()
+    return g.value, us.value
+
+
+def tune_lut3(X, Wq_copies, qmap, scales, N: int, calls: int = 200, workspace=None, stream=None):
+    """As tune_fp8 for the 3-bit LUT GEMM (Wq_copies: equal packed weights)."""
+    torch = _torch()
+    M, K = X.shape
+    Y = torch.empty((M, N), dtype=torch.float16, device=X.device)
+    Y_ref = torch.empty_like(Y)
+    buf, nb = _tune_common(M, N, X, Y_ref, workspace)
+    ptrs = (ctypes.c_void_p * len(Wq_copies))(*[w.data_ptr() for w in Wq_copies])
+    g, us = ctypes.c_int(0), ctypes.c_float(0)
+    _check(lib.qg_tune_lut3(X.data_ptr(), _ld(X), ctypes.cast(ptrs, ctypes.c_void_p), len(Wq_copies),
+                            qmap.data_ptr(), scales.data_ptr(), Y.data_ptr(), N, Y_ref.data_ptr(), M, N, K,
+                            buf.data_ptr() if buf is not None else None, nb, calls, ctypes.byref(g),
+                            ctypes.byref(us), _stream_ptr(stream)), "qg_tune_lut3")
+    _ws_need.clear()
+    return g.value, us.value

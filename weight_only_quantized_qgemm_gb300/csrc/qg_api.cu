@@ -206,7 +206,7 @@ const SchedEntry& cached_schedule(int kind, int M, int N, int K, int sms) {
 
 // Tensor maps of operands that stay put between calls, keyed by what the map
 // encodes (address, shape and kind).
-enum MapKind { kMapFp8Weights = 0, kMapLut3Scales = 1 };
+enum MapKind { kMapFp8Weights = 0, kMapLut3Scales = 1, kMapBf16Weights = 2 };
 
 struct MapEntry {
     const void* ptr = nullptr;
@@ -219,6 +219,7 @@ struct MapEntry {
 // driver refused it.
 //   kMapFp8Weights: E4M3 weights, 128 x 128 boxes, 128-byte swizzle.
 //   kMapLut3Scales: FP16 LUT3 scales [N, K/128], boxes of 8 groups x 128 rows.
+//   kMapBf16Weights: BF16 weights [N, K], 64 x 128 boxes, 128-byte swizzle.
 const CUtensorMap* cached_tmap(const void* ptr, uint64_t cols, uint64_t rows, MapKind kind) {
     thread_local MapEntry cache[kCacheWays];
     thread_local int next = 0;
@@ -227,6 +228,8 @@ const CUtensorMap* cached_tmap(const void* ptr, uint64_t cols, uint64_t rows, Ma
     MapEntry& e = cache[next];
     const bool ok = kind == kMapFp8Weights
                         ? make_tmap(&e.map, ptr, CU_TENSOR_MAP_DATA_TYPE_UINT8, cols, rows, cols, 128, 128)
+                    : kind == kMapBf16Weights
+                        ? make_tmap(&e.map, ptr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cols, rows, cols * 2, 64, 128)
                         : make_tmap(&e.map, ptr, CU_TENSOR_MAP_DATA_TYPE_UINT16, cols, rows, cols * 2, 8, 128,
                                     CU_TENSOR_MAP_SWIZZLE_NONE);
     if (!ok) {
@@ -420,10 +423,21 @@ extern "C" {
 
 size_t qg_workspace_bytes(int kind, int M, int N, int K) {
     if (M < 1 || N < 1 || K < 1 || M > 32) return 0;
-    if (kind != QG_KIND_FP8_BLOCK && kind != QG_KIND_LUT3) return 0;
+    if (kind != QG_KIND_FP8_BLOCK && kind != QG_KIND_LUT3 && kind != QG_KIND_BF16) return 0;
     DeviceInfo* d = device_info();
     if (!d) return 0;
     return cached_schedule(kind, M, N, K, d->sms).ws;
+}
+
+size_t qg_workspace_bytes_max(int N) {
+    if (N < 1) return 0;
+    DeviceInfo* d = device_info();
+    if (!d) return 0;
+    Schedule s;
+    s.T = (N + 127) / 128;
+    s.max_ctas = d->sms;
+    const size_t cnt = (static_cast<size_t>(s.T) * 4 * sizeof(uint32_t) + 255) & ~static_cast<size_t>(255);
+    return workspace_partial_bytes(s) + cnt;
 }
 
 qg_status qgemm_fp8_block(const void* X, int64_t ldx, const uint8_t* W, const float* W_scale, void* Y, int64_t ldy,
@@ -498,6 +512,42 @@ qg_status qgemm_fp8_block_multi(const void* X, int64_t ldx, const qg_fp8_segment
     a.K = K;
     a.ws = need > 0 ? workspace : nullptr;
     return launch_fp8(a, s, maps, launch_ctl(d), stream) == cudaSuccess ? QG_OK : QG_ERR_CUDA;
+}
+
+qg_status qgemm_bf16(const void* X, int64_t ldx, const void* W, void* Y, int64_t ldy, int M, int N, int K,
+                     void* workspace, size_t workspace_bytes_, cudaStream_t stream) {
+    if (M < 0 || N < 0 || K < 0) return QG_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return QG_OK;
+    if (!X || !W || !Y) return QG_ERR_INVALID_ARG;
+    if (M > 32 || K % 8 != 0) return QG_ERR_UNSUPPORTED_SHAPE;
+    if (ldx < K || ldy < N) return QG_ERR_INVALID_ARG;
+    if (!aligned16(X) || !aligned16(W) || (ldx % 8) != 0 || (reinterpret_cast<uintptr_t>(Y) & 1u) != 0)
+        return QG_ERR_MISALIGNED;
+    DeviceInfo* d = device_info();
+    if (!d) return QG_ERR_CUDA;
+    if (K == 0) return launch_zero_rows(Y, ldy, M, N, stream) == cudaSuccess ? QG_OK : QG_ERR_CUDA;
+    const SchedEntry& se = cached_schedule(QG_KIND_BF16, M, N, K, d->sms);
+    const Schedule s = se.s;
+    const size_t need = se.ws;
+    if (need > 0 && (!workspace || workspace_bytes_ < need || (reinterpret_cast<uintptr_t>(workspace) & 255u)))
+        return QG_ERR_WORKSPACE;
+    const CUtensorMap* tmW = cached_tmap(W, static_cast<uint64_t>(K), static_cast<uint64_t>(N), kMapBf16Weights);
+    if (!tmW) return QG_ERR_CUDA;
+    CUtensorMap tmX;
+    if (!make_tmap(&tmX, X, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<uint64_t>(K), static_cast<uint64_t>(M),
+                   static_cast<uint64_t>(ldx) * 2, 64, static_cast<uint32_t>(s.nmma)))
+        return QG_ERR_CUDA;
+    Bf16Args a;
+    a.X = X;
+    a.ldx = ldx;
+    a.W = W;
+    a.Y = Y;
+    a.ldy = ldy;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.ws = need > 0 ? workspace : nullptr;
+    return launch_bf16(a, s, *tmW, tmX, launch_ctl(d), stream) == cudaSuccess ? QG_OK : QG_ERR_CUDA;
 }
 
 qg_status qgemm_lut3(const void* X, int64_t ldx, const void* Wq, const void* qmap, const void* scales, void* Y,
@@ -625,9 +675,9 @@ qg_status qg_dequant_lut3(const void* Wq, const void* qmap, const void* scales, 
 
 qg_status qg_debug_schedule(int kind, int M, int N, int K, int* ctas, int64_t* ranges, int* info, int capacity,
                             cudaStream_t stream) {
-    if (kind != QG_KIND_FP8_BLOCK && kind != QG_KIND_LUT3) return QG_ERR_INVALID_ARG;
+    if (kind != QG_KIND_FP8_BLOCK && kind != QG_KIND_LUT3 && kind != QG_KIND_BF16) return QG_ERR_INVALID_ARG;
     if (M < 1 || M > 32 || N < 1 || K < 1 || !ctas) return QG_ERR_INVALID_ARG;
-    if (kind == QG_KIND_FP8_BLOCK ? K % 16 != 0 : K % 128 != 0) return QG_ERR_UNSUPPORTED_SHAPE;
+    if (K % (kind == QG_KIND_FP8_BLOCK ? 16 : kind == QG_KIND_BF16 ? 8 : 128) != 0) return QG_ERR_UNSUPPORTED_SHAPE;
     DeviceInfo* d = device_info();
     if (!d) return QG_ERR_CUDA;
     const Schedule s = cached_schedule(kind, M, N, K, d->sms).s;
@@ -640,7 +690,7 @@ qg_status qg_debug_schedule(int kind, int M, int N, int K, int* ctas, int64_t* r
 }
 
 qg_status qg_dispatch_set(int kind, int M, int N, int K, int ctas) {
-    if (kind != QG_KIND_FP8_BLOCK && kind != QG_KIND_LUT3) return QG_ERR_INVALID_ARG;
+    if (kind != QG_KIND_FP8_BLOCK && kind != QG_KIND_LUT3 && kind != QG_KIND_BF16) return QG_ERR_INVALID_ARG;
     if (M < 1 || M > 32 || N < 1 || K < 1 || ctas < 0) return QG_ERR_INVALID_ARG;
     DeviceInfo* d = device_info();
     if (!d) return QG_ERR_CUDA;
@@ -666,7 +716,7 @@ qg_status qg_dispatch_set(int kind, int M, int N, int K, int ctas) {
 }
 
 int qg_dispatch_get(int kind, int M, int N, int K) {
-    if (kind != QG_KIND_FP8_BLOCK && kind != QG_KIND_LUT3) return 0;
+    if (kind != QG_KIND_FP8_BLOCK && kind != QG_KIND_LUT3 && kind != QG_KIND_BF16) return 0;
     if (M < 1 || M > 32 || N < 1 || K < 1) return 0;
     DeviceInfo* d = device_info();
     if (!d) return 0;

@@ -10,7 +10,7 @@
 // one tile in a CTA's range) accumulate in TMEM; the fold warps read each
 // piece once.
 //
-// One persistent CTA per SM; warps by role (N = 16: 20 warps, 96 registers
+// One persistent CTA per SM; warps by role (N = 16: 24 warps, 80 registers
 // each; N = 32: 16 warps, 128 registers):
 //   warp 0        code producer: 4 lanes in step, one bulk copy per unit
 //                 (evict-first L2 hint) into a ring of up to 15 stages.  A
@@ -23,10 +23,11 @@
 //                 kind::f16 (M=128, N=16|32, K=16), A from TMEM, B (X) from
 //                 shared memory, then the commits, from one elected lane.
 //   warps 2-5     fold / epilogue, one per TMEM lane quadrant.
-//   warps 6-      dequant: 3 groups (2 at N = 32) of four warps, group g
+//   warps 6-      dequant: 4 groups (2 at N = 32) of four warps, group g
 //                 taking units i with i % groups == g: shared memory ->
 //                 registers -> FP16 by byte-permute lookups -> tcgen05.st into
-//                 a ring of 6 A buffers in TMEM.
+//                 a ring of A buffers in TMEM (one per group at N = 16, three
+//                 per group at N = 32).
 //
 // Work units are split evenly over the CTAs in tile-major order (stream-K);
 // a tile shared by several CTAs is summed, in ascending K order of its
@@ -50,11 +51,13 @@ constexpr int kWarpDeq0 = 6;
 
 // Warp roles for an MMA width: dequant groups of four warps (one per TMEM lane
 // quadrant) taking every kDeqGroups-th unit, then the second MMA issuer and the
-// X producer.  Three groups at N = 16 (20 warps); two at N = 32, whose wider
-// fold needs the registers of a 16-warp CTA.
+// X producer.  Four groups at N = 16 (24 warps): the byte permutes of the
+// dequant keep the ALU pipe busy only if enough warps convert at once (three
+// groups measured 31.7 us, four 30.4 us on 28672 x 8192 at M = 16, same box).
+// Two at N = 32, whose wider fold needs the registers of a 16-warp CTA.
 template <int NMMA>
 struct Roles {
-    static constexpr int kDeqGroups = NMMA == 16 ? 3 : 2;
+    static constexpr int kDeqGroups = NMMA == 16 ? 4 : 2;
     static constexpr int kWarpMma2 = kWarpDeq0 + 4 * kDeqGroups;
     static constexpr int kWarpXProd = kWarpMma2 + 1;
     static constexpr int kThreads = 32 * (kWarpXProd + 1);
@@ -113,15 +116,19 @@ struct Layout {
     // two tile pieces in flight (a piece = the units of one tile in this CTA's
     // range).  The format has no per-block fold scale, so a piece's MMAs
     // accumulate in TMEM across its K blocks and the fold reads each piece
-    // once instead of once per unit.
-    static constexpr int kNA = 6;
+    // once instead of once per unit.  Every A buffer belongs to one dequant
+    // group; four groups get one each (two each would need 512 columns before
+    // the accumulators), so a group converting its next unit first waits for
+    // the MMAs of its previous one.
+    static constexpr int kNA = Roles<NMMA>::kDeqGroups == 4 ? 4 : 6;
     static constexpr int kDCol0 = kNA * 64;               // accumulator (b, j) at kDCol0 + NMMA (2 b + j)
     static_assert(kDCol0 + 4 * NMMA <= kTmemCols, "TMEM columns");
     static constexpr int kXSlot = NMMA * 256;             // two 64-element X boxes
     static constexpr int kXBox = NMMA * 128;
-    // X slots: two per A buffer, enough for the X copies (L2 hits) to run
-    // ahead of the MMAs; the rest of the budget goes to the weight ring.
-    static constexpr int kXStages = 2 * kNA;
+    // X slots: enough for the X copies (L2 hits) to run ahead of the MMAs
+    // (and for the final split-K reduction's staging); the rest of the budget
+    // goes to the weight ring.
+    static constexpr int kXStages = 12;
     static constexpr int kWBudget = 212992 - kXStages * kXSlot;   // 208 KB in all
     // A multiple of the dequant group count, so that every use of a weight stage
     // falls to the same dequant group (units i and i + kWStages are taken by
@@ -245,11 +252,6 @@ __device__ __forceinline__ int split_info_lane(const Params& p, long long u0, lo
     return v;
 }
 
-// End of a CTA's piece of `tile` (one warp, TMEM lane quadrant q, one output
-// row per lane).  A whole tile is stored directly; a split piece goes to the
-// workspace, and the last of the tile's CTAs to arrive sums every piece in
-// ascending K order and stores the tile.  Store::store(Y, index, value)
-// writes one output element.
 // The segment holding `tile` (constant-index selects: a dynamic index into
 // the kernel parameters would go through local memory).
 __device__ __forceinline__ Seg seg_of(const Params& p, int tile) {

@@ -76,6 +76,16 @@ struct Lut3Args {
     void* ws;
 };
 
+struct Bf16Args {
+    const void* X;
+    int64_t ldx;
+    const void* W;
+    void* Y;
+    int64_t ldy;
+    int M, N, K;
+    void* ws;
+};
+
 struct LaunchCtl {
     uint64_t timeout_ns;
     int fault_unit;
@@ -91,6 +101,10 @@ cudaError_t launch_fp8(const Fp8Args& a, const Schedule& s, const Fp8Maps& maps,
 cudaError_t launch_lut3(const Lut3Args& a, const Schedule& s, const CUtensorMap& tmX, const CUtensorMap* tmS,
                         const LaunchCtl& c, cudaStream_t st);
 
+// tmW: the weight map ([N, K] BF16, boxes of 64 K x 128 rows); tmX: the
+// activation map ([M, K] BF16, boxes of 64 K x MMA-N rows).
+cudaError_t launch_bf16(const Bf16Args& a, const Schedule& s, const CUtensorMap& tmW, const CUtensorMap& tmX,
+                        const LaunchCtl& c, cudaStream_t st);
 cudaError_t launch_split_probe(const void* X, int64_t blocks, void* hi, void* lo, int* exponent, cudaStream_t st);
 cudaError_t launch_dequant_lut3(const void* Wq, const void* qmap, const void* scales, void* D,
                                 int N, int K, cudaStream_t st);
