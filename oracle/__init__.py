@@ -38,7 +38,8 @@ __all__ = [
     "qgemm_fp8_block_sample", "fp8_abs_mass", "lut3_dequant", "lut3_dequant_matrix",
     "qgemm_lut3", "qgemm_lut3_sample", "lut3_abs_mass", "pack_lut3", "unpack_lut3",
     "lut3_packed_bytes", "bf16_ord", "fp16_ord", "within_budget", "BudgetReport",
-    "gemm_bf16", "gemm_bf16_sample", "bf16_abs_mass",
+    "gemm_bf16", "gemm_bf16_sample", "bf16_abs_mass", "float_to_e4m3", "quantize_act_e4m3",
+    "qgemm_w8a8_block", "w8a8_abs_mass",
     "max_threads",
 ]
 
@@ -85,6 +86,10 @@ _SIGS = {
     "oracle_qgemm_fp8_block": (None, [_I, _I, _I, _P, _L, _P, _L, _P, _L, _P, _P, _L, _I]),
     "oracle_qgemm_fp8_block_sample": (None, [_I, _I, _I, _P, _L, _P, _L, _P, _L, _P, _P, _L, _P, _P, _I]),
     "oracle_fp8_abs_mass": (None, [_I, _I, _I, _P, _L, _P, _L, _P, _L, _P, _P, _L, _P, _I]),
+    "oracle_float_to_e4m3_rne_sat": (ctypes.c_uint8, [ctypes.c_float]),
+    "oracle_quantize_act_e4m3": (None, [_I, _I, _P, _L, _P, _L, _P, _L]),
+    "oracle_qgemm_w8a8_block": (None, [_I, _I, _I, _P, _L, _P, _L, _P, _L, _P, _L, _P, _P, _L, _I]),
+    "oracle_w8a8_abs_mass": (None, [_I, _I, _I, _P, _L, _P, _L, _P, _L, _P, _L, _P, _I]),
     "oracle_gemm_bf16": (None, [_I, _I, _I, _P, _L, _P, _L, _P, _P, _L, _I]),
     "oracle_gemm_bf16_sample": (None, [_I, _I, _I, _P, _L, _P, _L, _P, _P, _L, _P, _P, _I]),
     "oracle_bf16_abs_mass": (None, [_I, _I, _I, _P, _L, _P, _L, _P, _P, _L, _P, _I]),
@@ -157,6 +162,50 @@ def float_to_fp16(x) -> np.ndarray:
     out = np.empty(v.size, dtype=np.uint16)
     lib().oracle_float_to_fp16_array(v.size, _ptr(v), _ptr(out))
     return out.reshape(np.shape(x))
+
+
+# ---------------------------------------------------------------- W8A8
+def float_to_e4m3(x) -> np.ndarray:
+    """E4M3FN codes of float32 values: round to nearest even, saturating at +-448."""
+    a = np.ascontiguousarray(x, dtype=np.float32).ravel()
+    f = lib().oracle_float_to_e4m3_rne_sat
+    return np.array([f(float(v)) for v in a], dtype=np.uint8).reshape(np.shape(x))
+
+
+def quantize_act_e4m3(X):
+    """Per (row, 128-wide K block) activation quantiser: returns (Xq uint8
+    [M, K] E4M3 codes, Sx float32 [ceil(K/128), M] scales)."""
+    X = _c(X, np.uint16)
+    M, K = X.shape
+    KB = -(-K // 128)
+    Xq = np.empty((M, K), dtype=np.uint8)
+    Sx = np.empty((KB, M), dtype=np.float32)
+    lib().oracle_quantize_act_e4m3(M, K, _ptr(X), K, _ptr(Xq), K, _ptr(Sx), M)
+    return Xq, Sx
+
+
+def qgemm_w8a8_block(Xq, Sx, W, S, nthreads: int = 0, want_f32: bool = False):
+    """Y = bf16(two-level fold of E4M3 Xq[M,K] . W[N,K]^T with block factor
+    Sx[kb, m] * S[n/128, kb])."""
+    Xq = _c(Xq, np.uint8); Sx = _c(Sx, np.float32); W = _c(W, np.uint8); S = _c(S, np.float32)
+    M, K = Xq.shape
+    N = W.shape[0]
+    assert W.shape[1] == K and S.shape == (-(-N // 128), -(-K // 128)) and Sx.shape == (-(-K // 128), M)
+    Y = np.empty((M, N), dtype=np.uint16)
+    Yf = np.empty((M, N), dtype=np.float32) if want_f32 else None
+    lib().oracle_qgemm_w8a8_block(M, N, K, _ptr(Xq), K, _ptr(Sx), M, _ptr(W), K, _ptr(S), S.shape[1],
+                                  _ptr(Y), _ptr(Yf), N, nthreads)
+    return (Y, Yf) if want_f32 else Y
+
+
+def w8a8_abs_mass(Xq, Sx, W, S, nthreads: int = 0) -> np.ndarray:
+    Xq = _c(Xq, np.uint8); Sx = _c(Sx, np.float32); W = _c(W, np.uint8); S = _c(S, np.float32)
+    M, K = Xq.shape
+    N = W.shape[0]
+    A = np.empty((M, N), dtype=np.float64)
+    lib().oracle_w8a8_abs_mass(M, N, K, _ptr(Xq), K, _ptr(Sx), M, _ptr(W), K, _ptr(S), S.shape[1], _ptr(A),
+                               nthreads)
+    return A
 
 
 # ---------------------------------------------------------------- dense BF16 GEMM

@@ -20,6 +20,13 @@
  *    fp16_rne(qmap[code] * scale[n, k/128]) before accumulation, the products
  *    with the FP16 activations are summed in FP32 in strict K order, and the
  *    sum is rounded to FP16.
+ *  - The W8A8 block-scaled GEMM (FP8 activations as well as weights): the
+ *    "arc" PR page's cuBLASLt block-scale section notes that block-scaled FP8
+ *    needs FP8 activations and so an activation quantiser.  Activations are
+ *    quantised per (row, 128-wide K block) with the weights' rule (scale =
+ *    block amax / 448, codes = E4M3 round-to-nearest-even of x / scale,
+ *    saturating at 448); the GEMM is the two-level fold with the product of
+ *    the two block scales as the block factor.
  *  - The unquantised BF16 decode GEMM named beside the FP8 tier on the
  *    "atlas" m16_tc page (the numerics contract section: the BF16 lm_head
  *    tier graded by the same comparison): BF16 X and W, products summed in
@@ -317,6 +324,136 @@ void oracle_fp8_abs_mass(int M, int N, int K,
                 blk += fabs((double)oracle_bf16_to_float(X[(int64_t)m * ldx + k]) *
                             (double)oracle_e4m3_to_float(W[(int64_t)n * ldw + k]));
             acc += fabs((double)S[(int64_t)(n / 128) * lds + kb]) * blk;
+        }
+        A[i] = acc;
+    }
+}
+
+/* ------------------------------------------------------------------ */
+/* E4M3 encoding, activation quantiser, W8A8 block-scaled GEMM          */
+/* ------------------------------------------------------------------ */
+
+/* float -> E4M3FN code: round to nearest even on the E4M3 grid (4
+ * significand bits, smallest normal 2^-6, subnormal quantum 2^-9), values
+ * that round beyond the largest finite value 448 saturate to +-448; NaN gives
+ * the NaN code. */
+uint8_t oracle_float_to_e4m3_rne_sat(float f)
+{
+    uint8_t sign = signbit(f) ? 0x80 : 0x00;
+    double r;
+    int ex;
+    if (isnan(f))
+        return (uint8_t)(sign | 0x7F);
+    r = round_to_format(fabs((double)f), 4, -6);
+    if (r > 448.0)
+        r = 448.0;
+    if (r == 0.0)
+        return sign;
+    if (r < ldexp(1.0, -6))                /* subnormal: m * 2^-9 */
+        return (uint8_t)(sign | (uint8_t)(r / ldexp(1.0, -9)));
+    frexp(r, &ex);
+    ex -= 1;
+    return (uint8_t)(sign | (uint8_t)((ex + 7) << 3) | (uint8_t)((r / ldexp(1.0, ex) - 1.0) * 8.0));
+}
+
+/*
+ * Activation quantiser.  For every row m and 128-wide K block kb (the last
+ * one possibly partial): amax = max |x| over the block, s = fl32(amax / 448)
+ * (s = 1 for an all-zero block), q = e4m3(fl32(x / s)).  Xq: [M, K] codes
+ * (row stride ldxq); Sx: [ceil(K/128), ldsx] scales, entry (kb, m).
+ */
+void oracle_quantize_act_e4m3(int M, int K, const uint16_t *X, int64_t ldx,
+                              uint8_t *Xq, int64_t ldxq, float *Sx, int64_t ldsx)
+{
+    int m, kb, k, KB = (K + 127) / 128;
+    for (m = 0; m < M; ++m) {
+        for (kb = 0; kb < KB; ++kb) {
+            int k0 = 128 * kb, k1 = k0 + 128 < K ? k0 + 128 : K;
+            float amax = 0.0f, sc;
+            for (k = k0; k < k1; ++k) {
+                float a = fabsf(oracle_bf16_to_float(X[(int64_t)m * ldx + k]));
+                if (a > amax)
+                    amax = a;
+            }
+            sc = amax > 0.0f ? amax / 448.0f : 1.0f;
+            Sx[(int64_t)kb * ldsx + m] = sc;
+            for (k = k0; k < k1; ++k) {
+                float q = oracle_bf16_to_float(X[(int64_t)m * ldx + k]) / sc;
+                Xq[(int64_t)m * ldxq + k] = oracle_float_to_e4m3_rne_sat(q);
+            }
+        }
+    }
+}
+
+/* One output of the W8A8 two-level fold, as FP32. */
+static float w8a8_element(int K, const uint8_t *xrow, const float *sx, int64_t ldsx,
+                          const uint8_t *wrow, const float *srow)
+{
+    int kb, k, KB = (K + 127) / 128;
+    float outer = 0.0f;
+    for (kb = 0; kb < KB; ++kb) {
+        int k0 = 128 * kb;
+        int k1 = k0 + 128 < K ? k0 + 128 : K;
+        float inner = 0.0f;
+        for (k = k0; k < k1; ++k) {
+            float prod = oracle_e4m3_to_float(xrow[k]) * oracle_e4m3_to_float(wrow[k]);
+            inner = inner + prod;
+        }
+        {
+            float factor = sx[(int64_t)kb * ldsx] * srow[kb];
+            float scaled = inner * factor;
+            outer = outer + scaled;
+        }
+    }
+    return outer;
+}
+
+/*
+ * Y = bf16(sum_kb fl32(inner_kb * fl32(sx[kb, m] * sw[n/128, kb]))), K blocks
+ * ascending, inner_kb the strict-K FP32 sum of the exact E4M3 x E4M3
+ * products of the block.
+ */
+void oracle_qgemm_w8a8_block(int M, int N, int K,
+                             const uint8_t *Xq, int64_t ldxq, const float *Sx, int64_t ldsx,
+                             const uint8_t *W, int64_t ldw, const float *Sw, int64_t lds,
+                             uint16_t *Y, float *Yf, int64_t ldy, int nthreads)
+{
+    int n;
+    set_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 16)
+    for (n = 0; n < N; ++n) {
+        int m;
+        for (m = 0; m < M; ++m) {
+            float v = w8a8_element(K, Xq + (int64_t)m * ldxq, Sx + m, ldsx, W + (int64_t)n * ldw,
+                                   Sw + (int64_t)(n / 128) * lds);
+            if (Y)
+                Y[(int64_t)m * ldy + n] = oracle_float_to_bf16_rne(v);
+            if (Yf)
+                Yf[(int64_t)m * ldy + n] = v;
+        }
+    }
+}
+
+/* A[m, n] = sum_kb |sx * sw| * sum_{k in kb} |xq * wq| in double. */
+void oracle_w8a8_abs_mass(int M, int N, int K,
+                          const uint8_t *Xq, int64_t ldxq, const float *Sx, int64_t ldsx,
+                          const uint8_t *W, int64_t ldw, const float *Sw, int64_t lds,
+                          double *A, int nthreads)
+{
+    int64_t i, total = (int64_t)M * N;
+    set_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 64)
+    for (i = 0; i < total; ++i) {
+        int m = (int)(i / N), n = (int)(i % N);
+        int kb, k, KB = (K + 127) / 128;
+        double acc = 0.0;
+        for (kb = 0; kb < KB; ++kb) {
+            int k0 = 128 * kb, k1 = k0 + 128 < K ? k0 + 128 : K;
+            double blk = 0.0;
+            for (k = k0; k < k1; ++k)
+                blk += fabs((double)oracle_e4m3_to_float(Xq[(int64_t)m * ldxq + k]) *
+                            (double)oracle_e4m3_to_float(W[(int64_t)n * ldw + k]));
+            acc += fabs((double)Sx[(int64_t)kb * ldsx + m] * (double)Sw[(int64_t)(n / 128) * lds + kb]) * blk;
         }
         A[i] = acc;
     }

@@ -524,3 +524,92 @@ def test_bf16_oracle_rows_independent_and_sampled():
     assert np.array_equal(oracle.gemm_bf16_sample(p.X, p.W, ms, ns), Y[ms, ns])
     assert np.allclose(oracle.bf16_abs_mass(p.X, p.W, ms, ns), oracle.bf16_abs_mass(p.X, p.W)[ms, ns], rtol=0,
                        atol=0)
+
+
+# ------------------------------------------------------------------ W8A8 (FP8 activations)
+def _e4m3_grid():
+    codes = np.arange(0, 0x7F, dtype=np.uint8)
+    return oracle.e4m3_to_float(codes).astype(np.float64)
+
+
+def test_e4m3_encoder_matches_torch():
+    """Round to nearest even with saturation at 448, against torch's
+    float8_e4m3fn conversion of the clamped value: random values over the
+    whole range, every midpoint between neighbouring E4M3 values (ties), and
+    values beyond 448."""
+    rng = np.random.default_rng(31)
+    x = (rng.standard_normal(20000) * np.exp2(rng.uniform(-14, 10, 20000))).astype(np.float32)
+    g = _e4m3_grid()
+    mids = ((g[:-1] + g[1:]) / 2).astype(np.float32)
+    x = np.concatenate([x, mids, -mids, np.nextafter(mids, np.float32(np.inf)),
+                        np.array([448, 449, 464, 480, 1e6, -1e6, 0.0, -0.0, 2 ** -10, 3 * 2 ** -11], np.float32)])
+    ours = oracle.float_to_e4m3(x)
+    ref = torch.from_numpy(np.clip(x, -448, 448)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(ours, ref)
+
+
+def test_activation_quantiser_rule():
+    """Per (row, 128-K block): s = fl32(amax / 448), the largest |code| is
+    448, every value within half an E4M3 step (times s) of x, all-zero
+    blocks get s = 1 and zero codes."""
+    p = wl.make_fp8_problem(4, 128, 300, config_id=32)
+    X = p.X.copy()
+    X[2, 128:256] = 0
+    Xq, Sx = oracle.quantize_act_e4m3(X)
+    x = _bf16_decode(X)
+    dq = oracle.e4m3_to_float(Xq).astype(np.float64)
+    for m in range(4):
+        for kb in range(3):
+            sl = slice(128 * kb, min(300, 128 * kb + 128))
+            amax = np.float32(np.abs(x[m, sl]).max())
+            if amax == 0:
+                assert Sx[kb, m] == 1.0 and np.all(Xq[m, sl] & 0x7F == 0)
+                continue
+            assert Sx[kb, m] == np.float32(amax / np.float32(448.0))
+            assert np.abs(dq[m, sl]).max() == 448.0
+            s = np.float64(Sx[kb, m])
+            err = np.abs(dq[m, sl] * s - x[m, sl])
+            half_step = np.exp2(np.floor(np.log2(np.maximum(np.abs(dq[m, sl]), 2 ** -6))) - 4) * s
+            assert np.all(err <= half_step * (1 + 2 ** -20) + 2 ** -10 * s)
+
+
+def test_w8a8_with_unit_activation_scales_is_the_w8a16_oracle():
+    """When the activations are E4M3 values held as BF16 and their scales are
+    1, the W8A8 fold is the W8A16 fold term for term: identical bits."""
+    p = wl.make_fp8_problem(3, 256, 640, config_id=33)
+    rng = np.random.default_rng(33)
+    Xq = rng.integers(0, 256, size=(3, 640), dtype=np.uint8)
+    Xq[(Xq & 0x7F) == 0x7F] = 0x38                        # no NaN codes
+    Xbf = wl.bf16_bits_from_f32(oracle.e4m3_to_float(Xq).astype(np.float32))
+    Sx = np.ones((5, 3), dtype=np.float32)
+    Y8, Yf8 = oracle.qgemm_w8a8_block(Xq, Sx, p.W, p.S, want_f32=True)
+    Y16, Yf16 = oracle.qgemm_fp8_block(Xbf, p.W, p.S, want_f32=True)
+    assert np.array_equal(Yf8.view(np.uint32), Yf16.view(np.uint32))
+    assert np.array_equal(Y8, Y16)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 128, 128), (3, 256, 512), (5, 130, 200)])
+def test_w8a8_oracle_vs_fp64_brute_force(M, N, K):
+    p = wl.make_fp8_problem(M, N, K, config_id=34)
+    Xq, Sx = oracle.quantize_act_e4m3(p.X)
+    Yb, Yf = oracle.qgemm_w8a8_block(Xq, Sx, p.W, p.S, want_f32=True)
+    xq = oracle.e4m3_to_float(Xq).astype(np.float64)
+    wq = oracle.e4m3_to_float(p.W).astype(np.float64)
+    KB = -(-K // 128)
+    Y64 = np.zeros((M, N))
+    for kb in range(KB):
+        sl = slice(128 * kb, min(K, 128 * kb + 128))
+        f = Sx[kb][:, None].astype(np.float64) * p.S[np.arange(N) // 128, kb][None, :].astype(np.float64)
+        Y64 += (xq[:, sl] @ wq[:, sl].T) * f
+    A = oracle.w8a8_abs_mass(Xq, Sx, p.W, p.S)
+    err = np.abs(Yf.astype(np.float64) - Y64)
+    assert np.all(err <= (128 + KB + 6) * U * A * 1.01), err.max()
+    assert np.array_equal(Yb, torch.from_numpy(Yf).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16))
+
+
+def test_w8a8_power_of_two_activation_scale_is_exact():
+    p = wl.make_fp8_problem(2, 256, 384, config_id=35)
+    Xq, Sx = oracle.quantize_act_e4m3(p.X)
+    _, Yf = oracle.qgemm_w8a8_block(Xq, Sx, p.W, p.S, want_f32=True)
+    _, Yf2 = oracle.qgemm_w8a8_block(Xq, Sx * np.float32(4.0), p.W, p.S, want_f32=True)
+    assert np.array_equal(Yf2, Yf * np.float32(4.0))
