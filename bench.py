@@ -60,10 +60,15 @@ def measured_peaks():
         return 6800.0, "fallback"
 
 
+# The sources the headline (FP8) kernel is built from: a change to any of
+# them makes a stored ncu traffic figure stale.
+HEADLINE_KERNEL_SOURCES = ("qg_fp8.cu", "qg_gemm.cuh", "qg_device.cuh", "qg_internal.h")
+
+
 def kernel_source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "weight_only_quantized_qgemm_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in HEADLINE_KERNEL_SOURCES:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -576,6 +581,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--quick", action="store_true", help="headline only, no secondary configs or CPU baseline")
+    ap.add_argument("--headline-only", action="store_true",
+                    help="time the headline calls and print their line, nothing else (for profiling the kernel)")
     ap.add_argument("--overlap", type=int, choices=[0, 1], default=1,
                     help="launch with weight-prefetch overlap of consecutive calls (default 1)")
     ap.add_argument("--only", choices=["lut3", "fp8_down_m32", "bf16", "fp8_attn_n5120_m16"], default=None,
@@ -669,6 +676,16 @@ def main():
     value = per_call_bytes * world / (ms * 1e-3) / 1e9
     achieved = per_call_bytes / (ms * 1e-3) / 1e9
     copies = case.copies
+    if args.headline_only:
+        if rank == 0:
+            peak, _ = measured_peaks()
+            print(json.dumps({"workload": "fp8_block gate/up M=16 N=17408 K=5120", "us_per_call": round(ms * 1e3, 3),
+                              "GBps": round(achieved, 1), "frac": round(achieved / peak, 4), "steps": args.steps,
+                              "warmup": args.warmup, "clocks": clocks}))
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return 0
 
     e2e_ms, h2d, d2h, e2e_slots = e2e_fp8(torch, qg, stream, case, M, steps=max(200, min(args.steps, 5000)),
                                           warmup=args.warmup)
