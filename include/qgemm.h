@@ -60,20 +60,22 @@ struct CUstream_st; /* the same type as cudaStream_t */
 typedef enum {
     QG_OK = 0,
     QG_ERR_INVALID_ARG = 1,       /* null pointer, negative size, ld < row length */
-    QG_ERR_UNSUPPORTED_SHAPE = 2, /* M > 32, K % 16 (FP8), K % 128 (LUT3) or K % 8 (BF16) != 0 */
+    QG_ERR_UNSUPPORTED_SHAPE = 2, /* M > 32 (65536 for W8A8), K % 16 (FP8, W8A8), K % 128 (LUT3)
+                                     or K % 8 (BF16) != 0 */
     QG_ERR_MISALIGNED = 3,        /* a pointer or row stride breaks the 16-byte rule */
     QG_ERR_CUDA = 4,              /* a CUDA runtime call or kernel launch failed */
     QG_ERR_TIMEOUT = 5,           /* a bounded in-kernel wait ran out */
     QG_ERR_WORKSPACE = 6          /* workspace missing or smaller than qg_workspace_bytes */
 } qg_status;
 
-enum { QG_KIND_FP8_BLOCK = 0, QG_KIND_LUT3 = 1, QG_KIND_BF16 = 2 };
+enum { QG_KIND_FP8_BLOCK = 0, QG_KIND_LUT3 = 1, QG_KIND_BF16 = 2, QG_KIND_W8A8 = 3 };
 
 /*
  * Bytes of device workspace a call of the given kind and shape needs on the
  * current device (0 if none).  The workspace holds split-K partial sums
  * (scratch, sized for the device's largest grid) followed by per-tile arrival
- * counters (the last 16 * ceil(N/128) bytes, rounded up to 256).  It must be
+ * counters (the last 16 * tiles bytes, rounded up to 256; tiles = ceil(N/128),
+ * times ceil(M/32) for QG_KIND_W8A8).  It must be
  * zero-filled once before its first use; every successful call leaves its
  * counters at zero again, so one workspace serves later calls of any shape
  * without clearing.
@@ -238,6 +240,50 @@ qg_status qgemm_bf16(const void *X, int64_t ldx, const void *W,
                      struct CUstream_st *stream);
 
 /*
+ * FP8 activation quantiser of the W8A8 path (block-scaled FP8 GEMMs take FP8
+ * activations as well as FP8 weights: "arc" PR page, the cuBLASLt
+ * block-scale section).  For every row m and 128-wide K block kb (the last
+ * one may be partial):
+ *   X_scale[kb * ldsx + m] = max |X[m, k in kb]| / 448 (FP32 division; 1 for
+ *                            an all-zero block)
+ *   Xq[m * ldxq + k]       = E4M3 code of X[m, k] / X_scale (FP32 division,
+ *                            round to nearest even, saturating at +-448)
+ * and X_scale[kb * ldsx + m] = 0 for m in [M, ldsx).  Bit-exact: the same
+ * FP32 operations in the same order on every device.
+ *   X        device, BF16 [M, ldx], 16-byte aligned, ldx >= K, ldx % 8 == 0
+ *   Xq       device, E4M3 codes [M, ldxq], 16-byte aligned, ldxq >= K,
+ *            ldxq % 16 == 0
+ *   X_scale  device, FP32 [ceil(K/128), ldsx], 16-byte aligned,
+ *            ldsx >= M rounded up to a multiple of 32, ldsx % 4 == 0
+ *   M, K     0 <= M <= 65536, K % 16 == 0
+ * Finite inputs only (the codes of Inf and NaN are unspecified).
+ */
+qg_status qg_quantize_act_e4m3(const void *X, int64_t ldx, uint8_t *Xq, int64_t ldxq,
+                               float *X_scale, int64_t ldsx, int M, int K,
+                               struct CUstream_st *stream);
+
+/*
+ * W8A8 block-scaled GEMM, for batches beyond the decode tier (M > 32, though
+ * any M >= 1 is accepted):
+ *   Y[m, n] = bf16( sum_kb f(kb, m, n) * sum_{k in kb} xq[m, k] * w[n, k] ),
+ *   f(kb, m, n) = X_scale[kb * ldsx + m] * W_scale[n/128, kb]
+ * each 128-wide block sum accumulated in FP32 and folded once, with its
+ * factor, onto an FP32 outer sum (the two-level fold of qgemm_fp8_block).
+ *   Xq, ldxq, X_scale, ldsx  as written by qg_quantize_act_e4m3
+ *   W, W_scale, Y, ldy       as for qgemm_fp8_block
+ *   M, N, K  1 <= M <= 65536, N >= 1, K % 16 == 0
+ *   workspace as for qgemm_fp8_block, with kind QG_KIND_W8A8.
+ * Results match the strict-order FP32 fold within the header's comparison
+ * rule.
+ */
+qg_status qgemm_w8a8_block(const uint8_t *Xq, int64_t ldxq, const float *X_scale, int64_t ldsx,
+                           const uint8_t *W, const float *W_scale,
+                           void *Y, int64_t ldy,
+                           int M, int N, int K,
+                           void *workspace, size_t workspace_bytes,
+                           struct CUstream_st *stream);
+
+/*
  * Packed size, in bytes, of an [N, K] 3-bit code matrix:
  * ceil(N/128) * ceil(K/256) * 16384.
  */
@@ -305,7 +351,7 @@ qg_status qg_dequant_lut3(const void *Wq, const void *qmap, const void *scales,
  *
  * qg_dispatch_set: ctas in 1 .. SM count of the current device sets the
  *   entry (a grid larger than the shape's work units is cut to their
- *   number); ctas == 0 removes it.  M in 1..32.
+ *   number); ctas == 0 removes it.  M in 1..32 (1..65536 for QG_KIND_W8A8).
  * qg_dispatch_get: the grid the next call of the shape launches on the
  *   current device (0 for invalid arguments).
  * qg_dispatch_clear: removes every entry.

@@ -207,3 +207,54 @@ def test_tuner_argument_validation(qg):
 def test_bf16_argument_validation(qg, args, expect):
     X, ldx, W, Y, ldy, M, N, K = args
     assert qg.lib.qgemm_bf16(X, ldx, W, Y, ldy, M, N, K, None, 0, None) == expect
+
+
+@pytest.mark.parametrize("args,expect", [
+    # X, ldx, Xq, ldxq, Sx, ldsx, M, K
+    ((FAKE, 512, FAKE, 512, FAKE, 64, 0, 512), 0),              # M == 0: no-op
+    ((None, 512, FAKE, 512, FAKE, 64, 4, 512), 1),              # null X
+    ((FAKE, 512, None, 512, FAKE, 64, 4, 512), 1),              # null Xq
+    ((FAKE, 512, FAKE, 512, None, 64, 4, 512), 1),              # null scales
+    ((FAKE, 520, FAKE, 520, FAKE, 64, 4, 520), 2),              # K % 16
+    ((FAKE, 512, FAKE, 512, FAKE, 64, 65537, 512), 2),          # M > 65536
+    ((FAKE, 256, FAKE, 512, FAKE, 64, 4, 512), 1),              # ldx < K
+    ((FAKE, 512, FAKE, 256, FAKE, 64, 4, 512), 1),              # ldxq < K
+    ((FAKE, 512, FAKE, 512, FAKE, 32, 33, 512), 1),             # ldsx < M rounded up to 32
+    ((FAKE + 8, 512, FAKE, 512, FAKE, 64, 4, 512), 3),          # X not 16-byte aligned
+    ((FAKE, 512, FAKE, 520, FAKE, 64, 4, 512), 3),              # ldxq % 16
+    ((FAKE, 512, FAKE, 512, FAKE, 66, 4, 512), 3),              # ldsx % 4
+    ((FAKE, 512, FAKE, 512, FAKE + 4, 64, 4, 512), 3),          # scales not 16-byte aligned
+])
+def test_quantize_act_argument_validation(qg, args, expect):
+    X, ldx, Xq, ldxq, Sx, ldsx, M, K = args
+    assert qg.lib.qg_quantize_act_e4m3(X, ldx, Xq, ldxq, Sx, ldsx, M, K, None) == expect
+
+
+@pytest.mark.parametrize("args,expect", [
+    # Xq, ldxq, Sx, ldsx, W, S, Y, ldy, M, N, K
+    ((FAKE, 512, FAKE, 64, FAKE, FAKE, FAKE, 256, 0, 256, 512), 0),        # M == 0: no-op
+    ((None, 512, FAKE, 64, FAKE, FAKE, FAKE, 256, 40, 256, 512), 1),       # null Xq
+    ((FAKE, 512, None, 64, FAKE, FAKE, FAKE, 256, 40, 256, 512), 1),       # null X scales
+    ((FAKE, 512, FAKE, 64, None, FAKE, FAKE, 256, 40, 256, 512), 1),       # null W
+    ((FAKE, 512, FAKE, 64, FAKE, FAKE, None, 256, 40, 256, 512), 1),       # null Y
+    ((FAKE, 520, FAKE, 64, FAKE, FAKE, FAKE, 256, 40, 256, 520), 2),       # K % 16
+    ((FAKE, 512, FAKE, 65536, FAKE, FAKE, FAKE, 256, 65537, 256, 512), 2), # M > 65536
+    ((FAKE, 512, FAKE, 32, FAKE, FAKE, FAKE, 256, 40, 256, 512), 1),       # ldsx < 64
+    ((FAKE, 512, FAKE, 64, FAKE, FAKE, FAKE, 200, 40, 256, 512), 1),       # ldy < N
+    ((FAKE + 16, 520, FAKE, 64, FAKE, FAKE, FAKE, 256, 40, 256, 512), 3),  # ldxq % 16
+    ((FAKE, 512, FAKE + 4, 64, FAKE, FAKE, FAKE, 256, 40, 256, 512), 3),   # X scales alignment
+    ((FAKE, 512, FAKE, 64, FAKE + 8, FAKE, FAKE, 256, 40, 256, 512), 3),   # W alignment
+    ((FAKE, 512, FAKE, 64, FAKE, FAKE + 2, FAKE, 256, 40, 256, 512), 3),   # W scales alignment
+    ((FAKE, 512, FAKE, 64, FAKE, FAKE, FAKE + 1, 256, 40, 256, 512), 3),   # Y alignment
+])
+def test_w8a8_argument_validation(qg, args, expect):
+    Xq, ldxq, Sx, ldsx, W, S, Y, ldy, M, N, K = args
+    assert qg.lib.qgemm_w8a8_block(Xq, ldxq, Sx, ldsx, W, S, Y, ldy, M, N, K, None, 0, None) == expect
+
+
+def test_w8a8_dispatch_accepts_large_m(qg):
+    """The W8A8 kind takes M up to 65536 in the dispatch table's checks."""
+    assert qg.lib.qg_dispatch_set(qg.KIND_W8A8, 65537, 1024, 5120, 8) == 1
+    assert qg.lib.qg_dispatch_set(qg.KIND_W8A8, 256, 1024, 5120, -1) == 1
+    assert qg.lib.qg_dispatch_get(qg.KIND_W8A8, 0, 1024, 5120) == 0
+    assert qg.lib.qg_workspace_bytes(qg.KIND_W8A8, 65537, 1024, 5120) == 0

@@ -17,6 +17,10 @@ The names follow the C ABI in ``include/qgemm.h``:
   FP16 activations and output.
 * :func:`qgemm_bf16` -- unquantised BF16 weights (e.g. an lm_head), BF16
   activations and output.
+* :func:`quantize_act_e4m3` / :func:`qgemm_w8a8_block` -- the W8A8 path for
+  larger batches: BF16 activations quantised to E4M3 per (row, 128-wide K
+  block) with FP32 scales, then an E4M3 x E4M3 block-scaled GEMM
+  (:func:`qgemm_w8a8` runs both).
 * :func:`pack_lut3` / :func:`unpack_lut3` -- offline nibble packer (host).
 * :func:`debug_fp8_split` / :func:`dequant_lut3` -- test aids: the FP8
   kernel's activation split and the LUT3 kernel's dequantiser on their own,
@@ -35,6 +39,7 @@ __all__ = [
     "debug_fp8_split", "dequant_lut3", "last_device_status", "set_wait_timeout_ns",
     "set_fault_injection", "set_weight_prefetch_overlap", "dispatch_set", "dispatch_get", "dispatch_clear",
     "debug_schedule", "tune_fp8", "tune_lut3", "workspace_bytes_max", "qgemm_bf16", "KIND_BF16", "KIND_FP8_BLOCK", "KIND_LUT3", "STATUS",
+    "quantize_act_e4m3", "qgemm_w8a8_block", "qgemm_w8a8", "KIND_W8A8", "MAX_M_W8A8",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -43,6 +48,8 @@ LIB_PATH = os.path.join(_PKG, "libqgemm.so")
 KIND_FP8_BLOCK = 0
 KIND_LUT3 = 1
 KIND_BF16 = 2
+KIND_W8A8 = 3
+MAX_M_W8A8 = 65536
 STATUS = {
     0: "QG_OK", 1: "QG_ERR_INVALID_ARG", 2: "QG_ERR_UNSUPPORTED_SHAPE", 3: "QG_ERR_MISALIGNED",
     4: "QG_ERR_CUDA", 5: "QG_ERR_TIMEOUT", 6: "QG_ERR_WORKSPACE",
@@ -73,6 +80,8 @@ _SIGS = {
     "qgemm_fp8_block_host": (_I, [_P, _L, _P, _P, _P, _L, _I, _I, _I, _P, _P, _S, _P]),
     "qgemm_lut3": (_I, [_P, _L, _P, _P, _P, _P, _L, _I, _I, _I, _P, _S, _P]),
     "qgemm_bf16": (_I, [_P, _L, _P, _P, _L, _I, _I, _I, _P, _S, _P]),
+    "qg_quantize_act_e4m3": (_I, [_P, _L, _P, _L, _P, _L, _I, _I, _P]),
+    "qgemm_w8a8_block": (_I, [_P, _L, _P, _L, _P, _P, _P, _L, _I, _I, _I, _P, _S, _P]),
     "qg_lut3_packed_bytes": (_S, [_I, _I]),
     "pack_lut3": (_I, [_P, _P, _I, _I]),
     "unpack_lut3": (_I, [_P, _P, _I, _I]),
@@ -303,6 +312,65 @@ def qgemm_lut3(X, Wq, qmap, scales, N: int, Y=None, workspace=None, stream=None)
     _check(lib.qgemm_lut3(X.data_ptr(), _ld(X), Wq.data_ptr(), qmap.data_ptr(), scales.data_ptr(),
                           Y.data_ptr(), _ld(Y), M, N, K, ws, wsb, _stream_ptr(stream)), "qgemm_lut3")
     return Y
+
+
+def quantize_act_e4m3(X, Xq=None, X_scale=None, stream=None):
+    """E4M3 codes and FP32 scales of BF16 activations, per (row, 128-wide K
+    block): scale = block max |x| / 448 (1 for a zero block), code =
+    e4m3_rne_satfinite(x / scale).
+
+    X: bf16 CUDA [M, K] (row stride a multiple of 8, K % 16 == 0).  Returns
+    (Xq uint8 [M, K] (a view with row stride rounded up to 16), X_scale
+    float32 [ceil(K/128), ldsx] with ldsx = M rounded up to 32; columns
+    [M, ldsx) are 0).  Xq and X_scale (optional) are written in place.
+    """
+    torch = _torch()
+    if X.dtype != torch.bfloat16:
+        raise TypeError("X must be bfloat16")
+    M, K = X.shape
+    KB = -(-K // 128)
+    if Xq is None:
+        Xq = torch.empty((M, -(-K // 16) * 16), dtype=torch.uint8, device=X.device)[:, :K]
+    if X_scale is None:
+        X_scale = torch.empty((KB, max(32, -(-M // 32) * 32)), dtype=torch.float32, device=X.device)
+    if Xq.dtype not in (torch.uint8, torch.float8_e4m3fn) or X_scale.dtype != torch.float32:
+        raise TypeError("Xq must be uint8 or float8_e4m3fn, X_scale float32")
+    if tuple(Xq.shape) != (M, K) or X_scale.shape[0] != KB:
+        raise ValueError("shape mismatch between X, Xq and X_scale")
+    _check(lib.qg_quantize_act_e4m3(X.data_ptr(), _ld(X), Xq.data_ptr(), _ld(Xq), X_scale.data_ptr(),
+                                    _ld(X_scale), M, K, _stream_ptr(stream)), "qg_quantize_act_e4m3")
+    return Xq, X_scale
+
+
+def qgemm_w8a8_block(Xq, X_scale, W, W_scale, Y=None, workspace=None, stream=None):
+    """Y[M, N] = sum over 128-wide K blocks kb of X_scale[kb, m] *
+    W_scale[n/128, kb] * (Xq[m, kb] . W[n, kb]) (E4M3 x E4M3, FP32 fold, BF16
+    out), with Xq, X_scale as :func:`quantize_act_e4m3` returns them."""
+    torch = _torch()
+    if Xq.dtype not in (torch.uint8, torch.float8_e4m3fn) or W.dtype not in (torch.uint8, torch.float8_e4m3fn):
+        raise TypeError("Xq and W must hold E4M3 codes (uint8 or float8_e4m3fn)")
+    if X_scale.dtype != torch.float32 or W_scale.dtype != torch.float32:
+        raise TypeError("X_scale and W_scale must be float32")
+    if not W.is_contiguous() or not W_scale.is_contiguous():
+        raise TypeError("W and W_scale must be contiguous")
+    M, K = Xq.shape
+    N = W.shape[0]
+    if W.shape[1] != K or tuple(W_scale.shape) != (-(-N // 128), -(-K // 128)) or X_scale.shape[0] != -(-K // 128):
+        raise ValueError("shape mismatch between Xq, X_scale, W and W_scale")
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device=Xq.device)
+    ws, wsb = _workspace_for(KIND_W8A8, M, N, K, workspace, Xq.device)
+    _check(lib.qgemm_w8a8_block(Xq.data_ptr(), _ld(Xq), X_scale.data_ptr(), _ld(X_scale), W.data_ptr(),
+                                W_scale.data_ptr(), Y.data_ptr(), _ld(Y), M, N, K, ws, wsb, _stream_ptr(stream)),
+           "qgemm_w8a8_block")
+    return Y
+
+
+def qgemm_w8a8(X, W, W_scale, Y=None, workspace=None, stream=None):
+    """The W8A8 path from BF16 activations: :func:`quantize_act_e4m3` then
+    :func:`qgemm_w8a8_block` (two launches on one stream)."""
+    Xq, X_scale = quantize_act_e4m3(X, stream=stream)
+    return qgemm_w8a8_block(Xq, X_scale, W, W_scale, Y=Y, workspace=workspace, stream=stream)
 
 
 def qgemm_bf16(X, W, Y=None, workspace=None, stream=None):

@@ -14,8 +14,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OBJ = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libqgemm.so")
-SOURCES = ["qg_api.cu", "qg_fp8.cu", "qg_lut3.cu", "qg_noalloc.cu", "qg_hostio.cu", "qg_tune.cu", "qg_bf16.cu"]
-HEADERS = ["qg_device.cuh", "qg_internal.h", "qg_gemm.cuh"]
+SOURCES = ["qg_api.cu", "qg_fp8.cu", "qg_lut3.cu", "qg_noalloc.cu", "qg_hostio.cu", "qg_tune.cu", "qg_bf16.cu", "qg_w8a8.cu"]
+HEADERS = ["qg_device.cuh", "qg_internal.h", "qg_gemm.cuh", "qg_w8a8.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", os.path.join(ROOT, "include")]
 

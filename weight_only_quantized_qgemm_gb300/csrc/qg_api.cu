@@ -12,6 +12,7 @@
 #include "../../include/qgemm.h"
 #include "qg_gemm.cuh"
 #include "qg_internal.h"
+#include "qg_w8a8.h"
 
 namespace qg {
 
@@ -145,8 +146,9 @@ int table_lookup(int kind, int M, int N, int K) {
 
 Schedule choose_schedule(int kind, int M, int N, int K, int sms) {
     Schedule s;
-    s.nmma = M <= 16 ? 16 : 32;
-    s.T = (N + 127) / 128;
+    s.nmma = M <= 16 && kind != QG_KIND_W8A8 ? 16 : 32;
+    // W8A8 tiles are 128 weight rows x 32 activation rows, weight-tile-major
+    s.T = (N + 127) / 128 * (kind == QG_KIND_W8A8 ? (M + 31) / 32 : 1);
     s.KU = (K + 127) / 128;   // one unit = 128 rows x one 128-wide K block
     s.U = static_cast<long long>(s.T) * s.KU;
     const int forced = table_lookup(kind, M, N, K);
@@ -207,6 +209,21 @@ const SchedEntry& cached_schedule(int kind, int M, int N, int K, int sms) {
 // Tensor maps of operands that stay put between calls, keyed by what the map
 // encodes (address, shape and kind).
 enum MapKind { kMapFp8Weights = 0, kMapLut3Scales = 1, kMapBf16Weights = 2 };
+
+// The largest M a kind accepts: the decode kernels take M <= 32 in one MMA;
+// the W8A8 kernel tiles M in 32-row blocks.
+constexpr int kMaxMW8a8 = 1 << 16;
+int k_multiple(int kind) { return kind == QG_KIND_LUT3 ? 128 : kind == QG_KIND_BF16 ? 8 : 16; }
+
+int max_m(int kind) {
+    switch (kind) {
+        case QG_KIND_FP8_BLOCK:
+        case QG_KIND_LUT3:
+        case QG_KIND_BF16: return 32;
+        case QG_KIND_W8A8: return kMaxMW8a8;
+    }
+    return 0;
+}
 
 struct MapEntry {
     const void* ptr = nullptr;
@@ -422,8 +439,7 @@ using namespace qg;
 extern "C" {
 
 size_t qg_workspace_bytes(int kind, int M, int N, int K) {
-    if (M < 1 || N < 1 || K < 1 || M > 32) return 0;
-    if (kind != QG_KIND_FP8_BLOCK && kind != QG_KIND_LUT3 && kind != QG_KIND_BF16) return 0;
+    if (M < 1 || N < 1 || K < 1 || M > max_m(kind)) return 0;
     DeviceInfo* d = device_info();
     if (!d) return 0;
     return cached_schedule(kind, M, N, K, d->sms).ws;
@@ -548,6 +564,64 @@ qg_status qgemm_bf16(const void* X, int64_t ldx, const void* W, void* Y, int64_t
     a.K = K;
     a.ws = need > 0 ? workspace : nullptr;
     return launch_bf16(a, s, *tmW, tmX, launch_ctl(d), stream) == cudaSuccess ? QG_OK : QG_ERR_CUDA;
+}
+
+qg_status qg_quantize_act_e4m3(const void* X, int64_t ldx, uint8_t* Xq, int64_t ldxq, float* X_scale, int64_t ldsx,
+                               int M, int K, cudaStream_t stream) {
+    if (M < 0 || K < 0) return QG_ERR_INVALID_ARG;
+    if (M == 0 || K == 0) return QG_OK;
+    if (!X || !Xq || !X_scale) return QG_ERR_INVALID_ARG;
+    if (M > kMaxMW8a8 || K % 16 != 0) return QG_ERR_UNSUPPORTED_SHAPE;
+    if (ldx < K || ldxq < K || ldsx < (static_cast<int64_t>(M) + 31) / 32 * 32) return QG_ERR_INVALID_ARG;
+    if (!aligned16(X) || !aligned16(Xq) || !aligned16(X_scale) || ldx % 8 != 0 || ldxq % 16 != 0 || ldsx % 4 != 0)
+        return QG_ERR_MISALIGNED;
+    if ((K + 127) / 128 * ldsx > (int64_t(1) << 31) / 32) return QG_ERR_UNSUPPORTED_SHAPE;
+    DeviceInfo* d = device_info();
+    if (!d) return QG_ERR_CUDA;
+    return launch_quantize_act(X, ldx, Xq, ldxq, X_scale, ldsx, M, K, launch_ctl(d), stream) == cudaSuccess
+               ? QG_OK
+               : QG_ERR_CUDA;
+}
+
+qg_status qgemm_w8a8_block(const uint8_t* Xq, int64_t ldxq, const float* X_scale, int64_t ldsx, const uint8_t* W,
+                           const float* W_scale, void* Y, int64_t ldy, int M, int N, int K, void* workspace,
+                           size_t workspace_bytes_, cudaStream_t stream) {
+    if (M < 0 || N < 0 || K < 0) return QG_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return QG_OK;
+    if (!Xq || !X_scale || !W || !W_scale || !Y) return QG_ERR_INVALID_ARG;
+    if (M > kMaxMW8a8 || K % 16 != 0) return QG_ERR_UNSUPPORTED_SHAPE;
+    if (ldxq < K || ldy < N || ldsx < (static_cast<int64_t>(M) + 31) / 32 * 32) return QG_ERR_INVALID_ARG;
+    if (!aligned16(Xq) || !aligned16(W) || !aligned16(X_scale) || ldxq % 16 != 0 || ldsx % 4 != 0)
+        return QG_ERR_MISALIGNED;
+    if ((reinterpret_cast<uintptr_t>(W_scale) & 3u) != 0 || (reinterpret_cast<uintptr_t>(Y) & 1u) != 0)
+        return QG_ERR_MISALIGNED;
+    // 4 arrival counters per tile, indexed by int
+    if ((static_cast<int64_t>(N) + 127) / 128 * ((M + 31) / 32) > (int64_t(1) << 29)) return QG_ERR_UNSUPPORTED_SHAPE;
+    DeviceInfo* d = device_info();
+    if (!d) return QG_ERR_CUDA;
+    if (K == 0) return launch_zero_rows(Y, ldy, M, N, stream) == cudaSuccess ? QG_OK : QG_ERR_CUDA;
+    const SchedEntry& se = cached_schedule(QG_KIND_W8A8, M, N, K, d->sms);
+    const Schedule s = se.s;
+    const size_t need = se.ws;
+    if (need > 0 && (!workspace || workspace_bytes_ < need || (reinterpret_cast<uintptr_t>(workspace) & 255u)))
+        return QG_ERR_WORKSPACE;
+    const CUtensorMap* tmW = cached_tmap(W, static_cast<uint64_t>(K), static_cast<uint64_t>(N), kMapFp8Weights);
+    if (!tmW) return QG_ERR_CUDA;
+    CUtensorMap tmX;
+    if (!make_tmap(&tmX, Xq, CU_TENSOR_MAP_DATA_TYPE_UINT8, static_cast<uint64_t>(K), static_cast<uint64_t>(M),
+                   static_cast<uint64_t>(ldxq), 128, 32))
+        return QG_ERR_CUDA;
+    W8a8Args a;
+    a.Sx = X_scale;
+    a.ldsx = ldsx;
+    a.S = W_scale;
+    a.Y = Y;
+    a.ldy = ldy;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.ws = need > 0 ? workspace : nullptr;
+    return launch_w8a8(a, s, *tmW, tmX, launch_ctl(d), stream) == cudaSuccess ? QG_OK : QG_ERR_CUDA;
 }
 
 qg_status qgemm_lut3(const void* X, int64_t ldx, const void* Wq, const void* qmap, const void* scales, void* Y,
@@ -675,9 +749,9 @@ qg_status qg_dequant_lut3(const void* Wq, const void* qmap, const void* scales, 
 
 qg_status qg_debug_schedule(int kind, int M, int N, int K, int* ctas, int64_t* ranges, int* info, int capacity,
                             cudaStream_t stream) {
-    if (kind != QG_KIND_FP8_BLOCK && kind != QG_KIND_LUT3 && kind != QG_KIND_BF16) return QG_ERR_INVALID_ARG;
-    if (M < 1 || M > 32 || N < 1 || K < 1 || !ctas) return QG_ERR_INVALID_ARG;
-    if (K % (kind == QG_KIND_FP8_BLOCK ? 16 : kind == QG_KIND_BF16 ? 8 : 128) != 0) return QG_ERR_UNSUPPORTED_SHAPE;
+    if (max_m(kind) == 0) return QG_ERR_INVALID_ARG;
+    if (M < 1 || M > max_m(kind) || N < 1 || K < 1 || !ctas) return QG_ERR_INVALID_ARG;
+    if (K % k_multiple(kind) != 0) return QG_ERR_UNSUPPORTED_SHAPE;
     DeviceInfo* d = device_info();
     if (!d) return QG_ERR_CUDA;
     const Schedule s = cached_schedule(kind, M, N, K, d->sms).s;
@@ -690,8 +764,8 @@ qg_status qg_debug_schedule(int kind, int M, int N, int K, int* ctas, int64_t* r
 }
 
 qg_status qg_dispatch_set(int kind, int M, int N, int K, int ctas) {
-    if (kind != QG_KIND_FP8_BLOCK && kind != QG_KIND_LUT3 && kind != QG_KIND_BF16) return QG_ERR_INVALID_ARG;
-    if (M < 1 || M > 32 || N < 1 || K < 1 || ctas < 0) return QG_ERR_INVALID_ARG;
+    if (max_m(kind) == 0) return QG_ERR_INVALID_ARG;
+    if (M < 1 || M > max_m(kind) || N < 1 || K < 1 || ctas < 0) return QG_ERR_INVALID_ARG;
     DeviceInfo* d = device_info();
     if (!d) return QG_ERR_CUDA;
     if (ctas > d->sms) return QG_ERR_INVALID_ARG;
@@ -716,8 +790,7 @@ qg_status qg_dispatch_set(int kind, int M, int N, int K, int ctas) {
 }
 
 int qg_dispatch_get(int kind, int M, int N, int K) {
-    if (kind != QG_KIND_FP8_BLOCK && kind != QG_KIND_LUT3 && kind != QG_KIND_BF16) return 0;
-    if (M < 1 || M > 32 || N < 1 || K < 1) return 0;
+    if (M < 1 || M > max_m(kind) || N < 1 || K < 1) return 0;
     DeviceInfo* d = device_info();
     if (!d) return 0;
     return cached_schedule(kind, M, N, K, d->sms).s.G;

@@ -47,7 +47,7 @@ import numpy as np
 __all__ = [
     "SEED_BASE", "seed_for", "uniform01", "normal", "uniform_codes", "bf16_bits_from_f32",
     "fp16_bits_from_f32", "e4m3_codes_from_f32", "Fp8Problem", "Lut3Problem", "Bf16Problem", "make_bf16_problem",
-    "make_fp8_problem", "make_lut3_problem", "lut3_qmap_bits", "WORKLOADS",
+    "make_fp8_problem", "make_w8a8_problem", "make_lut3_problem", "lut3_qmap_bits", "WORKLOADS",
 ]
 
 SEED_BASE = 0x51A7E000
@@ -182,6 +182,12 @@ class Bf16Problem:
     W: np.ndarray        # uint16 [N, K]  BF16 bits
 
 
+def make_w8a8_problem(M: int, N: int, K: int, config_id: int = 6) -> Fp8Problem:
+    """Inputs of the W8A8 path: the FP8 weight generator and BF16 N(0,1)
+    activations (quantised to E4M3 by the path itself)."""
+    return make_fp8_problem(M, N, K, config_id=config_id)
+
+
 def make_bf16_problem(M: int, N: int, K: int, config_id: int = 5, x_seed_tensor: int = 0,
                       w_seed_tensor: int = 1) -> Bf16Problem:
     w = (normal(seed_for(config_id, w_seed_tensor), N * K) * np.float32(0.02)).reshape(N, K)
@@ -218,4 +224,6 @@ WORKLOADS = {
     "fp8_attn_6144": ("fp8", 3, 6144, 5120, [1, 2, 4, 5, 8, 16, 17, 24, 32]),
     "lut3": ("lut3", 4, 28672, 8192, [1, 4, 8, 16]),
     "bf16_lm_head": ("bf16", 5, 32768, 5120, [1, 16, 32]),
+    # W8A8 beyond the decode tier: the gate/up layer at prefill batch sizes
+    "w8a8_gateup": ("w8a8", 6, 17408, 5120, [64, 128, 256, 512]),
 }
