@@ -440,6 +440,77 @@ class QkvCase:
         self.sets = self.X = self.Y = self.ws = None
 
 
+class W8a8Case:
+    """W8A8 at prefill batch sizes on the gate/up shape: E4M3 activations and
+    their scales resident (the quantiser timed on its own), weights rotated
+    over copies (>= 2x L2)."""
+
+    def __init__(self, torch, qg, M_max, N, K):
+        import workloads as wl
+        self.torch, self.qg, self.N, self.K = torch, qg, N, K
+        p = wl.make_w8a8_problem(M_max, N, K, config_id=6)
+        self.copies = -(-2 * L2_BYTES // (N * K)) + 1
+        self.W = [torch.from_numpy(p.W).cuda() for _ in range(self.copies)]
+        self.S = torch.from_numpy(p.S).cuda()
+        self.X = torch.from_numpy(p.X.view(np.int16)).view(torch.bfloat16).cuda()
+        self.ldsx = -(-M_max // 32) * 32
+        self.Xq = torch.empty((M_max, K), dtype=torch.uint8, device="cuda")
+        self.Sx = torch.empty((-(-K // 128), self.ldsx), dtype=torch.float32, device="cuda")
+        self.Y = torch.empty((M_max, N), dtype=torch.bfloat16, device="cuda")
+        self.ws = qg.Workspace()
+
+    def time(self, M, stream, steps, warmup, what="gemm"):
+        """what: "gemm" (qgemm_w8a8_block on resident codes), "quant"
+        (qg_quantize_act_e4m3) or "both" (the two launches of a call from
+        BF16 activations)."""
+        qg, N, K = self.qg, self.N, self.K
+        buf = self.ws.get(qg.workspace_bytes(qg.KIND_W8A8, M, N, K))
+        ws_ptr = buf.data_ptr() if buf is not None else None
+        ws_n = buf.numel() if buf is not None else 0
+        lib, sptr, copies, ldsx = qg.lib, stream.cuda_stream, self.copies, self.ldsx
+        xp, xqp, sxp, sp, yp = (self.X.data_ptr(), self.Xq.data_ptr(), self.Sx.data_ptr(), self.S.data_ptr(),
+                                self.Y.data_ptr())
+        wps = [w.data_ptr() for w in self.W]
+
+        def quant():
+            r = lib.qg_quantize_act_e4m3(xp, K, xqp, K, sxp, ldsx, M, K, sptr)
+            if r:
+                raise RuntimeError(qg.status_string(r))
+
+        def gemm(i):
+            r = lib.qgemm_w8a8_block(xqp, K, sxp, ldsx, wps[i % copies], sp, yp, N, M, N, K, ws_ptr, ws_n, sptr)
+            if r:
+                raise RuntimeError(qg.status_string(r))
+        quant()
+        if what == "gemm":
+            step = gemm
+        elif what == "quant":
+            def step(i):
+                quant()
+        else:
+            def step(i):
+                quant()
+                gemm(i)
+        ms = time_calls(self.torch, stream, step, steps, warmup)
+        st = qg.last_device_status(stream)
+        if st:
+            raise RuntimeError(f"device status {qg.status_string(st)}")
+        return ms
+
+    def free(self):
+        self.W = self.X = self.Xq = self.Sx = self.Y = self.ws = None
+
+
+def fp8_tensor_peak():
+    """FP8 dense tensor peak: the measured BF16 GEMM peak times the nominal
+    FP8 / BF16 ratio (4.5 / 2.25 PFLOP/s)."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]) * 2.0, "2 x measured bf16_tflops"
+    return 1900.0 * 2.0, "2 x fallback bf16"
+
+
 def secondary_lines(torch, qg, stream, peak, steps=2000, warmup=50, tune=True):
     """The other configurations (not the headline): us/call, GB/s, fraction
     of the HBM peak.  With `tune`, each shape first runs the library's
@@ -493,6 +564,19 @@ def secondary_lines(torch, qg, stream, peak, steps=2000, warmup=50, tune=True):
     for m in (1, 4, 8, 16):
         g = tuned(c, m)
         rec(f"lut3_M{m}", c.time(m, stream, steps, warmup), lut3_bytes(m, 28672, 8192), g)
+    c.free()
+    # W8A8 beyond the decode tier: tensor-bound, so its lines carry TFLOP/s
+    # against the FP8 tensor peak
+    tpeak, _ = fp8_tensor_peak()
+    c = W8a8Case(torch, qg, 1024, 17408, 5120)
+    for m in (64, 256, 1024):
+        flops = 2.0 * m * 17408 * 5120
+        for what in ("gemm", "both"):
+            ms = c.time(m, stream, max(50, steps // 20), warmup, what)
+            tf = flops / (ms * 1e-3) / 1e12
+            out[f"w8a8_gateup_M{m}_{what}"] = {"us": round(ms * 1e3, 3), "TFLOPs": round(tf, 1),
+                                               "frac_fp8_tensor": round(tf / tpeak, 4)}
+        out[f"w8a8_gateup_M{m}_quant"] = {"us": round(c.time(m, stream, max(50, steps // 20), warmup, "quant") * 1e3, 3)}
     c.free()
     qg.dispatch_clear()
     torch.cuda.empty_cache()
@@ -585,10 +669,12 @@ def main():
                     help="time the headline calls and print their line, nothing else (for profiling the kernel)")
     ap.add_argument("--overlap", type=int, choices=[0, 1], default=1,
                     help="launch with weight-prefetch overlap of consecutive calls (default 1)")
-    ap.add_argument("--only", choices=["lut3", "fp8_down_m32", "bf16", "fp8_attn_n5120_m16"], default=None,
+    ap.add_argument("--only", choices=["lut3", "fp8_down_m32", "bf16", "fp8_attn_n5120_m16", "w8a8_m256"],
+                    default=None,
                     help="time one secondary workload alone and print its line, for profiling its kernel: "
                          "lut3 = 3-bit LUT, M=16, N=28672, K=8192; fp8_down_m32 = FP8 M=32, N=5120, K=17408; "
-                         "bf16 = dense BF16, M=16, N=32768, K=5120; fp8_attn_n5120_m16 = FP8 M=16, N=5120, K=5120")
+                         "bf16 = dense BF16, M=16, N=32768, K=5120; fp8_attn_n5120_m16 = FP8 M=16, N=5120, K=5120; "
+                         "w8a8_m256 = W8A8 GEMM, M=256, N=17408, K=5120")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -620,6 +706,16 @@ def main():
             c = Bf16Case(torch, qg, 16, 32768, 5120)
             ms = c.time(16, stream, args.steps, args.warmup)
             nbytes, name = bf16_bytes(16, 32768, 5120), "bf16 M=16 N=32768 K=5120"
+        elif args.only == "w8a8_m256":
+            c = W8a8Case(torch, qg, 256, 17408, 5120)
+            ms = c.time(256, stream, args.steps, args.warmup)
+            tpeak, tkind = fp8_tensor_peak()
+            tf = 2.0 * 256 * 17408 * 5120 / (ms * 1e-3) / 1e12
+            print(json.dumps({"workload": "w8a8 gate/up M=256 N=17408 K=5120 (GEMM on resident E4M3 codes)",
+                              "us_per_call": round(ms * 1e3, 3), "TFLOPs": round(tf, 1),
+                              "frac": round(tf / tpeak, 4), "peak": tpeak, "peak_kind": tkind,
+                              "steps": args.steps, "warmup": args.warmup}))
+            return 0
         elif args.only == "fp8_attn_n5120_m16":
             c = Fp8Case(torch, qg, 16, 5120, 5120, 3)
             ms = c.time(16, stream, args.steps, args.warmup)

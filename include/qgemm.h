@@ -74,11 +74,14 @@ enum { QG_KIND_FP8_BLOCK = 0, QG_KIND_LUT3 = 1, QG_KIND_BF16 = 2, QG_KIND_W8A8 =
  * Bytes of device workspace a call of the given kind and shape needs on the
  * current device (0 if none).  The workspace holds split-K partial sums
  * (scratch, sized for the device's largest grid) followed by per-tile arrival
- * counters (the last 16 * tiles bytes, rounded up to 256; tiles = ceil(N/128),
- * times ceil(M/32) for QG_KIND_W8A8).  It must be
+ * counters (the last 16 * ceil(N/128) bytes, rounded up to 256; for
+ * QG_KIND_W8A8, R / 4 bytes for each of its ceil(N/128) * ceil(M/R) tiles,
+ * R = 64 for M <= 64, else 128).  It must be
  * zero-filled once before its first use; every successful call leaves its
  * counters at zero again, so one workspace serves later calls of any shape
- * without clearing.
+ * without clearing.  The W8A8 kind lays its workspace out differently (wider
+ * partial sums): a workspace serves either QG_KIND_W8A8 calls or calls of
+ * the other kinds, not both, unless it is zero-filled again in between.
  */
 size_t qg_workspace_bytes(int kind, int M, int N, int K);
 

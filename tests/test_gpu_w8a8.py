@@ -137,7 +137,8 @@ def test_w8a8_grids_agree_and_repeat():
     Xq, Sx = _quantized(p)
     W = torch.from_numpy(p.W).cuda()
     S = torch.from_numpy(p.S).cuda()
-    tiles = -(-N // 128) * -(-M // 32)
+    R = 64 if M <= 64 else 128           # activation rows per tile
+    tiles = -(-N // 128) * -(-M // R)
     ws = q.Workspace("cuda")
     try:
         for g in (tiles, 7, 64, 152, 45):
@@ -153,7 +154,7 @@ def test_w8a8_grids_agree_and_repeat():
             _grade(Xq, Sx, p.W, p.S, to_bits(Y1))
             need = q.workspace_bytes(q.KIND_W8A8, M, N, K)
             if need:
-                cnt = (16 * tiles + 255) // 256 * 256
+                cnt = (tiles * (R // 16) * 4 + 255) // 256 * 256
                 assert int(ws.buf[need - cnt:need].count_nonzero()) == 0
     finally:
         q.dispatch_clear()
@@ -191,3 +192,25 @@ def test_w8a8_zero_m_is_a_no_op():
     Y = q.qgemm_w8a8_block(Xq, Sx, W, S)
     assert Y.shape == (0, 128)
     assert q.last_device_status() == 0
+
+
+def test_w8a8_and_decode_calls_interleave():
+    """Split-K calls of the W8A8 kind (both tile widths) and of the FP8
+    decode kind, interleaved on the binding's default workspaces, all meet
+    the rule (each family keeps its arrival counters in its own buffer)."""
+    q = qg()
+    from gpu_util import Fp8Device, grade_fp8
+    pf = cached(("fp8il",), lambda: wl.make_fp8_problem(16, 1024, 5120, config_id=42))
+    dev = Fp8Device(pf)
+    shapes = [(48, 136, 5120), (200, 256, 5120)]
+    probs = [_problem(*sh) for sh in shapes]
+    mats = [(torch.from_numpy(p.W).cuda(), torch.from_numpy(p.S).cuda()) for p in probs]
+    for _ in range(2):
+        for p, (W, S) in zip(probs, mats):
+            Xq, Sx = _quantized(p)
+            Y = _run_gemm(q, Xq, Sx, W, S, p.N)
+            _grade(Xq, Sx, p.W, p.S, to_bits(Y))
+            Yf = dev.run()
+            assert q.last_device_status() == 0
+            ok, rep = grade_fp8(pf, to_bits(Yf))
+            assert rep.ok, rep

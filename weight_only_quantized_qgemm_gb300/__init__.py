@@ -170,7 +170,8 @@ def _workspace_for(kind, M, N, K, workspace, device):
     if need == 0:
         return None, 0
     if workspace is None:
-        workspace = _default_ws.setdefault(device, Workspace(device))
+        # the W8A8 kind's workspace layout differs from the decode kinds': one buffer each
+        workspace = _default_ws.setdefault((device, kind == KIND_W8A8), Workspace(device))
     buf = workspace.get(need) if isinstance(workspace, Workspace) else workspace
     return buf.data_ptr(), buf.numel() * buf.element_size()
 

@@ -146,9 +146,9 @@ int table_lookup(int kind, int M, int N, int K) {
 
 Schedule choose_schedule(int kind, int M, int N, int K, int sms) {
     Schedule s;
-    s.nmma = M <= 16 && kind != QG_KIND_W8A8 ? 16 : 32;
-    // W8A8 tiles are 128 weight rows x 32 activation rows, weight-tile-major
-    s.T = (N + 127) / 128 * (kind == QG_KIND_W8A8 ? (M + 31) / 32 : 1);
+    s.nmma = kind == QG_KIND_W8A8 ? w8a8_tile_rows(M) : M <= 16 ? 16 : 32;
+    // W8A8 tiles are 128 weight rows x nmma activation rows, weight-tile-major
+    s.T = (N + 127) / 128 * (kind == QG_KIND_W8A8 ? (M + s.nmma - 1) / s.nmma : 1);
     s.KU = (K + 127) / 128;   // one unit = 128 rows x one 128-wide K block
     s.U = static_cast<long long>(s.T) * s.KU;
     const int forced = table_lookup(kind, M, N, K);
@@ -202,7 +202,7 @@ const SchedEntry& cached_schedule(int kind, int M, int N, int K, int sms) {
     e.sms = sms;
     e.gen = gen;
     e.s = choose_schedule(kind, M, N, K, sms);
-    e.ws = workspace_bytes_uncached(e.s);
+    e.ws = kind == QG_KIND_W8A8 ? w8a8_workspace_bytes(e.s, schedule_splits(e.s)) : workspace_bytes_uncached(e.s);
     return e;
 }
 
@@ -286,7 +286,7 @@ void workspace_counters(int kind, int M, int N, int K, size_t* offset, size_t* b
     const Schedule& s = e.s;
     const size_t total = e.ws;
     if (total == 0) return;
-    *offset = workspace_partial_bytes(s);
+    *offset = kind == QG_KIND_W8A8 ? w8a8_partial_bytes(s) : workspace_partial_bytes(s);
     *bytes = total - *offset;
 }
 
@@ -609,7 +609,7 @@ qg_status qgemm_w8a8_block(const uint8_t* Xq, int64_t ldxq, const float* X_scale
     if (!tmW) return QG_ERR_CUDA;
     CUtensorMap tmX;
     if (!make_tmap(&tmX, Xq, CU_TENSOR_MAP_DATA_TYPE_UINT8, static_cast<uint64_t>(K), static_cast<uint64_t>(M),
-                   static_cast<uint64_t>(ldxq), 128, 32))
+                   static_cast<uint64_t>(ldxq), 128, static_cast<uint32_t>(s.nmma)))
         return QG_ERR_CUDA;
     W8a8Args a;
     a.Sx = X_scale;

@@ -1,30 +1,36 @@
 // W8A8 block-scaled GEMM for sm_103a: FP8 activations as well as FP8
 // weights, for batches beyond the decode tier ("arc" PR page, the cuBLASLt
-// block-scale section: block-scaled FP8 needs FP8 activations, hence an
+// block-scale section: block-scaled FP8 takes FP8 activations, hence an
 // activation quantiser).
 //
 //   Xq, sx = quantise(X):  per (row m, 128-wide K block kb)
 //            sx[kb, m] = amax / 448,  xq = e4m3_rne_satfinite(x / sx)
 //   Y[m, n] = bf16( sum_kb (sx[kb, m] * s[n/128, kb]) * (sum_{k in kb} xq[m,k] * w[n,k]) )
 //
-// The GEMM tiles the output in 128 weight rows x 32 activation rows; a unit
-// is one such tile x one 128-wide K block.  Both operands go to
-// tcgen05.mma kind::f8f6f4 as stored (TMA, 128-byte swizzle); each unit's
-// block sum lands in its own TMEM accumulator and the fold multiplies it by
-// the unit's 32 block factors (activation scale x weight scale) once and adds
-// it to an FP32 outer accumulator in registers: the same two-level fold as
-// the W8A16 path.  Tiles are numbered weight-tile-major (the row blocks of a
-// weight tile are neighbours, so its weights are read from HBM once and from
-// L2 after); the stream-K split and the split-K partial sums are the shared
-// ones of qg_gemm.cuh.
+// The GEMM tiles the output in 128 weight rows x NA activation rows (NA = 64
+// or 128: the MMA's N side); a unit is one tile x one 128-wide K block.  Both
+// operands go to tcgen05.mma kind::f8f6f4 as stored (TMA, 128-byte swizzle).
+// Each unit's block sums land in their own TMEM accumulator; the fold
+// multiplies them by the unit's NA block factors (activation scale x weight
+// scale) once and adds them to FP32 outer sums held in registers: the
+// two-level fold of the W8A16 path.  Tiles are numbered weight-tile-major, so
+// the activation-row blocks of a weight tile are neighbours and its weights
+// come from L2 after the first read.  Work units are split evenly over the
+// CTAs (stream-K), a tile shared by several CTAs being summed by the last to
+// arrive, as in the decode kernels, with partial sums kept per fold warp.
 //
-// One persistent CTA per SM, 256 threads:
-//   warp 0      weight producer: one 16 KB TMA tile per unit (evict-first).
+// One persistent CTA per SM, 4 + NA/16 warps:
+//   warp 0      weight producer: one 16 KB TMA tile per unit.
 //   warp 1      activation producer, after the grid dependency wait: the
-//               unit's 32 x 128 E4M3 slice (TMA) and its 32 activation scales
-//               (one 128-byte bulk copy) into a ring.
-//   warp 2      MMA issuer: 4 tcgen05.mma (M = 128, N = 32, K = 32) per unit.
-//   warps 4-7   fold / epilogue, one per TMEM lane quadrant.
+//               unit's NA x 128 E4M3 slice (TMA) and its NA activation scales
+//               (one bulk copy) into a ring.
+//   warp 2      MMA issuer: 4 tcgen05.mma (M = 128, N = NA, K = 32) per unit.
+//   warp 3      factor warp: turns the unit's activation scales into block
+//               factors (times the unit's weight scale, fetched 32 units
+//               ahead, one unit per lane) in a ring of its own, so that an
+//               activation slot is free again as soon as its MMAs complete.
+//   warps 4-    fold / epilogue: NA/16 warps, warp w reading TMEM lane
+//               quadrant w % 4 and 64 of the NA columns.
 #include "qg_gemm.cuh"
 #include "qg_w8a8.h"
 
@@ -34,101 +40,193 @@ namespace {
 using gemm::Cursor;
 using gemm::Params;
 
-constexpr int kNA = 32;          // activation rows per output tile (MMA N)
-constexpr int kThreads = 256;
-constexpr int kWarpWProd = 0, kWarpXProd = 1, kWarpMma = 2, kWarpFold0 = 4;
+constexpr int kWarpWProd = 0, kWarpXProd = 1, kWarpMma = 2, kWarpFactor = 3, kWarpFold0 = 4;
+constexpr int kFoldCols = 64;   // activation rows (MMA columns) per fold warp
 
+template <int NA>
 struct W8a8Layout {
-    static constexpr int kWBytes = 128 * 128;      // one E4M3 weight unit
-    static constexpr int kXBytes = kNA * 128;      // one E4M3 activation slice
-    static constexpr int kXSlot = kXBytes + 1024;  // + 32 scales (128 B), padded to keep 1024-B alignment
-    static constexpr int kXStages = 12;
-    static constexpr int kAcc = 8;                 // TMEM accumulators of kNA columns
-    static constexpr int kTmemCols = kAcc * kNA;   // 256
-    static constexpr int kFixed = kXStages * kXSlot + 8 * (2 * 16 + 2 * kXStages + 2 * kAcc) + 64 + 1024;
-    static constexpr int kWFit = (232448 - kFixed) / kWBytes;
+    static constexpr int kFold = NA / 16;                     // fold warps: 4 quadrants x NA/64 column halves
+    static constexpr int kThreads = 32 * (kWarpFold0 + kFold);
+    static constexpr int kWBytes = 128 * 128;                 // one E4M3 weight unit
+    static constexpr int kXBytes = NA * 128;                  // one E4M3 activation slice
+    static constexpr int kXSlot = kXBytes + 1024;             // + NA scales, padded to keep 1024-B alignment
+    static constexpr int kXStages = NA == 128 ? 6 : 10;
+    static constexpr int kAcc = 512 / NA;                     // TMEM accumulators
+    static constexpr int kGStages = 2 * kAcc;                 // factor ring (NA floats a slot)
+    static constexpr int kReserve = kGStages * NA * 4 + 8 * 96 + 64 + 1024;   // + barriers, misc, alignment
+    static constexpr int kWFit = (232448 - kXStages * kXSlot - kReserve) / kWBytes;
     static constexpr int kWStages = kWFit < 12 ? kWFit : 12;
     static constexpr int kXOff = kWStages * kWBytes;
-    static constexpr int kBarOff = kXOff + kXStages * kXSlot;
-    static constexpr int kNumBars = 2 * kWStages + 2 * kXStages + 2 * kAcc;
+    static constexpr int kGOff = kXOff + kXStages * kXSlot;
+    static constexpr int kBarOff = kGOff + kGStages * NA * 4;
+    static constexpr int kNumBars = 2 * kWStages + 2 * kXStages + 2 * kGStages + 2 * kAcc;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     static constexpr int kSmemBytes = kMiscOff + 64 + 1024;
-    static_assert(kWStages >= 8, "weight ring");
+    // the final split-K reduction stages pieces in both idle operand rings:
+    // per fold warp, pieces of 32 rows x 64 columns of FP32
+    static constexpr int kPieceBytes = 32 * kFoldCols * 4;
+    static constexpr int kScratchWarp = kGOff / kFold / kPieceBytes * kPieceBytes;
+    static_assert(kNumBars <= 96, "barrier area");
+    static_assert(kWStages >= 6, "weight ring");
     static_assert(kXOff % 1024 == 0 && kXSlot % 1024 == 0, "keep the 1024-byte swizzle alignment");
-    static_assert(kWStages * kWBytes >= 4 * gemm::scratch_quadrant<kNA>(), "reduction scratch in the weight ring");
+    static_assert(kScratchWarp >= 2 * kPieceBytes, "reduction scratch");
     static_assert(kSmemBytes <= 232448, "shared memory");
+    static_assert(NA <= kMaxTileRows, "workspace slots");
 };
 
+// Workspace: partial sums [G][2 slots][NA/4 column groups][128 rows] float4
+// (slots sized for the widest tile, so that the counters behind them sit at
+// one offset for every W8A8 shape), then one arrival counter per (tile, fold
+// warp).
+template <int NA>
+__device__ __forceinline__ float4* part_slot(const Params& p, int cta, int which) {
+    return reinterpret_cast<float4*>(p.part) + (static_cast<size_t>(cta) * 2 + which) * (NA / 4) * 128;
+}
+
 // Output rows of tile t = (weight tile tn, activation row block tm), t = tn *
-// tm_count + tm: weight row n = tn * 128 + row, activation rows tm * 32 ...
-__device__ __forceinline__ void store_tile_rows(const Params& p, int tm_count, int tile, int row,
-                                                const float (&v)[kNA]) {
+// tm_count + tm: weight row n = tn * 128 + row, activation rows tm * NA + h *
+// 64 + j for the fold warp's column half h.
+template <int NA>
+__device__ __forceinline__ void store_cols(const Params& p, int tm_count, int tile, int row, int h,
+                                           const float (&v)[kFoldCols]) {
     const int tn = tile / tm_count;
-    const int m0 = (tile - tn * tm_count) * kNA;
+    const int m0 = (tile - tn * tm_count) * NA + h * kFoldCols;
     const int n = tn * 128 + row;
     if (n >= p.N) return;
     const gemm::Seg sg = p.seg[0];
+    __nv_bfloat16* Y = static_cast<__nv_bfloat16*>(sg.Y);
 #pragma unroll
-    for (int m = 0; m < kNA; ++m)
-        if (m0 + m < p.M)
-            static_cast<__nv_bfloat16*>(sg.Y)[static_cast<int64_t>(m0 + m) * sg.ldy + n] = __float2bfloat16_rn(v[m]);
+    for (int j = 0; j < kFoldCols; ++j)
+        if (m0 + j < p.M) Y[static_cast<int64_t>(m0 + j) * sg.ldy + n] = __float2bfloat16_rn(v[j]);
 }
 
-// Sum of a split tile's pieces (staged through idle shared memory) and its
-// store; resets the tile's arrival counter.
+// Sum of a split tile's pieces for the fold warp's 32 rows x 64 columns, in
+// ascending piece order, staged through idle shared memory (batches of
+// pieces copied by 16-byte cp.async before any is read back), then stored;
+// resets the warp's arrival counter.
+template <int NA>
 __device__ __forceinline__ void finish_tile(const Params& p, int tm_count, int tile, int which, int split_info,
-                                            int q, int lane, uint8_t* scratch) {
+                                            int q, int h, int fw, int lane, uint8_t* scratch) {
+    using L = W8a8Layout<NA>;
+    constexpr int kF4 = kFoldCols / 4;
+    constexpr int kPieces = L::kScratchWarp / L::kPieceBytes;
     const int row = q * 32 + lane;
     const int cf = __shfl_sync(0xffffffffu, split_info, 3 * which);
     const int cl = __shfl_sync(0xffffffffu, split_info, 3 * which + 1);
     const int w_first = __shfl_sync(0xffffffffu, split_info, 3 * which + 2);
-    float acc[kNA];
-    gemm::sum_pieces_staged<kNA>(p, row, lane, q, cf, cl, w_first, scratch, acc);
-    store_tile_rows(p, tm_count, tile, row, acc);
+    const float4* mine = reinterpret_cast<const float4*>(scratch + fw * L::kScratchWarp) + lane;
+    const uint32_t sq = smem_u32(mine);
+    float acc[kFoldCols];
+#pragma unroll
+    for (int j = 0; j < kFoldCols; ++j) acc[j] = 0.0f;
+    for (int c0 = cf; c0 <= cl; c0 += kPieces) {
+        const int nb = cl - c0 + 1 < kPieces ? cl - c0 + 1 : kPieces;
+#pragma unroll 1
+        for (int b = 0; b < nb; ++b) {
+            const int c2 = c0 + b;
+            const float4* src = part_slot<NA>(p, c2, c2 == cf ? w_first : 0) + h * kF4 * 128 + row;
+#pragma unroll
+            for (int g = 0; g < kF4; ++g) cp_async_16(sq + (b * kF4 + g) * 512, src + g * 128, 16u);
+        }
+        cp_async_commit();
+        cp_async_wait<0>();   // the lane reads back only what it copied
+#pragma unroll 1
+        for (int b = 0; b < nb; ++b) {
+#pragma unroll
+            for (int g = 0; g < kF4; ++g) {
+                const float4 x = mine[(b * kF4 + g) * 32];
+                acc[4 * g + 0] = __fadd_rn(acc[4 * g + 0], x.x);
+                acc[4 * g + 1] = __fadd_rn(acc[4 * g + 1], x.y);
+                acc[4 * g + 2] = __fadd_rn(acc[4 * g + 2], x.z);
+                acc[4 * g + 3] = __fadd_rn(acc[4 * g + 3], x.w);
+            }
+        }
+    }
+    store_cols<NA>(p, tm_count, tile, row, h, acc);
     __syncwarp();
-    if (lane == 0) p.cnt[tile * 4 + q] = 0u;
+    if (lane == 0) p.cnt[tile * L::kFold + fw] = 0u;   // ready for the next call
 }
 
-// End of a CTA's piece of `tile`, as gemm::end_piece with this kernel's
-// tile-to-output mapping: a whole tile is stored; a split piece is stored to
-// the workspace and counted; the last to arrive finishes the tile now when
-// `scratch` is given, else returns true (finished at the end of the range).
-__device__ __forceinline__ bool end_piece(const Params& p, int tm_count, const float (&outer)[kNA], int tile, int kb,
-                                          long long u, long long u0, int first_tile, int split_info, int q, int lane,
-                                          uint8_t* scratch) {
+// End of a CTA's piece of `tile` for one fold warp.  A whole tile is stored;
+// a split piece is stored to the workspace and counted; the last to arrive
+// finishes the tile now when `scratch` is given, else returns true (finished
+// at the end of the range, when shared memory is idle).
+template <int NA>
+__device__ __forceinline__ bool end_piece(const Params& p, int tm_count, const float (&outer)[kFoldCols], int tile,
+                                          int kb, long long u, long long u0, int first_tile, int split_info, int q,
+                                          int h, int fw, int lane, uint8_t* scratch) {
+    using L = W8a8Layout<NA>;
     const int row = q * 32 + lane;
     const bool whole = (kb == p.KB - 1) && (u - kb >= u0);
     if (whole) {
-        store_tile_rows(p, tm_count, tile, row, outer);
+        store_cols<NA>(p, tm_count, tile, row, h, outer);
         return false;
     }
     const int which = (tile == first_tile) ? 0 : 1;
-    float4* mine = gemm::slot_base<kNA>(p, blockIdx.x, which) + row;
+    float4* mine = part_slot<NA>(p, blockIdx.x, which) + h * (kFoldCols / 4) * 128 + row;
 #pragma unroll
-    for (int g = 0; g < kNA / 4; ++g)
+    for (int g = 0; g < kFoldCols / 4; ++g)
         __stcg(mine + g * 128, make_float4(outer[4 * g], outer[4 * g + 1], outer[4 * g + 2], outer[4 * g + 3]));
     // every lane's partial visible GPU-wide before lane 0's arrival
     __threadfence();
     __syncwarp();
     uint32_t prev = 0;
-    if (lane == 0) prev = atomicAdd(p.cnt + tile * 4 + q, 1u);
+    if (lane == 0) prev = atomicAdd(p.cnt + tile * L::kFold + fw, 1u);
     prev = __shfl_sync(0xffffffffu, prev, 0);
     const int cf = __shfl_sync(0xffffffffu, split_info, 3 * which);
     const int cl = __shfl_sync(0xffffffffu, split_info, 3 * which + 1);
     if (static_cast<int>(prev) != cl - cf) return false;
     __threadfence();
     if (scratch == nullptr) return true;
-    finish_tile(p, tm_count, tile, which, split_info, q, lane, scratch);
+    finish_tile<NA>(p, tm_count, tile, which, split_info, q, h, fw, lane, scratch);
     return false;
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+// Position of a running unit: its Cursor, its tile's (weight tile tn,
+// activation row block tm) and the number of activation scales the block's
+// copy takes (nsc), stepped without divisions.
+template <int NA>
+struct UnitPosT {
+    Cursor c;
+    int tn, tm, nsc;
+    __device__ UnitPosT(long long u, int KB, int tm_count, int64_t ldsx) : c(u, KB) {
+        tn = c.tile / tm_count;
+        tm = c.tile - tn * tm_count;
+        nsc = count(ldsx);
+    }
+    __device__ int count(int64_t ldsx) const {
+        const int64_t left = ldsx - static_cast<int64_t>(tm) * NA;
+        return left < NA ? static_cast<int>(left) : NA;
+    }
+    __device__ void next_tile(int tm_count, int64_t ldsx) {
+        if (++tm == tm_count) {
+            tm = 0;
+            ++tn;
+        }
+        nsc = count(ldsx);
+    }
+    __device__ void step(int KB, int tm_count, int64_t ldsx) {
+        c.step(KB);
+        if (c.kb == 0) next_tile(tm_count, ldsx);
+    }
+    __device__ void advance(int n, int KB, int tm_count, int64_t ldsx) {
+        const int t0 = c.tile;
+        c.step(n, KB);
+        for (int t = t0; t < c.tile; ++t) next_tile(tm_count, ldsx);
+    }
+};
+
+template <int NA>
+__global__ void __launch_bounds__(W8a8Layout<NA>::kThreads, 1)
     w8a8_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, const Params p,
                 const float* __restrict__ sx, int64_t ldsx, int tm_count) {
-    using L = W8a8Layout;
+    using L = W8a8Layout<NA>;
+    using UnitPos = UnitPosT<NA>;
     constexpr int kWStages = L::kWStages;
     constexpr int kXStages = L::kXStages;
     constexpr int kAcc = L::kAcc;
+    constexpr int kFold = L::kFold;
+    constexpr int kGStages = L::kGStages;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -139,11 +237,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto wempty = [&](int s) { return bar0 + 8u * (kWStages + s); };
     auto xfull = [&](int s) { return bar0 + 8u * (2 * kWStages + s); };
     auto xempty = [&](int s) { return bar0 + 8u * (2 * kWStages + kXStages + s); };
-    constexpr int kBarD = 2 * kWStages + 2 * kXStages;
+    constexpr int kBarG = 2 * kWStages + 2 * kXStages;
+    auto gready = [&](int j) { return bar0 + 8u * (kBarG + j); };
+    auto gempty = [&](int j) { return bar0 + 8u * (kBarG + kGStages + j); };
+    constexpr int kBarD = kBarG + 2 * kGStages;
     auto dfull = [&](int a) { return bar0 + 8u * (kBarD + a); };
     auto dempty = [&](int a) { return bar0 + 8u * (kBarD + kAcc + a); };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + L::kMiscOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + L::kMiscOff + 4);
+    auto scales_at = [&](int s) {
+        return reinterpret_cast<const float*>(gbase + L::kXOff + s * L::kXSlot + L::kXBytes);
+    };
+    auto factors_at = [&](int j) { return reinterpret_cast<float*>(gbase + L::kGOff + j * NA * 4); };
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -159,17 +264,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int s = 0; s < kXStages; ++s) {
             mbar_init(xfull(s), 1);
-            mbar_init(xempty(s), 1 + 4);   // the MMA commit and the four fold warps (scales read)
+            mbar_init(xempty(s), 2);   // the MMA commit and the factor warp (scales read)
+        }
+        for (int j = 0; j < kGStages; ++j) {
+            mbar_init(gready(j), 1);       // the factor warp
+            mbar_init(gempty(j), kFold);   // every fold warp
         }
         for (int a = 0; a < kAcc; ++a) {
             mbar_init(dfull(a), 1);
-            mbar_init(dempty(a), 4);
+            mbar_init(dempty(a), kFold);
         }
         *abort_flag = 0;
         fence_barrier_init();
     }
     __syncwarp();
-    if (warp == 0) tmem_alloc(smem_u32(tmem_slot), L::kTmemCols);
+    if (warp == 0) tmem_alloc(smem_u32(tmem_slot), 512);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -177,21 +286,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     const WaitCtl wc{p.timeout_ns, p.status, abort_flag};
     grid_dependents_launch();
 
+    // Every role runs one iteration per unit, and a unit's four MMAs take
+    // only a few hundred cycles: the loops avoid divisions (rings and tile
+    // coordinates are stepped incrementally).  The producers and the factor
+    // and fold warps wait in one lane; the MMA warp waits as a whole and
+    // issues from one elected lane (issuing from a lone diverged lane
+    // measured about 15% slower).
     if (warp == kWarpWProd) {
         // ------------------------------------------------------------ weight producer
         if (lane == 0) {
             prefetch_tmap(&tmW);
-            const uint64_t pol_w = policy_evict_first();
+            // a weight tile serves tm_count tiles in a row: keep it for their re-reads
+            const uint64_t pol_w = tm_count > 1 ? policy_evict_last() : policy_evict_first();
             int issued = 0;
-            Cursor cur(u0, p.KB);
-            for (int i = 0; i < nunits; ++i, cur.step(p.KB)) {
-                const int s = i % kWStages;
-                if (i >= kWStages && !wait_bounded(wempty(s), ((i / kWStages) - 1) & 1, wc)) break;
-                if (cta == 0 && i == p.fault_unit) continue;   // failure-path test hook
-                const int tn = cur.tile / tm_count;
-                mbar_arrive_expect_tx(wfull(s), L::kWBytes);
-                tma_load_2d(base + s * L::kWBytes, &tmW, wfull(s), cur.kr * 128, tn * 128, pol_w);
+            UnitPos up(u0, p.KB, tm_count, ldsx);
+            gemm::Ring<kWStages> rw(0);
+            for (int i = 0; i < nunits; ++i, up.step(p.KB, tm_count, ldsx), rw.step(1)) {
+                if (i >= kWStages && !wait_bounded(wempty(rw.slot), rw.phase ^ 1u, wc)) break;
                 issued = i + 1;
+                if (cta == 0 && i == p.fault_unit) continue;   // failure-path test hook
+                mbar_arrive_expect_tx(wfull(rw.slot), L::kWBytes);
+                tma_load_2d(base + rw.slot * L::kWBytes, &tmW, wfull(rw.slot), up.c.kr * 128, up.tn * 128, pol_w);
             }
             for (int i = issued - kWStages < 0 ? 0 : issued - kWStages; i < issued; ++i) {
                 if (cta == 0 && i == p.fault_unit) continue;
@@ -206,16 +321,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             grid_dependency_wait();
             const uint64_t pol_x = policy_evict_last();
             int issued = 0;
-            Cursor cur(u0, p.KB);
-            for (int i = 0; i < nunits; ++i, cur.step(p.KB)) {
-                const int s = i % kXStages;
-                if (i >= kXStages && !wait_bounded(xempty(s), ((i / kXStages) - 1) & 1, wc)) break;
-                const int tm = cur.tile - (cur.tile / tm_count) * tm_count;
-                const uint32_t dst = base + L::kXOff + s * L::kXSlot;
-                mbar_arrive_expect_tx(xfull(s), L::kXBytes + kNA * 4);
-                tma_load_2d(dst, &tmX, xfull(s), cur.kr * 128, tm * kNA, pol_x);
-                bulk_load(dst + L::kXBytes, sx + static_cast<int64_t>(cur.kr) * ldsx + tm * kNA, kNA * 4, xfull(s),
-                          pol_x);
+            UnitPos up(u0, p.KB, tm_count, ldsx);
+            gemm::Ring<kXStages> rx(0);
+            for (int i = 0; i < nunits; ++i, up.step(p.KB, tm_count, ldsx), rx.step(1)) {
+                if (i >= kXStages && !wait_bounded(xempty(rx.slot), rx.phase ^ 1u, wc)) break;
+                const uint32_t dst = base + L::kXOff + rx.slot * L::kXSlot;
+                mbar_arrive_expect_tx(xfull(rx.slot), L::kXBytes + up.nsc * 4);
+                tma_load_2d(dst, &tmX, xfull(rx.slot), up.c.kr * 128, up.tm * NA, pol_x);
+                bulk_load(dst + L::kXBytes, sx + static_cast<int64_t>(up.c.kr) * ldsx + static_cast<int64_t>(up.tm) * NA,
+                          up.nsc * 4, xfull(rx.slot), pol_x);
                 issued = i + 1;
             }
             for (int i = issued - kXStages < 0 ? 0 : issued - kXStages; i < issued; ++i)
@@ -224,90 +338,149 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == kWarpMma) {
         // ------------------------------------------------------------ MMA issuer
         const bool elected = elect_one();
-        constexpr uint32_t idesc = idesc_f8_e4m3(kNA);
+        constexpr uint32_t idesc = idesc_f8_e4m3(NA);
         const uint64_t dw0 = smem_desc_sw128(base);
         const uint64_t dx0 = smem_desc_sw128(base + L::kXOff);
+        gemm::Ring<kWStages> rw(0);
+        gemm::Ring<kXStages> rx(0);
+        gemm::Ring<kAcc> ra(0);
         int last = -1;
-        for (int i = 0; i < nunits; ++i) {
-            const int sw = i % kWStages;
-            const int sx_ = i % kXStages;
-            const int a = i % kAcc;
-            if (!gemm::warp_wait(wfull(sw), (i / kWStages) & 1, wc)) break;
-            if (!gemm::warp_wait(xfull(sx_), (i / kXStages) & 1, wc)) break;
-            if (i >= kAcc && !gemm::warp_wait(dempty(a), ((i / kAcc) - 1) & 1, wc)) break;
+        for (int i = 0; i < nunits; ++i, rw.step(1), rx.step(1), ra.step(1)) {
+            if (!gemm::warp_wait(wfull(rw.slot), rw.phase, wc)) break;
+            if (!gemm::warp_wait(xfull(rx.slot), rx.phase, wc)) break;
+            if (i >= kAcc && !gemm::warp_wait(dempty(ra.slot), ra.phase ^ 1u, wc)) break;
             tc_fence_after();
-            const uint64_t ad = dw0 + static_cast<uint64_t>((sw * L::kWBytes) >> 4);
-            const uint64_t bd = dx0 + static_cast<uint64_t>((sx_ * L::kXSlot) >> 4);
+            const uint64_t ad = dw0 + static_cast<uint64_t>((rw.slot * L::kWBytes) >> 4);
+            const uint64_t bd = dx0 + static_cast<uint64_t>((rx.slot * L::kXSlot) >> 4);
             if (elected) {
 #pragma unroll
-                for (int j = 0; j < 4; ++j) mma_ss_f8(tmem + a * kNA, ad + 2 * j, bd + 2 * j, idesc, j > 0 ? 1u : 0u);
-                tc_commit(wempty(sw));
-                tc_commit(xempty(sx_));
-                tc_commit(dfull(a));
+                for (int j = 0; j < 4; ++j)
+                    mma_ss_f8(tmem + ra.slot * NA, ad + 2 * j, bd + 2 * j, idesc, j > 0 ? 1u : 0u);
+                tc_commit(wempty(rw.slot));
+                tc_commit(xempty(rx.slot));
+                tc_commit(dfull(ra.slot));
             }
             __syncwarp();
             last = i;
         }
         if (last >= 0 && elected) gemm::drain_wait(dfull(last % kAcc), (last / kAcc) & 1, p.timeout_ns);
-    } else if (warp >= kWarpFold0) {
+    } else if (warp == kWarpFactor) {
+        // ------------------------------------------------------------ block factors
+        // Lane l fetches the weight scale of unit i0 + l one batch of 32 units
+        // ahead of its use, so that no unit waits for a global load.
+        UnitPos bp(u0, p.KB, tm_count, ldsx);   // the first unit of the batch fetched next
+        auto fetch = [&](int i0) {
+            float v = 0.0f;
+            if (i0 + lane < nunits) {
+                UnitPos mine = bp;
+                mine.advance(lane, p.KB, tm_count, ldsx);
+                v = __ldg(p.S + static_cast<int64_t>(mine.tn) * p.lds + mine.c.kr);
+            }
+            bp.advance(32, p.KB, tm_count, ldsx);
+            return v;
+        };
+        float sw_now = fetch(0);
+        float sw_next = fetch(32);
+        UnitPos up(u0, p.KB, tm_count, ldsx);
+        gemm::Ring<kXStages> rx(0);
+        gemm::Ring<kGStages> rg(0);
+        for (int i = 0; i < nunits; ++i, up.step(p.KB, tm_count, ldsx), rx.step(1), rg.step(1)) {
+            if (i > 0 && (i & 31) == 0) {
+                sw_now = sw_next;
+                sw_next = fetch(i + 32);
+            }
+            bool ok = true;
+            if (lane == 0) {
+                ok = wait_bounded(xfull(rx.slot), rx.phase, wc);
+                if (ok && i >= kGStages) ok = wait_bounded(gempty(rg.slot), rg.phase ^ 1u, wc);
+            }
+            if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+            __syncwarp();   // orders the other lanes' reads after lane 0's wait
+            const float sw = __shfl_sync(0xffffffffu, sw_now, i & 31);
+            const float* sc = scales_at(rx.slot);
+            float* f = factors_at(rg.slot);
+#pragma unroll
+            for (int c = 0; c < NA / 32; ++c) {
+                const int m = c * 32 + lane;
+                f[m] = m < up.nsc ? __fmul_rn(sc[m], sw) : 0.0f;
+            }
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(xempty(rx.slot));
+                mbar_arrive(gready(rg.slot));
+            }
+        }
+    } else {
         // ------------------------------------------------------------ fold / epilogue
-        const int q = warp & 3;
-        const uint32_t tl = tmem + (static_cast<uint32_t>(q * 32) << 16);
+        const int fw = warp - kWarpFold0;   // 0 .. kFold-1
+        const int q = warp & 3;             // TMEM lane quadrant of this warp
+        const int h = fw >> 2;              // column half
+        const uint32_t tl = tmem + (static_cast<uint32_t>(q * 32) << 16) + h * kFoldCols;
         const int first_tile = static_cast<int>(u0 / p.KB);
         const int split_info = gemm::split_info_lane(p, u0, u1, lane);
         // Y and the workspace may still be in use by the preceding grid
         grid_dependency_wait();
         bool deferred = false;
-        float outer[kNA];
+        float outer[kFoldCols];
 #pragma unroll
-        for (int m = 0; m < kNA; ++m) outer[m] = 0.0f;
+        for (int j = 0; j < kFoldCols; ++j) outer[j] = 0.0f;
         Cursor cur(u0, p.KB);
-        for (int i = 0; i < nunits; ++i, cur.step(p.KB)) {
-            const int a = i % kAcc;
-            const int sx_ = i % kXStages;
-            // the unit's weight block scale (one per 128 x 128 block)
-            const int tn = cur.tile / tm_count;
-            const float sw = __ldg(p.S + static_cast<int64_t>(tn) * p.lds + cur.kr);
-            if (!gemm::warp_wait(dfull(a), (i / kAcc) & 1, wc)) break;
-            // the scales came with the slice (async proxy): observe its barrier too
-            if (!gemm::warp_wait(xfull(sx_), (i / kXStages) & 1, wc)) break;
-            tc_fence_after();
-            uint32_t v0[16], v1[16];
-            tmem_ld_x16(tl + a * kNA, v0);
-            tmem_ld_x16(tl + a * kNA + 16, v1);
-            // the unit's activation scales, one per row of the block
-            const float4* f4 = reinterpret_cast<const float4*>(gbase + L::kXOff + sx_ * L::kXSlot + L::kXBytes);
-            float f[kNA];
-#pragma unroll
-            for (int j = 0; j < kNA / 4; ++j) {
-                const float4 t = f4[j];
-                f[4 * j] = t.x;
-                f[4 * j + 1] = t.y;
-                f[4 * j + 2] = t.z;
-                f[4 * j + 3] = t.w;
+        gemm::Ring<kAcc> ra(0);
+        gemm::Ring<kGStages> rg(0);
+        for (int i = 0; i < nunits; ++i, cur.step(p.KB), ra.step(1), rg.step(1)) {
+            bool ok = true;
+            if (lane == 0) {
+                ok = wait_bounded(dfull(ra.slot), ra.phase, wc);
+                if (ok) ok = wait_bounded(gready(rg.slot), rg.phase, wc);
             }
-            tmem_wait_ld();
+            if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+            __syncwarp();   // orders the other lanes' reads after lane 0's wait
+            tc_fence_after();
+            const float4* f4 = reinterpret_cast<const float4*>(factors_at(rg.slot) + h * kFoldCols);
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                uint32_t v0[16], v1[16];
+                tmem_ld_x16(tl + ra.slot * NA + 32 * c, v0);
+                tmem_ld_x16(tl + ra.slot * NA + 32 * c + 16, v1);
+                tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float4 g0 = f4[8 * c + e];
+                    const float4 g1 = f4[8 * c + 4 + e];
+                    float* o = outer + 32 * c;
+                    o[4 * e + 0] = __fmaf_rn(__uint_as_float(v0[4 * e + 0]), g0.x, o[4 * e + 0]);
+                    o[4 * e + 1] = __fmaf_rn(__uint_as_float(v0[4 * e + 1]), g0.y, o[4 * e + 1]);
+                    o[4 * e + 2] = __fmaf_rn(__uint_as_float(v0[4 * e + 2]), g0.z, o[4 * e + 2]);
+                    o[4 * e + 3] = __fmaf_rn(__uint_as_float(v0[4 * e + 3]), g0.w, o[4 * e + 3]);
+                    o[16 + 4 * e + 0] = __fmaf_rn(__uint_as_float(v1[4 * e + 0]), g1.x, o[16 + 4 * e + 0]);
+                    o[16 + 4 * e + 1] = __fmaf_rn(__uint_as_float(v1[4 * e + 1]), g1.y, o[16 + 4 * e + 1]);
+                    o[16 + 4 * e + 2] = __fmaf_rn(__uint_as_float(v1[4 * e + 2]), g1.z, o[16 + 4 * e + 2]);
+                    o[16 + 4 * e + 3] = __fmaf_rn(__uint_as_float(v1[4 * e + 3]), g1.w, o[16 + 4 * e + 3]);
+                }
+            }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
-                mbar_arrive(dempty(a));
-                mbar_arrive(xempty(sx_));
+                mbar_arrive(dempty(ra.slot));
+                mbar_arrive(gempty(rg.slot));
             }
-#pragma unroll
-            for (int m = 0; m < 16; ++m) {
-                outer[m] = __fmaf_rn(__uint_as_float(v0[m]), __fmul_rn(f[m], sw), outer[m]);
-                outer[m + 16] = __fmaf_rn(__uint_as_float(v1[m]), __fmul_rn(f[m + 16], sw), outer[m + 16]);
-            }
-
             if (cur.kb != p.KB - 1 && i != nunits - 1) continue;
-            // after the CTA's last unit the weight ring is idle: the reduction may use it
+            // After the CTA's last unit both operand rings are idle once the
+            // factor warp has read the last scales (the slot's release
+            // completes; the MMAs are complete): the reduction may use them.
             const bool last = i == nunits - 1;
-            if (end_piece(p, tm_count, outer, cur.tile, cur.kb, u0 + i, u0, first_tile, split_info, q, lane,
-                          last ? gbase : nullptr))
+            if (last) {
+                bool idle = true;
+                if (lane == 0) idle = wait_bounded(xempty(i % kXStages), (i / kXStages) & 1, wc);
+                if (!__shfl_sync(0xffffffffu, idle, 0)) break;
+            }
+            if (end_piece<NA>(p, tm_count, outer, cur.tile, cur.kb, u0 + i, u0, first_tile, split_info, q, h, fw,
+                              lane, last ? gbase : nullptr))
                 deferred = true;
-            if (last && deferred) finish_tile(p, tm_count, first_tile, 0, split_info, q, lane, gbase);
+            if (last && deferred)
+                finish_tile<NA>(p, tm_count, first_tile, 0, split_info, q, h, fw, lane, gbase);
 #pragma unroll
-            for (int m = 0; m < kNA; ++m) outer[m] = 0.0f;
+            for (int j = 0; j < kFoldCols; ++j) outer[j] = 0.0f;
         }
     }
 
@@ -316,7 +489,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         __syncwarp();
         tc_fence_after();
-        tmem_dealloc(tmem, L::kTmemCols);
+        tmem_dealloc(tmem, 512);
     }
 }
 
@@ -363,25 +536,40 @@ __global__ void quantize_act_kernel(const uint16_t* __restrict__ X, int64_t ldx,
 
 }  // namespace
 
-cudaError_t launch_w8a8(const W8a8Args& a, const Schedule& s, const CUtensorMap& tmW, const CUtensorMap& tmX,
-                        const LaunchCtl& c, cudaStream_t st) {
-    using L = W8a8Layout;
+size_t w8a8_partial_bytes(const Schedule& s) {
+    return static_cast<size_t>(s.max_ctas) * 2 * 128 * kMaxTileRows * sizeof(float);
+}
+
+size_t w8a8_workspace_bytes(const Schedule& s, bool split) {
+    if (!split) return 0;
+    const size_t part = w8a8_partial_bytes(s);
+    const size_t cnt = (static_cast<size_t>(s.T) * (s.nmma / 16) * sizeof(uint32_t) + 255) & ~static_cast<size_t>(255);
+    return part + cnt;
+}
+
+template <int NA>
+static cudaError_t launch_w8a8_na(const W8a8Args& a, const Schedule& s, const CUtensorMap& tmW,
+                                  const CUtensorMap& tmX, const LaunchCtl& c, cudaStream_t st) {
+    using L = W8a8Layout<NA>;
     static int configured_device = -1;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (configured_device != dev) {
-        e = cudaFuncSetAttribute(w8a8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
+        e = cudaFuncSetAttribute(w8a8_kernel<NA>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
         if (e != cudaSuccess) return e;
         configured_device = dev;
     }
     gemm::Params p = gemm::base_params(s, a.Y, a.ldy, a.M, a.N, a.K, a.ws, c);
     p.S = a.S;
     p.lds = (a.K + 127) / 128;
-    const int tm_count = (a.M + kNA - 1) / kNA;
+    uint8_t* w = static_cast<uint8_t*>(a.ws);
+    p.part = reinterpret_cast<float*>(w);
+    p.cnt = w ? reinterpret_cast<uint32_t*>(w + w8a8_partial_bytes(s)) : nullptr;
+    const int tm_count = (a.M + NA - 1) / NA;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(s.G));
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(L::kThreads);
     cfg.dynamicSmemBytes = L::kSmemBytes;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
@@ -391,7 +579,14 @@ cudaError_t launch_w8a8(const W8a8Args& a, const Schedule& s, const CUtensorMap&
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    return cudaLaunchKernelEx(&cfg, w8a8_kernel, tmW, tmX, p, a.Sx, a.ldsx, tm_count);
+    return cudaLaunchKernelEx(&cfg, w8a8_kernel<NA>, tmW, tmX, p, a.Sx, a.ldsx, tm_count);
+}
+
+cudaError_t launch_w8a8(const W8a8Args& a, const Schedule& s, const CUtensorMap& tmW, const CUtensorMap& tmX,
+                        const LaunchCtl& c, cudaStream_t st) {
+    if (s.nmma == 64) return launch_w8a8_na<64>(a, s, tmW, tmX, c, st);
+    if (s.nmma == 128) return launch_w8a8_na<128>(a, s, tmW, tmX, c, st);
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_quantize_act(const void* X, int64_t ldx, void* Xq, int64_t ldxq, float* Sx, int64_t ldsx, int M,
