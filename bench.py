@@ -152,6 +152,20 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def head_config(overlap, world):
+    """The headline workload's `config` (shared by both arms of the bench)."""
+    M, N, K = HEAD["M"], HEAD["N"], HEAD["K"]
+    copies = -(-2 * L2_BYTES // (N * K)) + 1   # as Fp8Case
+    return {"workload": "fp8_block gate/up M=16 N=17408 K=5120",
+            "M": M, "N": N, "K": K, "weights": "E4M3 [N,K] + FP32 [128x128] block scales",
+            "arith": "E4M3 weights as stored into tcgen05 kind::f8f6f4 (no weight dequant); BF16 X split "
+                     "per (row, 128-K block) into two power-of-two-scaled E4M3 planes; FP32 two-level fold; "
+                     "BF16 out",
+            "l2": f"inputs larger than L2: {copies} rotating weight copies ({copies * N * K / 1e6:.0f} MB)",
+            "overlap": "weight prefetch overlaps the previous call" if overlap else "off",
+            "parallelism": "replicas" if world > 1 else "1 GPU"}
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -648,8 +662,7 @@ def run_reference(args):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(per * 1e3, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": "fp8_block gate/up M=16 N=17408 K=5120", "M": M, "N": N, "K": K,
-                   "sample_columns": n_s},
+        "config": head_config(bool(args.overlap), args.gpus),
         "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": nt, "kind": "oracle",
                          "sample": f"columns 0..{n_s - 1} of {N} per step (all {M} rows, full K)"},
         "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -827,14 +840,7 @@ def main():
         "vs_baseline_ref": "H100 w8a16_gemv_batch16 gate/up M=16, 342 GB/s (atlas m16_tc page, WHY table): context, other hardware",
         "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": "fp8_block gate/up M=16 N=17408 K=5120",
-                   "M": M, "N": N, "K": K, "weights": "E4M3 [N,K] + FP32 [128x128] block scales",
-                   "arith": "E4M3 weights as stored into tcgen05 kind::f8f6f4 (no weight dequant); BF16 X split "
-                            "per (row, 128-K block) into two power-of-two-scaled E4M3 planes; FP32 two-level fold; "
-                            "BF16 out",
-                   "l2": f"inputs larger than L2: {copies} rotating weight copies ({copies * N * K / 1e6:.0f} MB)",
-                   "overlap": "weight prefetch overlaps the previous call" if args.overlap else "off",
-                   "parallelism": "replicas" if world > 1 else "1 GPU"},
+        "config": head_config(bool(args.overlap), world),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
                      "bytes_per_launch": per_call_bytes,
