@@ -149,7 +149,8 @@ Schedule choose_schedule(int kind, int M, int N, int K, int sms) {
     s.nmma = kind == QG_KIND_W8A8 ? w8a8_tile_rows(M) : M <= 16 ? 16 : 32;
     // W8A8 tiles are 128 weight rows x nmma activation rows, weight-tile-major
     s.T = (N + 127) / 128 * (kind == QG_KIND_W8A8 ? (M + s.nmma - 1) / s.nmma : 1);
-    s.KU = (K + 127) / 128;   // one unit = 128 rows x one 128-wide K block
+    // one unit = 128 rows x one 128-wide K block (W8A8: two blocks)
+    s.KU = kind == QG_KIND_W8A8 ? (K + 255) / 256 : (K + 127) / 128;
     s.U = static_cast<long long>(s.T) * s.KU;
     const int forced = table_lookup(kind, M, N, K);
     long long g = sms;

@@ -42,23 +42,27 @@ using gemm::Params;
 
 constexpr int kWarpWProd = 0, kWarpXProd = 1, kWarpMma = 2, kWarpFactor = 3, kWarpFold0 = 4;
 constexpr int kFoldCols = 64;   // activation rows (MMA columns) per fold warp
+constexpr int kBlk = 2;         // 128-wide K blocks per unit
 
 template <int NA>
 struct W8a8Layout {
     static constexpr int kFold = NA / 16;                     // fold warps: 4 quadrants x NA/64 column halves
     static constexpr int kThreads = 32 * (kWarpFold0 + kFold);
-    static constexpr int kWBytes = 128 * 128;                 // one E4M3 weight unit
-    static constexpr int kXBytes = NA * 128;                  // one E4M3 activation slice
-    static constexpr int kXSlot = kXBytes + 1024;             // + NA scales, padded to keep 1024-B alignment
-    static constexpr int kXStages = NA == 128 ? 6 : 10;
-    static constexpr int kAcc = 512 / NA;                     // TMEM accumulators
-    static constexpr int kGStages = 2 * kAcc;                 // factor ring (NA floats a slot)
-    static constexpr int kReserve = kGStages * NA * 4 + 8 * 96 + 64 + 1024;   // + barriers, misc, alignment
+    static constexpr int kWBox = 128 * 128;                   // one 128 x 128 E4M3 weight block
+    static constexpr int kWBytes = kBlk * kWBox;              // one unit of weights
+    static constexpr int kXBox = NA * 128;                    // one NA x 128 E4M3 activation block
+    static constexpr int kXBytes = kBlk * kXBox;
+    static constexpr int kXSlot = kXBytes + 1024;             // + kBlk x NA scales, padded to keep 1024-B alignment
+    static constexpr int kXStages = NA == 128 ? 3 : 5;
+    static constexpr int kAcc = 512 / (kBlk * NA);            // TMEM accumulator sets (kBlk x NA columns each)
+    static constexpr int kGStages = 2 * kAcc;                 // factor ring (kBlk x NA floats a slot)
+    static constexpr int kGSlot = kBlk * NA * 4;
+    static constexpr int kReserve = kGStages * kGSlot + 8 * 96 + 64 + 1024;   // + barriers, misc, alignment
     static constexpr int kWFit = (232448 - kXStages * kXSlot - kReserve) / kWBytes;
     static constexpr int kWStages = kWFit < 12 ? kWFit : 12;
     static constexpr int kXOff = kWStages * kWBytes;
     static constexpr int kGOff = kXOff + kXStages * kXSlot;
-    static constexpr int kBarOff = kGOff + kGStages * NA * 4;
+    static constexpr int kBarOff = kGOff + kGStages * kGSlot;
     static constexpr int kNumBars = 2 * kWStages + 2 * kXStages + 2 * kGStages + 2 * kAcc;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     static constexpr int kSmemBytes = kMiscOff + 64 + 1024;
@@ -67,7 +71,8 @@ struct W8a8Layout {
     static constexpr int kPieceBytes = 32 * kFoldCols * 4;
     static constexpr int kScratchWarp = kGOff / kFold / kPieceBytes * kPieceBytes;
     static_assert(kNumBars <= 96, "barrier area");
-    static_assert(kWStages >= 6, "weight ring");
+    static_assert(kWStages >= 3, "weight ring");
+    static_assert(kBlk * NA * 4 <= 1024, "scales fit the slot's padding");
     static_assert(kXOff % 1024 == 0 && kXSlot % 1024 == 0, "keep the 1024-byte swizzle alignment");
     static_assert(kScratchWarp >= 2 * kPieceBytes, "reduction scratch");
     static_assert(kSmemBytes <= 232448, "shared memory");
@@ -248,7 +253,7 @@ __global__ void __launch_bounds__(W8a8Layout<NA>::kThreads, 1)
     auto scales_at = [&](int s) {
         return reinterpret_cast<const float*>(gbase + L::kXOff + s * L::kXSlot + L::kXBytes);
     };
-    auto factors_at = [&](int j) { return reinterpret_cast<float*>(gbase + L::kGOff + j * NA * 4); };
+    auto factors_at = [&](int j) { return reinterpret_cast<float*>(gbase + L::kGOff + j * L::kGSlot); };
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -305,8 +310,12 @@ __global__ void __launch_bounds__(W8a8Layout<NA>::kThreads, 1)
                 if (i >= kWStages && !wait_bounded(wempty(rw.slot), rw.phase ^ 1u, wc)) break;
                 issued = i + 1;
                 if (cta == 0 && i == p.fault_unit) continue;   // failure-path test hook
+                // both 128 x 128 blocks of the unit (a block past K reads as zeros)
                 mbar_arrive_expect_tx(wfull(rw.slot), L::kWBytes);
-                tma_load_2d(base + rw.slot * L::kWBytes, &tmW, wfull(rw.slot), up.c.kr * 128, up.tn * 128, pol_w);
+#pragma unroll
+                for (int b = 0; b < kBlk; ++b)
+                    tma_load_2d(base + rw.slot * L::kWBytes + b * L::kWBox, &tmW, wfull(rw.slot),
+                                (up.c.kr * kBlk + b) * 128, up.tn * 128, pol_w);
             }
             for (int i = issued - kWStages < 0 ? 0 : issued - kWStages; i < issued; ++i) {
                 if (cta == 0 && i == p.fault_unit) continue;
@@ -326,10 +335,17 @@ __global__ void __launch_bounds__(W8a8Layout<NA>::kThreads, 1)
             for (int i = 0; i < nunits; ++i, up.step(p.KB, tm_count, ldsx), rx.step(1)) {
                 if (i >= kXStages && !wait_bounded(xempty(rx.slot), rx.phase ^ 1u, wc)) break;
                 const uint32_t dst = base + L::kXOff + rx.slot * L::kXSlot;
-                mbar_arrive_expect_tx(xfull(rx.slot), L::kXBytes + up.nsc * 4);
-                tma_load_2d(dst, &tmX, xfull(rx.slot), up.c.kr * 128, up.tm * NA, pol_x);
-                bulk_load(dst + L::kXBytes, sx + static_cast<int64_t>(up.c.kr) * ldsx + static_cast<int64_t>(up.tm) * NA,
-                          up.nsc * 4, xfull(rx.slot), pol_x);
+                // the unit's K blocks that exist (the last unit of a row may hold one)
+                const int kb0 = up.c.kr * kBlk;
+                const int nblk = p.lds - kb0 < kBlk ? p.lds - kb0 : kBlk;
+                mbar_arrive_expect_tx(xfull(rx.slot), L::kXBytes + nblk * up.nsc * 4);
+#pragma unroll
+                for (int b = 0; b < kBlk; ++b)
+                    tma_load_2d(dst + b * L::kXBox, &tmX, xfull(rx.slot), (kb0 + b) * 128, up.tm * NA, pol_x);
+                for (int b = 0; b < nblk; ++b)
+                    bulk_load(dst + L::kXBytes + b * NA * 4,
+                              sx + static_cast<int64_t>(kb0 + b) * ldsx + static_cast<int64_t>(up.tm) * NA,
+                              up.nsc * 4, xfull(rx.slot), pol_x);
                 issued = i + 1;
             }
             for (int i = issued - kXStages < 0 ? 0 : issued - kXStages; i < issued; ++i)
@@ -354,8 +370,14 @@ __global__ void __launch_bounds__(W8a8Layout<NA>::kThreads, 1)
             const uint64_t bd = dx0 + static_cast<uint64_t>((rx.slot * L::kXSlot) >> 4);
             if (elected) {
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    mma_ss_f8(tmem + ra.slot * NA, ad + 2 * j, bd + 2 * j, idesc, j > 0 ? 1u : 0u);
+                for (int b = 0; b < kBlk; ++b) {
+                    // block b: its own accumulator of NA columns
+                    const uint64_t adb = ad + static_cast<uint64_t>((b * L::kWBox) >> 4);
+                    const uint64_t bdb = bd + static_cast<uint64_t>((b * L::kXBox) >> 4);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        mma_ss_f8(tmem + (ra.slot * kBlk + b) * NA, adb + 2 * j, bdb + 2 * j, idesc, j > 0 ? 1u : 0u);
+                }
                 tc_commit(wempty(rw.slot));
                 tc_commit(xempty(rx.slot));
                 tc_commit(dfull(ra.slot));
@@ -366,28 +388,32 @@ __global__ void __launch_bounds__(W8a8Layout<NA>::kThreads, 1)
         if (last >= 0 && elected) gemm::drain_wait(dfull(last % kAcc), (last / kAcc) & 1, p.timeout_ns);
     } else if (warp == kWarpFactor) {
         // ------------------------------------------------------------ block factors
-        // Lane l fetches the weight scale of unit i0 + l one batch of 32 units
-        // ahead of its use, so that no unit waits for a global load.
+        // Lane l fetches the weight scales of unit i0 + l one batch of 32
+        // units ahead of their use, so that no unit waits for a global load
+        // (0 for a K block past the end).
         UnitPos bp(u0, p.KB, tm_count, ldsx);   // the first unit of the batch fetched next
-        auto fetch = [&](int i0) {
-            float v = 0.0f;
+        auto fetch = [&](int i0, float2& v) {
+            v = make_float2(0.0f, 0.0f);
             if (i0 + lane < nunits) {
                 UnitPos mine = bp;
                 mine.advance(lane, p.KB, tm_count, ldsx);
-                v = __ldg(p.S + static_cast<int64_t>(mine.tn) * p.lds + mine.c.kr);
+                const int kb0 = mine.c.kr * kBlk;
+                const float* srow = p.S + static_cast<int64_t>(mine.tn) * p.lds;
+                v.x = __ldg(srow + kb0);
+                if (kb0 + 1 < p.lds) v.y = __ldg(srow + kb0 + 1);
             }
             bp.advance(32, p.KB, tm_count, ldsx);
-            return v;
         };
-        float sw_now = fetch(0);
-        float sw_next = fetch(32);
+        float2 sw_now, sw_next;
+        fetch(0, sw_now);
+        fetch(32, sw_next);
         UnitPos up(u0, p.KB, tm_count, ldsx);
         gemm::Ring<kXStages> rx(0);
         gemm::Ring<kGStages> rg(0);
         for (int i = 0; i < nunits; ++i, up.step(p.KB, tm_count, ldsx), rx.step(1), rg.step(1)) {
             if (i > 0 && (i & 31) == 0) {
                 sw_now = sw_next;
-                sw_next = fetch(i + 32);
+                fetch(i + 32, sw_next);
             }
             bool ok = true;
             if (lane == 0) {
@@ -396,13 +422,16 @@ __global__ void __launch_bounds__(W8a8Layout<NA>::kThreads, 1)
             }
             if (!__shfl_sync(0xffffffffu, ok, 0)) break;
             __syncwarp();   // orders the other lanes' reads after lane 0's wait
-            const float sw = __shfl_sync(0xffffffffu, sw_now, i & 31);
+            const float sw0 = __shfl_sync(0xffffffffu, sw_now.x, i & 31);
+            const float sw1 = __shfl_sync(0xffffffffu, sw_now.y, i & 31);
+            const bool has1 = up.c.kr * kBlk + 1 < p.lds;
             const float* sc = scales_at(rx.slot);
             float* f = factors_at(rg.slot);
 #pragma unroll
             for (int c = 0; c < NA / 32; ++c) {
                 const int m = c * 32 + lane;
-                f[m] = m < up.nsc ? __fmul_rn(sc[m], sw) : 0.0f;
+                f[m] = m < up.nsc ? __fmul_rn(sc[m], sw0) : 0.0f;
+                f[NA + m] = (has1 && m < up.nsc) ? __fmul_rn(sc[NA + m], sw1) : 0.0f;
             }
             __syncwarp();
             if (lane == 0) {
@@ -436,26 +465,30 @@ __global__ void __launch_bounds__(W8a8Layout<NA>::kThreads, 1)
             if (!__shfl_sync(0xffffffffu, ok, 0)) break;
             __syncwarp();   // orders the other lanes' reads after lane 0's wait
             tc_fence_after();
-            const float4* f4 = reinterpret_cast<const float4*>(factors_at(rg.slot) + h * kFoldCols);
+#pragma unroll 1
+            for (int b = 0; b < kBlk; ++b) {
+                const float4* f4 = reinterpret_cast<const float4*>(factors_at(rg.slot) + b * NA + h * kFoldCols);
+                const uint32_t tb = tl + (ra.slot * kBlk + b) * NA;
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                uint32_t v0[16], v1[16];
-                tmem_ld_x16(tl + ra.slot * NA + 32 * c, v0);
-                tmem_ld_x16(tl + ra.slot * NA + 32 * c + 16, v1);
-                tmem_wait_ld();
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t v0[16], v1[16];
+                    tmem_ld_x16(tb + 32 * c, v0);
+                    tmem_ld_x16(tb + 32 * c + 16, v1);
+                    tmem_wait_ld();
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float4 g0 = f4[8 * c + e];
-                    const float4 g1 = f4[8 * c + 4 + e];
-                    float* o = outer + 32 * c;
-                    o[4 * e + 0] = __fmaf_rn(__uint_as_float(v0[4 * e + 0]), g0.x, o[4 * e + 0]);
-                    o[4 * e + 1] = __fmaf_rn(__uint_as_float(v0[4 * e + 1]), g0.y, o[4 * e + 1]);
-                    o[4 * e + 2] = __fmaf_rn(__uint_as_float(v0[4 * e + 2]), g0.z, o[4 * e + 2]);
-                    o[4 * e + 3] = __fmaf_rn(__uint_as_float(v0[4 * e + 3]), g0.w, o[4 * e + 3]);
-                    o[16 + 4 * e + 0] = __fmaf_rn(__uint_as_float(v1[4 * e + 0]), g1.x, o[16 + 4 * e + 0]);
-                    o[16 + 4 * e + 1] = __fmaf_rn(__uint_as_float(v1[4 * e + 1]), g1.y, o[16 + 4 * e + 1]);
-                    o[16 + 4 * e + 2] = __fmaf_rn(__uint_as_float(v1[4 * e + 2]), g1.z, o[16 + 4 * e + 2]);
-                    o[16 + 4 * e + 3] = __fmaf_rn(__uint_as_float(v1[4 * e + 3]), g1.w, o[16 + 4 * e + 3]);
+                    for (int e = 0; e < 4; ++e) {
+                        const float4 g0 = f4[8 * c + e];
+                        const float4 g1 = f4[8 * c + 4 + e];
+                        float* o = outer + 32 * c;
+                        o[4 * e + 0] = __fmaf_rn(__uint_as_float(v0[4 * e + 0]), g0.x, o[4 * e + 0]);
+                        o[4 * e + 1] = __fmaf_rn(__uint_as_float(v0[4 * e + 1]), g0.y, o[4 * e + 1]);
+                        o[4 * e + 2] = __fmaf_rn(__uint_as_float(v0[4 * e + 2]), g0.z, o[4 * e + 2]);
+                        o[4 * e + 3] = __fmaf_rn(__uint_as_float(v0[4 * e + 3]), g0.w, o[4 * e + 3]);
+                        o[16 + 4 * e + 0] = __fmaf_rn(__uint_as_float(v1[4 * e + 0]), g1.x, o[16 + 4 * e + 0]);
+                        o[16 + 4 * e + 1] = __fmaf_rn(__uint_as_float(v1[4 * e + 1]), g1.y, o[16 + 4 * e + 1]);
+                        o[16 + 4 * e + 2] = __fmaf_rn(__uint_as_float(v1[4 * e + 2]), g1.z, o[16 + 4 * e + 2]);
+                        o[16 + 4 * e + 3] = __fmaf_rn(__uint_as_float(v1[4 * e + 3]), g1.w, o[16 + 4 * e + 3]);
+                    }
                 }
             }
             tc_fence_before();
