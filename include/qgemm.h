@@ -407,7 +407,9 @@ qg_status qg_tune_lut3(const void *X, int64_t ldx, const void *const *Wq_copies,
  * Test aid: the work split of a shape's schedule, computed on the device by
  * the same functions the GEMM kernels use.  Work units are (128-row tile,
  * 128-wide K block) pairs numbered tile-major, ceil(N/128) * ceil(K/128) in
- * all.  Writes the CTA count to *ctas (host); then, unless ranges or info is
+ * all (QG_KIND_W8A8: tiles of 128 rows x R activation rows as in
+ * qg_workspace_bytes, units of two K blocks, ceil(K/256) per tile).  Writes
+ * the CTA count to *ctas (host); then, unless ranges or info is
  * null, launches one small kernel on `stream` that writes, for every CTA g:
  *   ranges[2g], ranges[2g+1]   device int64: its units [first, end)
  *   info[6g .. 6g+2]           device int32: for its first tile, the first

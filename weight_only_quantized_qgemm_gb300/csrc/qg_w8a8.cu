@@ -8,23 +8,26 @@
 //   Y[m, n] = bf16( sum_kb (sx[kb, m] * s[n/128, kb]) * (sum_{k in kb} xq[m,k] * w[n,k]) )
 //
 // The GEMM tiles the output in 128 weight rows x NA activation rows (NA = 64
-// or 128: the MMA's N side); a unit is one tile x one 128-wide K block.  Both
-// operands go to tcgen05.mma kind::f8f6f4 as stored (TMA, 128-byte swizzle).
-// Each unit's block sums land in their own TMEM accumulator; the fold
-// multiplies them by the unit's NA block factors (activation scale x weight
-// scale) once and adds them to FP32 outer sums held in registers: the
-// two-level fold of the W8A16 path.  Tiles are numbered weight-tile-major, so
+// or 128: the MMA's N side); a unit is one tile x two 128-wide K blocks (two
+// blocks per unit halve the barrier rounds per MMA).  Both operands go to
+// tcgen05.mma kind::f8f6f4 as stored (TMA, 128-byte swizzle).  Each K
+// block's sums land in their own TMEM accumulator; the fold multiplies them
+// by the block's NA factors (activation scale x weight scale) once and adds
+// them to FP32 outer sums held in registers: the two-level fold of the
+// W8A16 path.  Tiles are numbered weight-tile-major, so
 // the activation-row blocks of a weight tile are neighbours and its weights
 // come from L2 after the first read.  Work units are split evenly over the
 // CTAs (stream-K), a tile shared by several CTAs being summed by the last to
 // arrive, as in the decode kernels, with partial sums kept per fold warp.
 //
 // One persistent CTA per SM, 4 + NA/16 warps:
-//   warp 0      weight producer: one 16 KB TMA tile per unit.
+//   warp 0      weight producer: two 128 x 128 TMA boxes per unit (a box
+//               past K reads as zeros).
 //   warp 1      activation producer, after the grid dependency wait: the
-//               unit's NA x 128 E4M3 slice (TMA) and its NA activation scales
-//               (one bulk copy) into a ring.
-//   warp 2      MMA issuer: 4 tcgen05.mma (M = 128, N = NA, K = 32) per unit.
+//               unit's two NA x 128 E4M3 boxes (TMA) and the NA activation
+//               scales of each existing block (bulk copies) into a ring.
+//   warp 2      MMA issuer: 8 tcgen05.mma (M = 128, N = NA, K = 32) per unit,
+//               four per K block into that block's accumulator.
 //   warp 3      factor warp: turns the unit's activation scales into block
 //               factors (times the unit's weight scale, fetched 32 units
 //               ahead, one unit per lane) in a ring of its own, so that an
