@@ -386,6 +386,10 @@ class Bf16Case:
         self.Y = torch.empty((M_max, N), dtype=torch.bfloat16, device="cuda")
         self.ws = qg.Workspace()
 
+    def tune(self, M, stream):
+        g, _ = self.qg.tune_bf16(self.X[:M], self.W, calls=50, workspace=self.ws, stream=stream)
+        return g
+
     def time(self, M, stream, steps, warmup):
         qg, N, K = self.qg, self.N, self.K
         buf = self.ws.get(qg.workspace_bytes(qg.KIND_BF16, M, N, K))
@@ -472,6 +476,16 @@ class W8a8Case:
         self.Sx = torch.empty((-(-K // 128), self.ldsx), dtype=torch.float32, device="cuda")
         self.Y = torch.empty((M_max, N), dtype=torch.bfloat16, device="cuda")
         self.ws = qg.Workspace()
+
+    def tune(self, M, stream):
+        """The dispatch tuner on the GEMM of the first M rows (quantised first)."""
+        qg, K = self.qg, self.K
+        r = qg.lib.qg_quantize_act_e4m3(self.X.data_ptr(), K, self.Xq.data_ptr(), K, self.Sx.data_ptr(), self.ldsx,
+                                        M, K, stream.cuda_stream)
+        if r:
+            raise RuntimeError(qg.status_string(r))
+        g, _ = qg.tune_w8a8(self.Xq[:M], self.Sx, self.W, self.S, calls=20, workspace=self.ws, stream=stream)
+        return g
 
     def time(self, M, stream, steps, warmup, what="gemm"):
         """what: "gemm" (qgemm_w8a8_block on resident codes), "quant"
@@ -566,7 +580,8 @@ def secondary_lines(torch, qg, stream, peak, steps=2000, warmup=50, tune=True):
     # unquantised BF16 output projection (lm_head shape)
     c = Bf16Case(torch, qg, 32, 32768, 5120)
     for m in (1, 16, 32):
-        rec(f"bf16_lm_head_M{m}", c.time(m, stream, steps // 4, warmup), bf16_bytes(m, 32768, 5120))
+        g = tuned(c, m)
+        rec(f"bf16_lm_head_M{m}", c.time(m, stream, steps // 4, warmup), bf16_bytes(m, 32768, 5120), g)
     c.free()
     # Q, K and V in one launch against the three calls one after another
     c = QkvCase(torch, qg, 32)
@@ -585,11 +600,14 @@ def secondary_lines(torch, qg, stream, peak, steps=2000, warmup=50, tune=True):
     c = W8a8Case(torch, qg, 1024, 17408, 5120)
     for m in (64, 256, 1024):
         flops = 2.0 * m * 17408 * 5120
+        g = tuned(c, m)
         for what in ("gemm", "both"):
             ms = c.time(m, stream, max(50, steps // 20), warmup, what)
             tf = flops / (ms * 1e-3) / 1e12
             out[f"w8a8_gateup_M{m}_{what}"] = {"us": round(ms * 1e3, 3), "TFLOPs": round(tf, 1),
                                                "frac_fp8_tensor": round(tf / tpeak, 4)}
+            if g is not None:
+                out[f"w8a8_gateup_M{m}_{what}"]["grid"] = g
         out[f"w8a8_gateup_M{m}_quant"] = {"us": round(c.time(m, stream, max(50, steps // 20), warmup, "quant") * 1e3, 3)}
     c.free()
     qg.dispatch_clear()

@@ -372,6 +372,12 @@ void qg_dispatch_clear(void);
 size_t qg_workspace_bytes_max(int N);
 
 /*
+ * The same bound for QG_KIND_W8A8 shapes with M activation rows and N output
+ * rows (any K, any grid); 0 for invalid arguments.
+ */
+size_t qg_workspace_bytes_max_w8a8(int M, int N);
+
+/*
  * Tuning of the dispatch table for one shape: an exactness-gated search
  * (FLUTE "optimized_w3" page, Results: a candidate is accepted only after
  * its output is checked).  The built-in schedule's output, written to Y_ref
@@ -401,6 +407,23 @@ qg_status qg_tune_fp8(const void *X, int64_t ldx, const uint8_t *const *W_copies
 qg_status qg_tune_lut3(const void *X, int64_t ldx, const void *const *Wq_copies, int ncopies,
                        const void *qmap, const void *scales, void *Y, int64_t ldy, void *Y_ref,
                        int M, int N, int K, void *workspace, size_t workspace_bytes,
+                       int calls, int *best_ctas, float *best_us, struct CUstream_st *stream);
+
+/*
+ * The same search for the dense BF16 GEMM (workspace bound
+ * qg_workspace_bytes_max(N)) and for the W8A8 GEMM on quantised activations
+ * (workspace bound qg_workspace_bytes_max_w8a8(M, N); candidate grids count
+ * that kind's tiles of 128 x R rows and units of two K blocks).
+ */
+qg_status qg_tune_bf16(const void *X, int64_t ldx, const void *const *W_copies, int ncopies,
+                       void *Y, int64_t ldy, void *Y_ref, int M, int N, int K,
+                       void *workspace, size_t workspace_bytes,
+                       int calls, int *best_ctas, float *best_us, struct CUstream_st *stream);
+
+qg_status qg_tune_w8a8(const uint8_t *Xq, int64_t ldxq, const float *X_scale, int64_t ldsx,
+                       const uint8_t *const *W_copies, int ncopies, const float *W_scale,
+                       void *Y, int64_t ldy, void *Y_ref, int M, int N, int K,
+                       void *workspace, size_t workspace_bytes,
                        int calls, int *best_ctas, float *best_us, struct CUstream_st *stream);
 
 /*

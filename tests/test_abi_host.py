@@ -258,3 +258,24 @@ def test_w8a8_dispatch_accepts_large_m(qg):
     assert qg.lib.qg_dispatch_set(qg.KIND_W8A8, 256, 1024, 5120, -1) == 1
     assert qg.lib.qg_dispatch_get(qg.KIND_W8A8, 0, 1024, 5120) == 0
     assert qg.lib.qg_workspace_bytes(qg.KIND_W8A8, 65537, 1024, 5120) == 0
+
+
+def test_bf16_and_w8a8_tuner_argument_validation(qg):
+    """The BF16 and W8A8 tuners check their arguments before touching a device."""
+    P = ctypes.c_void_p
+    ptrs = (P * 1)(FAKE)
+    pp = ctypes.cast(ptrs, P)
+    t = qg.lib.qg_tune_bf16
+    assert t(FAKE, 512, None, 1, FAKE, 256, FAKE, 4, 256, 512, None, 0, 10, None, None, None) == 1   # no copies
+    assert t(FAKE, 512, pp, 0, FAKE, 256, FAKE, 4, 256, 512, None, 0, 10, None, None, None) == 1     # ncopies 0
+    assert t(FAKE, 512, pp, 1, FAKE, 256, None, 4, 256, 512, None, 0, 10, None, None, None) == 1     # no Y_ref
+    assert t(FAKE, 512, pp, 1, FAKE, 256, FAKE, 4, 256, 512, None, 0, 0, None, None, None) == 1      # calls 0
+    assert t(FAKE, 512, pp, 1, FAKE, 256, FAKE, 33, 256, 512, None, 0, 10, None, None, None) == 2    # M > 32
+    w = qg.lib.qg_tune_w8a8
+    assert w(FAKE, 512, FAKE, 64, None, 1, FAKE, FAKE, 256, FAKE, 40, 256, 512, None, 0, 10, None, None, None) == 1
+    assert w(FAKE, 512, FAKE, 64, pp, 1, FAKE, FAKE, 256, FAKE, 40, 256, 512, None, 0, 0, None, None, None) == 1
+    assert w(FAKE, 512, FAKE, 64, pp, 1, FAKE, FAKE, 256, None, 40, 256, 512, None, 0, 10, None, None, None) == 1
+    assert w(FAKE, 512, FAKE, 64, pp, 1, FAKE, FAKE, 256, FAKE, 65537, 256, 512, None, 0, 10, None, None,
+             None) == 2
+    assert qg.lib.qg_workspace_bytes_max_w8a8(0, 256) == 0
+    assert qg.lib.qg_workspace_bytes_max_w8a8(64, 0) == 0

@@ -13,6 +13,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import workloads as wl
 from gpu_util import Fp8Device, Lut3Device, cached, grade_fp8, grade_lut3, qg, to_bits
 
@@ -147,6 +148,44 @@ def test_lut3_tuner_installs_a_gated_grid():
         Y = q.qgemm_lut3(Xd, dev.Wq, dev.qmap, dev.scales, N)
         assert q.last_device_status() == 0
         ok, rep = grade_lut3(p, to_bits(Y))
+        assert rep.ok, rep
+    finally:
+        q.dispatch_clear()
+
+
+def test_bf16_tuner_installs_a_gated_grid():
+    q = qg()
+    M, N, K = 16, 4096, 5120
+    p = cached(("bf16", M, N, K, 72), lambda: wl.make_bf16_problem(M, N, K, config_id=72))
+    W = torch.from_numpy(p.W.view(np.int16)).view(torch.bfloat16).cuda()
+    Xd = torch.from_numpy(p.X.view(np.int16)).view(torch.bfloat16).cuda()
+    try:
+        g, us = q.tune_bf16(Xd, [W, W.clone()], calls=40)
+        assert q.dispatch_get(q.KIND_BF16, M, N, K) == g and us > 0
+        Y = q.qgemm_bf16(Xd, W)
+        assert q.last_device_status() == 0
+        ref = oracle.gemm_bf16(p.X, p.W)
+        ok, rep = oracle.within_budget(to_bits(Y), ref, oracle.bf16_abs_mass(p.X, p.W), fmt="bf16")
+        assert rep.ok, rep
+    finally:
+        q.dispatch_clear()
+
+
+def test_w8a8_tuner_installs_a_gated_grid():
+    q = qg()
+    M, N, K = 160, 1152, 2048
+    p = cached(("w8a8", M, N, K, 73), lambda: wl.make_w8a8_problem(M, N, K, config_id=73))
+    Xq_ref, Sx_ref = oracle.quantize_act_e4m3(p.X)
+    W = torch.from_numpy(p.W).cuda()
+    S = torch.from_numpy(p.S).cuda()
+    Xq, Sx = q.quantize_act_e4m3(torch.from_numpy(p.X.view(np.int16)).view(torch.bfloat16).cuda())
+    try:
+        g, us = q.tune_w8a8(Xq, Sx, [W, W.clone()], S, calls=20)
+        assert q.dispatch_get(q.KIND_W8A8, M, N, K) == g and us > 0
+        Y = q.qgemm_w8a8_block(Xq, Sx, W, S)
+        assert q.last_device_status() == 0
+        ref = oracle.qgemm_w8a8_block(Xq_ref, Sx_ref, p.W, p.S)
+        ok, rep = oracle.within_budget(to_bits(Y), ref, oracle.w8a8_abs_mass(Xq_ref, Sx_ref, p.W, p.S), fmt="bf16")
         assert rep.ok, rep
     finally:
         q.dispatch_clear()

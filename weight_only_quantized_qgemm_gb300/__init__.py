@@ -40,6 +40,7 @@ __all__ = [
     "set_fault_injection", "set_weight_prefetch_overlap", "dispatch_set", "dispatch_get", "dispatch_clear",
     "debug_schedule", "tune_fp8", "tune_lut3", "workspace_bytes_max", "qgemm_bf16", "KIND_BF16", "KIND_FP8_BLOCK", "KIND_LUT3", "STATUS",
     "quantize_act_e4m3", "qgemm_w8a8_block", "qgemm_w8a8", "KIND_W8A8", "MAX_M_W8A8",
+    "tune_bf16", "tune_w8a8", "workspace_bytes_max_w8a8",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -91,6 +92,9 @@ _SIGS = {
     "qg_dispatch_get": (_I, [_I, _I, _I, _I]),
     "qg_dispatch_clear": (None, []),
     "qg_workspace_bytes_max": (_S, [_I]),
+    "qg_workspace_bytes_max_w8a8": (_S, [_I, _I]),
+    "qg_tune_bf16": (_I, [_P, _L, _P, _I, _P, _L, _P, _I, _I, _I, _P, _S, _I, _P, _P, _P]),
+    "qg_tune_w8a8": (_I, [_P, _L, _P, _L, _P, _I, _P, _P, _L, _P, _I, _I, _I, _P, _S, _I, _P, _P, _P]),
     "qg_tune_fp8": (_I, [_P, _L, _P, _I, _P, _P, _L, _P, _I, _I, _I, _P, _S, _I, _P, _P, _P]),
     "qg_tune_lut3": (_I, [_P, _L, _P, _I, _P, _P, _P, _L, _P, _I, _I, _I, _P, _S, _I, _P, _P, _P]),
     "qg_dequant_lut3": (_I, [_P, _P, _P, _P, _I, _I, _P]),
@@ -500,11 +504,11 @@ def workspace_bytes_max(N: int) -> int:
     return int(lib.qg_workspace_bytes_max(N))
 
 
-def _tune_common(M, N, X, Y_ref, workspace):
-    torch = _torch()
+def _tune_common(M, N, X, Y_ref, workspace, nbytes=None):
     if workspace is None:
         workspace = Workspace(X.device)
-    buf = workspace.get(workspace_bytes_max(N)) if isinstance(workspace, Workspace) else workspace
+    need = workspace_bytes_max(N) if nbytes is None else nbytes
+    buf = workspace.get(need) if isinstance(workspace, Workspace) else workspace
     return buf, (buf.numel() * buf.element_size() if buf is not None else 0)
 
 
@@ -524,6 +528,48 @@ def tune_fp8(X, W_copies, W_scale, calls: int = 200, workspace=None, stream=None
                            W_scale.data_ptr(), Y.data_ptr(), N, Y_ref.data_ptr(), M, N, K,
                            buf.data_ptr() if buf is not None else None, nb, calls, ctypes.byref(g), ctypes.byref(us),
                            _stream_ptr(stream)), "qg_tune_fp8")
+    _ws_need.clear()
+    return g.value, us.value
+
+
+def workspace_bytes_max_w8a8(M: int, N: int) -> int:
+    """The largest workspace any grid of a W8A8 shape with M activation rows
+    and N output rows may need on the current device."""
+    return int(lib.qg_workspace_bytes_max_w8a8(M, N))
+
+
+def tune_bf16(X, W_copies, calls: int = 200, workspace=None, stream=None):
+    """As tune_fp8 for the dense BF16 GEMM (W_copies: equal BF16 weights)."""
+    torch = _torch()
+    M, K = X.shape
+    N = W_copies[0].shape[0]
+    Y = torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
+    Y_ref = torch.empty_like(Y)
+    buf, nb = _tune_common(M, N, X, Y_ref, workspace)
+    ptrs = (ctypes.c_void_p * len(W_copies))(*[w.data_ptr() for w in W_copies])
+    g, us = ctypes.c_int(0), ctypes.c_float(0)
+    _check(lib.qg_tune_bf16(X.data_ptr(), _ld(X), ctypes.cast(ptrs, ctypes.c_void_p), len(W_copies), Y.data_ptr(),
+                            N, Y_ref.data_ptr(), M, N, K, buf.data_ptr() if buf is not None else None, nb, calls,
+                            ctypes.byref(g), ctypes.byref(us), _stream_ptr(stream)), "qg_tune_bf16")
+    _ws_need.clear()
+    return g.value, us.value
+
+
+def tune_w8a8(Xq, X_scale, W_copies, W_scale, calls: int = 100, workspace=None, stream=None):
+    """As tune_fp8 for the W8A8 GEMM on quantised activations (Xq, X_scale as
+    quantize_act_e4m3 returns them; W_copies: equal E4M3 weights)."""
+    torch = _torch()
+    M, K = Xq.shape
+    N = W_copies[0].shape[0]
+    Y = torch.empty((M, N), dtype=torch.bfloat16, device=Xq.device)
+    Y_ref = torch.empty_like(Y)
+    buf, nb = _tune_common(M, N, Xq, Y_ref, workspace, workspace_bytes_max_w8a8(M, N))
+    ptrs = (ctypes.c_void_p * len(W_copies))(*[w.data_ptr() for w in W_copies])
+    g, us = ctypes.c_int(0), ctypes.c_float(0)
+    _check(lib.qg_tune_w8a8(Xq.data_ptr(), _ld(Xq), X_scale.data_ptr(), _ld(X_scale),
+                            ctypes.cast(ptrs, ctypes.c_void_p), len(W_copies), W_scale.data_ptr(), Y.data_ptr(), N,
+                            Y_ref.data_ptr(), M, N, K, buf.data_ptr() if buf is not None else None, nb, calls,
+                            ctypes.byref(g), ctypes.byref(us), _stream_ptr(stream)), "qg_tune_w8a8")
     _ws_need.clear()
     return g.value, us.value
 

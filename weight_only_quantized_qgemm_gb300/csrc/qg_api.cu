@@ -457,6 +457,20 @@ size_t qg_workspace_bytes_max(int N) {
     return workspace_partial_bytes(s) + cnt;
 }
 
+size_t qg_workspace_bytes_max_w8a8(int M, int N) {
+    if (M < 1 || M > kMaxMW8a8 || N < 1) return 0;
+    DeviceInfo* d = device_info();
+    if (!d) return 0;
+    Schedule s;
+    s.nmma = w8a8_tile_rows(M);
+    s.T = (N + 127) / 128 * ((M + s.nmma - 1) / s.nmma);
+    s.max_ctas = d->sms;
+    s.U = 1;
+    s.KU = 1;
+    s.G = 2;   // any split schedule: the size does not depend on K or the grid
+    return w8a8_workspace_bytes(s, true);
+}
+
 qg_status qgemm_fp8_block(const void* X, int64_t ldx, const uint8_t* W, const float* W_scale, void* Y, int64_t ldy,
                           int M, int N, int K, void* workspace, size_t workspace_bytes_, cudaStream_t stream) {
     const qg_status v = check_fp8_args(X, ldx, W, W_scale, Y, ldy, M, N, K);

@@ -10,6 +10,7 @@
 
 #include "../../include/qgemm.h"
 #include "qg_internal.h"
+#include "qg_w8a8.h"
 
 namespace qg {
 namespace {
@@ -66,6 +67,8 @@ std::vector<int> candidates(int T, long long U, int sms) {
 
 struct Tuner {
     int kind, M, N, K;
+    int T;          // the shape's tiles
+    long long U;    // its work units
     void* Y;
     void* Y_ref;
     int64_t ldy;
@@ -97,8 +100,6 @@ struct Tuner {
         if (cudaGetDevice(&dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
             return QG_ERR_CUDA;
-        const int T = (N + 127) / 128;
-        const long long U = static_cast<long long>(T) * ((K + 127) / 128);
         std::vector<int> cand = candidates(T, U, sms);
         bool has_builtin = false;
         for (int g : cand) has_builtin |= g == builtin;
@@ -160,6 +161,26 @@ struct Tuner {
     }
 };
 
+// Tiles and work units of a shape (the dispatch rule's decomposition).
+void shape_units(int kind, int M, int N, int K, int* T, long long* U) {
+    const int tn = (N + 127) / 128;
+    if (kind == QG_KIND_W8A8) {
+        const int R = w8a8_tile_rows(M);
+        *T = tn * ((M + R - 1) / R);
+        *U = static_cast<long long>(*T) * ((K + 255) / 256);
+    } else {
+        *T = tn;
+        *U = static_cast<long long>(tn) * ((K + 127) / 128);
+    }
+}
+
+Tuner make_tuner(int kind, int M, int N, int K, void* Y, int64_t ldy, void* Y_ref, void* workspace,
+                 size_t workspace_bytes, int calls, cudaStream_t stream, bool bf16) {
+    Tuner t{kind, M, N, K, 0, 0, Y, Y_ref, ldy, workspace ? workspace_bytes : 0, calls, stream, bf16};
+    shape_units(kind, M, N, K, &t.T, &t.U);
+    return t;
+}
+
 }  // namespace
 }  // namespace qg
 
@@ -174,7 +195,8 @@ extern "C" qg_status qg_tune_fp8(const void* X, int64_t ldx, const uint8_t* cons
     }
     if (M == 0 || N == 0 || K == 0) return QG_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(Y_ref) & 1u) != 0) return QG_ERR_MISALIGNED;
-    qg::Tuner t{QG_KIND_FP8_BLOCK, M, N, K, Y, Y_ref, ldy, workspace ? workspace_bytes : 0, calls, stream, true};
+    qg::Tuner t = qg::make_tuner(QG_KIND_FP8_BLOCK, M, N, K, Y, ldy, Y_ref, workspace, workspace_bytes, calls, stream,
+                                 true);
     auto run = [&](void* out, int i) {
         return qgemm_fp8_block(X, ldx, W_copies[i % ncopies], W_scale, out, ldy, M, N, K, workspace,
                                workspace_bytes, stream);
@@ -189,10 +211,44 @@ extern "C" qg_status qg_tune_lut3(const void* X, int64_t ldx, const void* const*
     if (!Wq_copies || ncopies < 1 || !Y_ref || calls < 1) return QG_ERR_INVALID_ARG;
     if (M < 1 || N < 1 || K < 1) return QG_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(Y_ref) & 1u) != 0) return QG_ERR_MISALIGNED;
-    qg::Tuner t{QG_KIND_LUT3, M, N, K, Y, Y_ref, ldy, workspace ? workspace_bytes : 0, calls, stream, false};
+    qg::Tuner t = qg::make_tuner(QG_KIND_LUT3, M, N, K, Y, ldy, Y_ref, workspace, workspace_bytes, calls, stream,
+                                 false);
     auto run = [&](void* out, int i) {
         return qgemm_lut3(X, ldx, Wq_copies[i % ncopies], qmap, scales, out, ldy, M, N, K, workspace,
                           workspace_bytes, stream);
+    };
+    return t.tune(run, best_ctas, best_us);
+}
+
+extern "C" qg_status qg_tune_bf16(const void* X, int64_t ldx, const void* const* W_copies, int ncopies, void* Y,
+                                  int64_t ldy, void* Y_ref, int M, int N, int K, void* workspace,
+                                  size_t workspace_bytes, int calls, int* best_ctas, float* best_us,
+                                  cudaStream_t stream) {
+    if (!W_copies || ncopies < 1 || !Y_ref || calls < 1) return QG_ERR_INVALID_ARG;
+    if (M < 1 || M > 32 || N < 1 || K < 1) return M > 32 ? QG_ERR_UNSUPPORTED_SHAPE : QG_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(Y_ref) & 1u) != 0) return QG_ERR_MISALIGNED;
+    qg::Tuner t = qg::make_tuner(QG_KIND_BF16, M, N, K, Y, ldy, Y_ref, workspace, workspace_bytes, calls, stream,
+                                 true);
+    auto run = [&](void* out, int i) {
+        return qgemm_bf16(X, ldx, W_copies[i % ncopies], out, ldy, M, N, K, workspace, workspace_bytes, stream);
+    };
+    return t.tune(run, best_ctas, best_us);
+}
+
+extern "C" qg_status qg_tune_w8a8(const uint8_t* Xq, int64_t ldxq, const float* X_scale, int64_t ldsx,
+                                  const uint8_t* const* W_copies, int ncopies, const float* W_scale, void* Y,
+                                  int64_t ldy, void* Y_ref, int M, int N, int K, void* workspace,
+                                  size_t workspace_bytes, int calls, int* best_ctas, float* best_us,
+                                  cudaStream_t stream) {
+    if (!W_copies || ncopies < 1 || !Y_ref || calls < 1) return QG_ERR_INVALID_ARG;
+    if (M < 1 || N < 1 || K < 1) return QG_ERR_INVALID_ARG;
+    if (M > 65536) return QG_ERR_UNSUPPORTED_SHAPE;
+    if ((reinterpret_cast<uintptr_t>(Y_ref) & 1u) != 0) return QG_ERR_MISALIGNED;
+    qg::Tuner t = qg::make_tuner(QG_KIND_W8A8, M, N, K, Y, ldy, Y_ref, workspace, workspace_bytes, calls, stream,
+                                 true);
+    auto run = [&](void* out, int i) {
+        return qgemm_w8a8_block(Xq, ldxq, X_scale, ldsx, W_copies[i % ncopies], W_scale, out, ldy, M, N, K,
+                                workspace, workspace_bytes, stream);
     };
     return t.tune(run, best_ctas, best_us);
 }
