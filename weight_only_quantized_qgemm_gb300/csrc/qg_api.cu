@@ -102,18 +102,29 @@ namespace {
 // Per-(kind, M, N, K) choice of MMA width and grid.  The MMA N side is 16 for
 // M <= 16 and 32 above (one weight pass for every M <= 32).  The grid comes
 // from the dispatch table when it holds an entry for the shape (set by a
-// caller, e.g. after measuring candidates), else from a cost rule weighing
-// two grids by the work units (128 rows x 128 K) of their busiest CTA:
-//  - one CTA per 128-row tile, when the tiles fit on the SMs: no tile is
-//    split, so no partial sums and no reduction;
-//  - stream-K: one CTA per SM, the units split evenly, capped so that a tile
-//    is shared by about kMaxPiecesPerTile CTAs at most.  A split tile costs
-//    the CTA that finishes it a partial-sum store, an arrival atomic and the
-//    reduction, at the end of the kernel; that tail measured about as long
-//    as kSplitCostUnits units of steady streaming.
-// Ties go to the grid without splits.
-constexpr int kMaxPiecesPerTile = 4;
+// caller, e.g. after measuring candidates), else from a cost rule.  When the
+// tiles fit on the SMs it weighs two grids by the work units (128 rows x
+// 128 K) of their busiest CTA:
+//  - one CTA per 128-row tile: no tile is split, so no partial sums and no
+//    reduction;
+//  - k CTAs per tile, k the largest whole number with k x tiles <= SMs, at
+//    most kMaxPiecesPerTile: the units split evenly, every tile into k
+//    pieces of equal size.  (The tuner's picks on the attention and down
+//    shapes were all such whole multiples: 3 per tile at 40 and 48 tiles, 8
+//    at 8 tiles.)  A split tile costs the CTA that finishes it a partial-sum
+//    store, an arrival atomic and the reduction, at the end of the kernel;
+//    that tail measured about as long as kSplitCostUnits units of steady
+//    streaming;
+//  - where a unit's on-chip work rather than HBM sets the pace (the FP8
+//    kernel at 17-32 rows, whose activation split doubles, and W8A8), also
+//    one CTA per SM with the units split evenly, whose pieces straddle tile
+//    boundaries: kStraddleCostUnits more (on down at 32 rows, 152 CTAs ran
+//    25.5 us against 27.4 at 120; on the 5120 x 5120 shape 14.4 against 13.2).
+// Ties go to the grid without splits, then to whole multiples.  More tiles
+// than SMs: stream-K, one CTA per SM.
+constexpr int kMaxPiecesPerTile = 8;
 constexpr long long kSplitCostUnits = 10;
+constexpr long long kStraddleCostUnits = 5;
 
 long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
 
@@ -157,12 +168,25 @@ Schedule choose_schedule(int kind, int M, int N, int K, int sms) {
     if (forced > 0) {
         g = forced;
         if (g > s.U) g = s.U;
+    } else if (s.T <= sms) {
+        auto cost_of = [&](long long G, long long extra) {
+            return ceil_div(s.U, G) + (splits(s.U, s.KU, static_cast<int>(G)) ? kSplitCostUnits + extra : 0);
+        };
+        long long k = sms / s.T;
+        if (k > kMaxPiecesPerTile) k = kMaxPiecesPerTile;
+        long long gb = k * s.T;
+        if (gb > s.U) gb = s.U;
+        long long best = s.KU;   // one CTA per tile
+        g = s.T;
+        if (cost_of(gb, 0) < best) {
+            best = cost_of(gb, 0);
+            g = gb;
+        }
+        const bool unit_bound = kind == QG_KIND_W8A8 || (kind == QG_KIND_FP8_BLOCK && M > 16);
+        const long long gc = sms < s.U ? sms : s.U;
+        if (unit_bound && gc != g && cost_of(gc, kStraddleCostUnits) < best) g = gc;
     } else {
         if (g > s.U) g = s.U;
-        if (g > static_cast<long long>(kMaxPiecesPerTile) * s.T) g = static_cast<long long>(kMaxPiecesPerTile) * s.T;
-        if (g < 1) g = 1;
-        long long cost = ceil_div(s.U, g) + (splits(s.U, s.KU, static_cast<int>(g)) ? kSplitCostUnits : 0);
-        if (s.T <= sms && static_cast<long long>(s.KU) <= cost) g = s.T;
     }
     s.G = static_cast<int>(g);
     s.max_ctas = sms > s.G ? sms : s.G;
