@@ -5,8 +5,9 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import workloads as wl
-from gpu_util import Fp8Device, Lut3Device, grade_fp8, grade_lut3, qg, to_bits
+from gpu_util import Fp8Device, Lut3Device, bits_to_bf16, grade_fp8, grade_lut3, qg, to_bits
 
 pytestmark = pytest.mark.gpu
 
@@ -48,6 +49,34 @@ def test_lut3_timeout_reported_and_context_survives():
     ws = q.Workspace()
     _timeout_then_recover(lambda w: q.qgemm_lut3(Xd, dev.Wq, dev.qmap, dev.scales, 1024, workspace=w),
                           lambda y: grade_lut3(p, y), ws)
+
+
+def test_bf16_timeout_reported_and_context_survives():
+    q = qg()
+    p = wl.make_bf16_problem(4, 1024, 5120, config_id=53)
+    W = torch.from_numpy(p.W.view(np.int16)).view(torch.bfloat16).cuda()
+    Xd = bits_to_bf16(p.X)
+    ws = q.Workspace()
+
+    def grade(y):
+        return oracle.within_budget(y, oracle.gemm_bf16(p.X, p.W), oracle.bf16_abs_mass(p.X, p.W), fmt="bf16")
+    _timeout_then_recover(lambda w: q.qgemm_bf16(Xd, W, workspace=w), grade, ws)
+
+
+def test_w8a8_timeout_reported_and_context_survives():
+    q = qg()
+    p = wl.make_w8a8_problem(160, 1152, 2048, config_id=54)
+    Xq_ref, Sx_ref = oracle.quantize_act_e4m3(p.X)
+    W = torch.from_numpy(p.W).cuda()
+    S = torch.from_numpy(p.S).cuda()
+    Xq, Sx = q.quantize_act_e4m3(bits_to_bf16(p.X))
+    assert q.last_device_status() == 0
+    ws = q.Workspace()
+
+    def grade(y):
+        return oracle.within_budget(y, oracle.qgemm_w8a8_block(Xq_ref, Sx_ref, p.W, p.S),
+                                    oracle.w8a8_abs_mass(Xq_ref, Sx_ref, p.W, p.S), fmt="bf16")
+    _timeout_then_recover(lambda w: q.qgemm_w8a8_block(Xq, Sx, W, S, workspace=w), grade, ws)
 
 
 def test_missing_workspace_is_rejected():
