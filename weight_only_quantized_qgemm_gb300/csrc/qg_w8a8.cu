@@ -294,8 +294,8 @@ __global__ void __launch_bounds__(W8a8Layout<NA>::kThreads, 1)
     const WaitCtl wc{p.timeout_ns, p.status, abort_flag};
     grid_dependents_launch();
 
-    // Every role runs one iteration per unit, and a unit's four MMAs take
-    // only a few hundred cycles: the loops avoid divisions (rings and tile
+    // Every role runs one iteration per unit, and a unit's MMAs take well
+    // under a microsecond: the loops avoid divisions (rings and tile
     // coordinates are stepped incrementally).  The producers and the factor
     // and fold warps wait in one lane; the MMA warp waits as a whole and
     // issues from one elected lane (issuing from a lone diverged lane
