@@ -189,3 +189,28 @@ def test_w8a8_tuner_installs_a_gated_grid():
         assert rep.ok, rep
     finally:
         q.dispatch_clear()
+
+
+def test_default_workspaces_are_per_stream():
+    """Split-K calls enqueued on two streams with the binding's default
+    workspaces (one per stream) overlap freely and all meet the rule."""
+    q = qg()
+    pa = cached(("fp8", 4, 1024, 5120, 74), lambda: wl.make_fp8_problem(4, 1024, 5120, config_id=74))
+    pb = cached(("fp8", 16, 5120, 5120, 75), lambda: wl.make_fp8_problem(16, 5120, 5120, config_id=75))
+    da, db = Fp8Device(pa), Fp8Device(pb)
+    Xa = torch.from_numpy(pa.X.view(np.int16)).view(torch.bfloat16).cuda()
+    Xb = torch.from_numpy(pb.X.view(np.int16)).view(torch.bfloat16).cuda()
+    sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+    torch.cuda.synchronize()
+    Ya = [torch.empty((4, 1024), dtype=torch.bfloat16, device="cuda") for _ in range(8)]
+    Yb = [torch.empty((16, 5120), dtype=torch.bfloat16, device="cuda") for _ in range(8)]
+    for i in range(8):
+        q.qgemm_fp8_block(Xa, da.W[0], da.S, Y=Ya[i], stream=sa)
+        q.qgemm_fp8_block(Xb, db.W[0], db.S, Y=Yb[i], stream=sb)
+    torch.cuda.synchronize()
+    assert q.last_device_status() == 0
+    for i in range(8):
+        ok, rep = grade_fp8(pa, to_bits(Ya[i]))
+        assert rep.ok, (i, rep)
+        ok, rep = grade_fp8(pb, to_bits(Yb[i]))
+        assert rep.ok, (i, rep)

@@ -140,7 +140,11 @@ def workspace_bytes(kind: int, M: int, N: int, K: int) -> int:
 class Workspace:
     """A zero-filled device byte buffer that grows on demand.  Calls leave
     its arrival counters at zero again (the partial-sum area in front of them
-    is scratch), so one buffer serves any sequence of calls on one stream."""
+    is scratch), so one buffer serves any sequence of calls on one stream
+    (calls that may run at the same time, on different streams, need one
+    buffer each).  Growing synchronises the device, so that no call still
+    uses the old buffer and the zero fill has landed before any stream uses
+    the new one."""
 
     def __init__(self, device=None):
         self.device = device
@@ -151,8 +155,11 @@ class Workspace:
         if nbytes == 0:
             return None
         if self.buf is None or self.buf.numel() < nbytes:
-            self.buf = torch.zeros(max(nbytes, 1 << 20), dtype=torch.uint8,
-                                   device=self.device or torch.cuda.current_device())
+            dev = self.device or torch.cuda.current_device()
+            if self.buf is not None:
+                torch.cuda.synchronize(dev)
+            self.buf = torch.zeros(max(nbytes, 1 << 20), dtype=torch.uint8, device=dev)
+            torch.cuda.synchronize(dev)
         return self.buf
 
     def reset(self):
@@ -166,7 +173,7 @@ _default_ws = {}
 _ws_need = {}
 
 
-def _workspace_for(kind, M, N, K, workspace, device):
+def _workspace_for(kind, M, N, K, workspace, device, stream=None):
     key = (kind, M, N, K, device)
     need = _ws_need.get(key)
     if need is None:
@@ -174,8 +181,12 @@ def _workspace_for(kind, M, N, K, workspace, device):
     if need == 0:
         return None, 0
     if workspace is None:
-        # the W8A8 kind's workspace layout differs from the decode kinds': one buffer each
-        workspace = _default_ws.setdefault((device, kind == KIND_W8A8), Workspace(device))
+        # one default buffer per device, stream (calls on different streams may
+        # overlap) and layout family (the W8A8 kind's differs from the others')
+        key = (device, _stream_ptr(stream), kind == KIND_W8A8)
+        workspace = _default_ws.get(key)
+        if workspace is None:
+            workspace = _default_ws[key] = Workspace(device)
     buf = workspace.get(need) if isinstance(workspace, Workspace) else workspace
     return buf.data_ptr(), buf.numel() * buf.element_size()
 
@@ -206,7 +217,7 @@ def qgemm_fp8_block(X, W, W_scale, Y=None, workspace=None, stream=None):
         raise ValueError("shape mismatch between X, W and W_scale")
     if Y is None:
         Y = torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
-    ws, wsb = _workspace_for(KIND_FP8_BLOCK, M, N, K, workspace, X.device)
+    ws, wsb = _workspace_for(KIND_FP8_BLOCK, M, N, K, workspace, X.device, stream)
     _check(lib.qgemm_fp8_block(X.data_ptr(), _ld(X), W.data_ptr(), W_scale.data_ptr(), Y.data_ptr(),
                                _ld(Y), M, N, K, ws, wsb, _stream_ptr(stream)), "qgemm_fp8_block")
     return Y
@@ -246,7 +257,7 @@ def qgemm_fp8_block_multi(X, weights, Ys=None, workspace=None, stream=None):
         outs.append(Y)
         segs[j] = Fp8Segment(W.data_ptr(), S.data_ptr(), Y.data_ptr(), _ld(Y), N)
         rows += -(-N // 128) * 128
-    ws, wsb = _workspace_for(KIND_FP8_BLOCK, M, rows, K, workspace, X.device)
+    ws, wsb = _workspace_for(KIND_FP8_BLOCK, M, rows, K, workspace, X.device, stream)
     _check(lib.qgemm_fp8_block_multi(X.data_ptr(), _ld(X), ctypes.cast(segs, ctypes.c_void_p), len(weights), M, K,
                                      ws, wsb, _stream_ptr(stream)), "qgemm_fp8_block_multi")
     return outs
@@ -290,7 +301,7 @@ def qgemm_fp8_block_host(X, W, W_scale, Y=None, X_stage=None, workspace=None, st
                                                              device=W.device)
     elif not X_stage.is_cuda or X_stage.numel() * X_stage.element_size() < M * K * 2:
         raise ValueError("X_stage must be a device buffer of at least M*K bfloat16 elements")
-    ws, wsb = _workspace_for(KIND_FP8_BLOCK, M, N, K, workspace, W.device)
+    ws, wsb = _workspace_for(KIND_FP8_BLOCK, M, N, K, workspace, W.device, stream)
     _check(lib.qgemm_fp8_block_host(X.data_ptr(), _ld(X), W.data_ptr(), W_scale.data_ptr(), Y.data_ptr(),
                                     _ld(Y), M, N, K, X_stage.data_ptr(), ws, wsb, _stream_ptr(stream)),
            "qgemm_fp8_block_host")
@@ -313,7 +324,7 @@ def qgemm_lut3(X, Wq, qmap, scales, N: int, Y=None, workspace=None, stream=None)
         raise ValueError("packed weights are smaller than pack_lut3 produces for this shape")
     if Y is None:
         Y = torch.empty((M, N), dtype=torch.float16, device=X.device)
-    ws, wsb = _workspace_for(KIND_LUT3, M, N, K, workspace, X.device)
+    ws, wsb = _workspace_for(KIND_LUT3, M, N, K, workspace, X.device, stream)
     _check(lib.qgemm_lut3(X.data_ptr(), _ld(X), Wq.data_ptr(), qmap.data_ptr(), scales.data_ptr(),
                           Y.data_ptr(), _ld(Y), M, N, K, ws, wsb, _stream_ptr(stream)), "qgemm_lut3")
     return Y
@@ -364,7 +375,7 @@ def qgemm_w8a8_block(Xq, X_scale, W, W_scale, Y=None, workspace=None, stream=Non
         raise ValueError("shape mismatch between Xq, X_scale, W and W_scale")
     if Y is None:
         Y = torch.empty((M, N), dtype=torch.bfloat16, device=Xq.device)
-    ws, wsb = _workspace_for(KIND_W8A8, M, N, K, workspace, Xq.device)
+    ws, wsb = _workspace_for(KIND_W8A8, M, N, K, workspace, Xq.device, stream)
     _check(lib.qgemm_w8a8_block(Xq.data_ptr(), _ld(Xq), X_scale.data_ptr(), _ld(X_scale), W.data_ptr(),
                                 W_scale.data_ptr(), Y.data_ptr(), _ld(Y), M, N, K, ws, wsb, _stream_ptr(stream)),
            "qgemm_w8a8_block")
@@ -395,7 +406,7 @@ def qgemm_bf16(X, W, Y=None, workspace=None, stream=None):
         raise ValueError("shape mismatch between X and W")
     if Y is None:
         Y = torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
-    ws, wsb = _workspace_for(KIND_BF16, M, N, K, workspace, X.device)
+    ws, wsb = _workspace_for(KIND_BF16, M, N, K, workspace, X.device, stream)
     _check(lib.qgemm_bf16(X.data_ptr(), _ld(X), W.data_ptr(), Y.data_ptr(), _ld(Y), M, N, K, ws, wsb,
                           _stream_ptr(stream)), "qgemm_bf16")
     return Y
