@@ -50,6 +50,21 @@ def test_device_work_split(M, N, K):
     _check_schedule(ranges, info, U, KB)
 
 
+@pytest.mark.parametrize("M,N,K", [(64, 17408, 5120), (256, 17408, 5120), (160, 1152, 2048), (100, 300, 272),
+                                   (1024, 5120, 17408)])
+def test_device_work_split_w8a8(M, N, K):
+    """The W8A8 kind's work split: tiles of 128 weight rows x R activation
+    rows (R = 64 up to 64 rows, else 128), units of two 128-wide K blocks."""
+    q = qg()
+    R = 64 if M <= 64 else 128
+    KU = -(-K // 256)
+    U = (-(-N // 128)) * (-(-M // R)) * KU
+    ranges, info = q.debug_schedule(q.KIND_W8A8, M, N, K)
+    assert q.last_device_status() == 0
+    assert ranges.shape[0] == q.dispatch_get(q.KIND_W8A8, M, N, K)
+    _check_schedule(ranges, info, U, KU)
+
+
 @pytest.mark.parametrize("G", [1, 3, 40, 41, 77, 152])
 def test_device_work_split_forced_grids(G):
     q = qg()
