@@ -841,7 +841,8 @@ def main():
             secondary = secondary_lines(torch, qg, stream, peak)
         except Exception as e:  # secondary numbers must not hide the headline
             secondary["error"] = repr(e)[:300]
-        cpu, _ = cpu_baseline(M, N, K, cid)
+        if world == 1:   # the CPU baseline is taken at one GPU only
+            cpu, _ = cpu_baseline(M, N, K, cid)
 
     line = {
         "metric": METRIC,
