@@ -93,7 +93,8 @@ def test_quantize_act_bit_exact(M, K):
 
 # ------------------------------------------------------------------ GEMM
 @pytest.mark.parametrize("M,N,K", [(33, 256, 512), (64, 384, 1024), (100, 300, 272), (1, 128, 128),
-                                   (32, 256, 512), (129, 1000, 2064), (256, 2048, 4096), (48, 136, 5120)])
+                                   (32, 256, 512), (129, 1000, 2064), (256, 2048, 4096), (48, 136, 5120),
+                                   (33, 128, 16), (65, 129, 144)])
 def test_w8a8_shapes(M, N, K):
     q = qg()
     p = _problem(M, N, K)
@@ -214,3 +215,20 @@ def test_w8a8_and_decode_calls_interleave():
             assert q.last_device_status() == 0
             ok, rep = grade_fp8(pf, to_bits(Yf))
             assert rep.ok, rep
+
+
+def test_w8a8_k_zero_writes_zeros():
+    """K = 0: every output is the empty sum, 0."""
+    q = qg()
+    M, N = 40, 300
+    Y = torch.full((M, N), 3.0, dtype=torch.bfloat16, device="cuda")
+    W = torch.zeros((N, 16), dtype=torch.uint8, device="cuda")
+    S = torch.ones((3, 1), dtype=torch.float32, device="cuda")
+    Xq = torch.zeros((M, 16), dtype=torch.uint8, device="cuda")
+    Sx = torch.zeros((1, 64), dtype=torch.float32, device="cuda")
+    r = q.lib.qgemm_w8a8_block(Xq.data_ptr(), 16, Sx.data_ptr(), 64, W.data_ptr(), S.data_ptr(), Y.data_ptr(), N,
+                               M, N, 0, None, 0, None)
+    assert r == 0
+    torch.cuda.synchronize()
+    assert q.last_device_status() == 0
+    assert torch.count_nonzero(Y.float()) == 0
