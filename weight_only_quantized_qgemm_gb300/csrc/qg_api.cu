@@ -878,6 +878,6 @@ const char* qg_status_string(qg_status s) {
     return "unknown status";
 }
 
-const char* qg_version(void) { return "0.1.0"; }
+const char* qg_version(void) { return "0.2.0"; }
 
 }  // extern "C"
