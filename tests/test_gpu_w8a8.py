@@ -128,6 +128,30 @@ def test_w8a8_strided_and_padding_untouched():
     assert np.all(to_bits(Y[:, N:]) == 0x7FC1)
 
 
+@pytest.mark.parametrize("M,N,y_pad,shift", [(70, 504, 8, 0), (130, 248, 24, 0), (33, 384, 0, 0),
+                                             (70, 500, 12, 0), (70, 504, 8, 1)])
+def test_w8a8_y_store_paths(M, N, y_pad, shift):
+    """Y through the TMA store (Y 16-byte aligned, ldy and N multiples of 8:
+    ragged last tiles clipped at N and at M, padding columns and the rows
+    below Y untouched) and through plain stores (N % 8 != 0; Y starting one
+    element in, not 16-byte aligned)."""
+    q = qg()
+    K = 784
+    p = _problem(M, N, K)
+    Xq, Sx = _quantized(p)
+    W = torch.from_numpy(p.W).cuda()
+    S = torch.from_numpy(p.S).cuda()
+    ldsx = max(32, -(-M // 32) * 32)
+    Y = torch.empty((M + 40, N + y_pad + 8), dtype=torch.bfloat16, device="cuda")
+    Y.view(torch.int16).fill_(0x7FC1)
+    q.qgemm_w8a8_block(_codes_dev(Xq), _scales_dev(Sx, ldsx), W, S, Y=Y[:M, shift:shift + N])
+    assert q.last_device_status() == 0
+    bits = to_bits(Y)
+    _grade(Xq, Sx, p.W, p.S, bits[:M, shift:shift + N])
+    assert np.all(bits[:M, :shift] == 0x7FC1) and np.all(bits[:M, shift + N:] == 0x7FC1)
+    assert np.all(bits[M:] == 0x7FC1)
+
+
 def test_w8a8_grids_agree_and_repeat():
     """Forced grids (one CTA per tile, stream-K over several counts) all meet
     the rule; each grid gives the same bits twice; the workspace's arrival

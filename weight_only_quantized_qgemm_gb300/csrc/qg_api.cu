@@ -650,7 +650,7 @@ qg_status qgemm_w8a8_block(const uint8_t* Xq, int64_t ldxq, const float* X_scale
     if (!make_tmap(&tmX, Xq, CU_TENSOR_MAP_DATA_TYPE_UINT8, static_cast<uint64_t>(K), static_cast<uint64_t>(M),
                    static_cast<uint64_t>(ldxq), 128, static_cast<uint32_t>(s.nmma)))
         return QG_ERR_CUDA;
-    W8a8Args a;
+    W8a8Args a{};
     a.Sx = X_scale;
     a.ldsx = ldsx;
     a.S = W_scale;
@@ -660,6 +660,12 @@ qg_status qgemm_w8a8_block(const uint8_t* Xq, int64_t ldxq, const float* X_scale
     a.N = N;
     a.K = K;
     a.ws = need > 0 ? workspace : nullptr;
+    // Y by TMA stores where its alignment allows (see W8a8Args); N % 8 == 0
+    // too, since the store writes the 16-byte granule that holds column N - 1
+    // whole (measured: columns up to the next multiple of 8 were written)
+    a.y_tma = aligned16(Y) && ldy % 8 == 0 && N % 8 == 0 &&
+              make_tmap(&a.tmY, Y, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<uint64_t>(N),
+                        static_cast<uint64_t>(M), static_cast<uint64_t>(ldy) * 2, 32, 16, CU_TENSOR_MAP_SWIZZLE_NONE);
     return launch_w8a8(a, s, *tmW, tmX, launch_ctl(d), stream) == cudaSuccess ? QG_OK : QG_ERR_CUDA;
 }
 

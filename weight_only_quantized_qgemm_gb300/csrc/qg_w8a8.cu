@@ -33,7 +33,8 @@
 //               ahead, one unit per lane) in a ring of its own, so that an
 //               activation slot is free again as soon as its MMAs complete.
 //   warps 4-    fold / epilogue: NA/16 warps, warp w reading TMEM lane
-//               quadrant w % 4 and 64 of the NA columns.
+//               quadrant w % 4 and 64 of the NA columns; a finished tile's
+//               outputs go out through shared memory by TMA stores.
 #include "qg_gemm.cuh"
 #include "qg_w8a8.h"
 
@@ -60,12 +61,17 @@ struct W8a8Layout {
     static constexpr int kAcc = 512 / (kBlk * NA);            // TMEM accumulator sets (kBlk x NA columns each)
     static constexpr int kGStages = 2 * kAcc;                 // factor ring (kBlk x NA floats a slot)
     static constexpr int kGSlot = kBlk * NA * 4;
-    static constexpr int kReserve = kGStages * kGSlot + 8 * 96 + 64 + 1024;   // + barriers, misc, alignment
+    // per fold warp, two output staging buffers of 32 weight rows x 16
+    // activation rows of BF16 (the boxes of the TMA stores of Y)
+    static constexpr int kStageBuf = 32 * 16 * 2;
+    static constexpr int kStageWarp = 2 * kStageBuf;
+    static constexpr int kReserve = kGStages * kGSlot + kFold * kStageWarp + 8 * 96 + 64 + 1024;   // + barriers, misc, alignment
     static constexpr int kWFit = (232448 - kXStages * kXSlot - kReserve) / kWBytes;
     static constexpr int kWStages = kWFit < 12 ? kWFit : 12;
     static constexpr int kXOff = kWStages * kWBytes;
     static constexpr int kGOff = kXOff + kXStages * kXSlot;
-    static constexpr int kBarOff = kGOff + kGStages * kGSlot;
+    static constexpr int kStageOff = kGOff + kGStages * kGSlot;
+    static constexpr int kBarOff = kStageOff + kFold * kStageWarp;
     static constexpr int kNumBars = 2 * kWStages + 2 * kXStages + 2 * kGStages + 2 * kAcc;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     static constexpr int kSmemBytes = kMiscOff + 64 + 1024;
@@ -91,15 +97,53 @@ __device__ __forceinline__ float4* part_slot(const Params& p, int cta, int which
     return reinterpret_cast<float4*>(p.part) + (static_cast<size_t>(cta) * 2 + which) * (NA / 4) * 128;
 }
 
+// Where a fold warp's outputs go: through its staging buffers and TMA
+// stores of the Y map (Y 16-byte aligned, ldy and N multiples of 8), else by
+// plain stores.
+struct YOut {
+    const CUtensorMap* map;
+    int tma;
+    uint8_t* stage;      // the warp's two staging buffers
+};
+
 // Output rows of tile t = (weight tile tn, activation row block tm), t = tn *
 // tm_count + tm: weight row n = tn * 128 + row, activation rows tm * NA + h *
-// 64 + j for the fold warp's column half h.
+// 64 + j for the fold warp's column half h (row = q * 32 + lane).
+//
+// TMA path: four boxes of 32 weight rows x 16 activation rows, staged as
+// [m][n] BF16 (64 bytes per activation row) in two alternating buffers; a
+// buffer is rewritten once the store issued from it two boxes earlier has
+// read it.  The store skips rows m >= M and columns n >= N.  The stores are
+// asynchronous, so the fold goes on while they drain (scattered 2-byte
+// stores held the fold warps for microseconds per tile, with the MMAs
+// waiting behind them).
 template <int NA>
-__device__ __forceinline__ void store_cols(const Params& p, int tm_count, int tile, int row, int h,
+__device__ __forceinline__ void store_cols(const Params& p, const YOut& yo, int tm_count, int tile, int row, int h,
                                            const float (&v)[kFoldCols]) {
     const int tn = tile / tm_count;
     const int m0 = (tile - tn * tm_count) * NA + h * kFoldCols;
     const int n = tn * 128 + row;
+    if (yo.tma) {
+        const int lane = row & 31;
+#pragma unroll
+        for (int r = 0; r < kFoldCols / 16; ++r) {
+            uint8_t* buf = yo.stage + (r & 1) * (32 * 16 * 2);
+            if (lane == 0) bulk_wait_read<1>();
+            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                *reinterpret_cast<__nv_bfloat16*>(buf + j * 64 + lane * 2) = __float2bfloat16_rn(v[16 * r + j]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                // lane 0's n is the box's first column; a box wholly outside Y
+                // is not issued, but its (empty) group keeps the alternation
+                if (n < p.N && m0 + 16 * r < p.M) tma_store_2d(yo.map, smem_u32(buf), n, m0 + 16 * r);
+                bulk_commit();
+            }
+        }
+        return;
+    }
     if (n >= p.N) return;
     const gemm::Seg sg = p.seg[0];
     __nv_bfloat16* Y = static_cast<__nv_bfloat16*>(sg.Y);
@@ -113,8 +157,8 @@ __device__ __forceinline__ void store_cols(const Params& p, int tm_count, int ti
 // pieces copied by 16-byte cp.async before any is read back), then stored;
 // resets the warp's arrival counter.
 template <int NA>
-__device__ __forceinline__ void finish_tile(const Params& p, int tm_count, int tile, int which, int split_info,
-                                            int q, int h, int fw, int lane, uint8_t* scratch) {
+__device__ __forceinline__ void finish_tile(const Params& p, const YOut& yo, int tm_count, int tile, int which,
+                                            int split_info, int q, int h, int fw, int lane, uint8_t* scratch) {
     using L = W8a8Layout<NA>;
     constexpr int kF4 = kFoldCols / 4;
     constexpr int kPieces = L::kScratchWarp / L::kPieceBytes;
@@ -150,7 +194,7 @@ __device__ __forceinline__ void finish_tile(const Params& p, int tm_count, int t
             }
         }
     }
-    store_cols<NA>(p, tm_count, tile, row, h, acc);
+    store_cols<NA>(p, yo, tm_count, tile, row, h, acc);
     __syncwarp();
     if (lane == 0) p.cnt[tile * L::kFold + fw] = 0u;   // ready for the next call
 }
@@ -160,14 +204,15 @@ __device__ __forceinline__ void finish_tile(const Params& p, int tm_count, int t
 // finishes the tile now when `scratch` is given, else returns true (finished
 // at the end of the range, when shared memory is idle).
 template <int NA>
-__device__ __forceinline__ bool end_piece(const Params& p, int tm_count, const float (&outer)[kFoldCols], int tile,
-                                          int kb, long long u, long long u0, int first_tile, int split_info, int q,
-                                          int h, int fw, int lane, uint8_t* scratch) {
+__device__ __forceinline__ bool end_piece(const Params& p, const YOut& yo, int tm_count,
+                                          const float (&outer)[kFoldCols], int tile, int kb, long long u,
+                                          long long u0, int first_tile, int split_info, int q, int h, int fw,
+                                          int lane, uint8_t* scratch) {
     using L = W8a8Layout<NA>;
     const int row = q * 32 + lane;
     const bool whole = (kb == p.KB - 1) && (u - kb >= u0);
     if (whole) {
-        store_cols<NA>(p, tm_count, tile, row, h, outer);
+        store_cols<NA>(p, yo, tm_count, tile, row, h, outer);
         return false;
     }
     const int which = (tile == first_tile) ? 0 : 1;
@@ -186,7 +231,7 @@ __device__ __forceinline__ bool end_piece(const Params& p, int tm_count, const f
     if (static_cast<int>(prev) != cl - cf) return false;
     __threadfence();
     if (scratch == nullptr) return true;
-    finish_tile<NA>(p, tm_count, tile, which, split_info, q, h, fw, lane, scratch);
+    finish_tile<NA>(p, yo, tm_count, tile, which, split_info, q, h, fw, lane, scratch);
     return false;
 }
 
@@ -226,8 +271,9 @@ struct UnitPosT {
 
 template <int NA>
 __global__ void __launch_bounds__(W8a8Layout<NA>::kThreads, 1)
-    w8a8_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, const Params p,
-                const float* __restrict__ sx, int64_t ldsx, int tm_count) {
+    w8a8_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                const __grid_constant__ CUtensorMap tmY, const Params p, const float* __restrict__ sx, int64_t ldsx,
+                int tm_count, int y_tma) {
     using L = W8a8Layout<NA>;
     using UnitPos = UnitPosT<NA>;
     constexpr int kWStages = L::kWStages;
@@ -450,6 +496,8 @@ __global__ void __launch_bounds__(W8a8Layout<NA>::kThreads, 1)
         const uint32_t tl = tmem + (static_cast<uint32_t>(q * 32) << 16) + h * kFoldCols;
         const int first_tile = static_cast<int>(u0 / p.KB);
         const int split_info = gemm::split_info_lane(p, u0, u1, lane);
+        const YOut yo{&tmY, y_tma, gbase + L::kStageOff + fw * L::kStageWarp};
+        if (y_tma && lane == 0) prefetch_tmap(&tmY);
         // Y and the workspace may still be in use by the preceding grid
         grid_dependency_wait();
         bool deferred = false;
@@ -510,14 +558,16 @@ __global__ void __launch_bounds__(W8a8Layout<NA>::kThreads, 1)
                 if (lane == 0) idle = wait_bounded(xempty(i % kXStages), (i / kXStages) & 1, wc);
                 if (!__shfl_sync(0xffffffffu, idle, 0)) break;
             }
-            if (end_piece<NA>(p, tm_count, outer, cur.tile, cur.kb, u0 + i, u0, first_tile, split_info, q, h, fw,
-                              lane, last ? gbase : nullptr))
+            if (end_piece<NA>(p, yo, tm_count, outer, cur.tile, cur.kb, u0 + i, u0, first_tile, split_info, q, h,
+                              fw, lane, last ? gbase : nullptr))
                 deferred = true;
             if (last && deferred)
-                finish_tile<NA>(p, tm_count, first_tile, 0, split_info, q, h, fw, lane, gbase);
+                finish_tile<NA>(p, yo, tm_count, first_tile, 0, split_info, q, h, fw, lane, gbase);
 #pragma unroll
             for (int j = 0; j < kFoldCols; ++j) outer[j] = 0.0f;
         }
+        // the staging buffers must have been read before the CTA's shared memory goes
+        if (y_tma && lane == 0) bulk_wait_read<0>();
     }
 
     tc_fence_before();
@@ -615,7 +665,7 @@ static cudaError_t launch_w8a8_na(const W8a8Args& a, const Schedule& s, const CU
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    return cudaLaunchKernelEx(&cfg, w8a8_kernel<NA>, tmW, tmX, p, a.Sx, a.ldsx, tm_count);
+    return cudaLaunchKernelEx(&cfg, w8a8_kernel<NA>, tmW, tmX, a.tmY, p, a.Sx, a.ldsx, tm_count, a.y_tma);
 }
 
 cudaError_t launch_w8a8(const W8a8Args& a, const Schedule& s, const CUtensorMap& tmW, const CUtensorMap& tmX,

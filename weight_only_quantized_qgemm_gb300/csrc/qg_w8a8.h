@@ -16,6 +16,11 @@ struct W8a8Args {
     int64_t ldy;
     int M, N, K;
     void* ws;
+    // Y as a BF16 [M, N] tensor map (row pitch ldy * 2 bytes, boxes of 32
+    // columns x 16 rows, no swizzle) when y_tma != 0, which needs Y 16-byte
+    // aligned and ldy and N multiples of 8; else the kernel stores Y directly
+    CUtensorMap tmY;
+    int y_tma;
 };
 
 // The W8A8 kernel's activation rows per tile (its MMA N) for a batch size.
