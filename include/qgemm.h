@@ -382,8 +382,9 @@ size_t qg_workspace_bytes_max_w8a8(int M, int N);
  * (FLUTE "optimized_w3" page, Results: a candidate is accepted only after
  * its output is checked).  The built-in schedule's output, written to Y_ref
  * (a device buffer shaped like Y), is the reference.  Candidate grids (one CTA
- * per 128-row tile, 2..8 CTAs per tile, and 4/8..8/8 of the SMs, each at most
- * the SM count) then run on the caller's buffers; a candidate whose output is
+ * per 128-row tile, 2..8 CTAs per tile, 4/8..8/8 of the SMs, and, with more
+ * tiles than SMs, the largest grid over which whole tiles divide evenly; each
+ * at most the SM count) then run on the caller's buffers; a candidate whose output is
  * not finite, or differs from the reference by more than a relative
  * Frobenius distance of 1e-3 or anywhere by more than 1e-2 of the
  * reference's largest magnitude (a reordered FP32 sum moves results by a

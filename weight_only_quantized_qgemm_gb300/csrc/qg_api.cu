@@ -121,7 +121,11 @@ namespace {
 //    boundaries: kStraddleCostUnits more (on down at 32 rows, 152 CTAs ran
 //    25.5 us against 27.4 at 120; on the 5120 x 5120 shape 14.4 against 13.2).
 // Ties go to the grid without splits, then to whole multiples.  More tiles
-// than SMs: stream-K, one CTA per SM.
+// than SMs: stream-K, one CTA per SM, unless whole tiles divide evenly over
+// a grid (the largest divisor of the tile count up to the SM count) whose
+// busiest CTA costs fewer units than stream-K's plus its split tail (W8A8
+// at 256 rows: 136 CTAs of two whole tiles ran 36.5 us against 41.1 us for
+// stream-K over 152).
 constexpr int kMaxPiecesPerTile = 8;
 constexpr long long kSplitCostUnits = 10;
 constexpr long long kStraddleCostUnits = 5;
@@ -164,6 +168,7 @@ Schedule choose_schedule(int kind, int M, int N, int K, int sms) {
     s.KU = kind == QG_KIND_W8A8 ? (K + 255) / 256 : (K + 127) / 128;
     s.U = static_cast<long long>(s.T) * s.KU;
     const int forced = table_lookup(kind, M, N, K);
+    const bool unit_bound = kind == QG_KIND_W8A8 || (kind == QG_KIND_FP8_BLOCK && M > 16);
     long long g = sms;
     if (forced > 0) {
         g = forced;
@@ -182,11 +187,18 @@ Schedule choose_schedule(int kind, int M, int N, int K, int sms) {
             best = cost_of(gb, 0);
             g = gb;
         }
-        const bool unit_bound = kind == QG_KIND_W8A8 || (kind == QG_KIND_FP8_BLOCK && M > 16);
         const long long gc = sms < s.U ? sms : s.U;
         if (unit_bound && gc != g && cost_of(gc, kStraddleCostUnits) < best) g = gc;
     } else {
         if (g > s.U) g = s.U;
+        const long long stream_cost =
+            ceil_div(s.U, g) + (splits(s.U, s.KU, static_cast<int>(g)) ? kSplitCostUnits : 0) +
+            (unit_bound ? kStraddleCostUnits : 0);
+        for (long long d = sms; d >= 1; --d) {
+            if (s.T % d != 0) continue;
+            if (s.T / d * s.KU < stream_cost) g = d;
+            break;
+        }
     }
     s.G = static_cast<int>(g);
     s.max_ctas = sms > s.G ? sms : s.G;

@@ -50,8 +50,9 @@ bool gate(const std::vector<uint16_t>& got, const std::vector<uint16_t>& ref, bo
     return std::sqrt(num / den) <= 1e-3 && dmax <= 1e-2 * rmax;
 }
 
-// Candidate grids: one CTA per tile, 2..8 CTAs per tile, and fractions of the
-// SMs, each at most the SM count and the number of work units.
+// Candidate grids: one CTA per tile, 2..8 CTAs per tile, fractions of the
+// SMs, and (more tiles than SMs) the largest grid over which whole tiles
+// divide evenly, each at most the SM count and the number of work units.
 std::vector<int> candidates(int T, long long U, int sms) {
     std::vector<int> c;
     auto add = [&](long long g) {
@@ -62,6 +63,12 @@ std::vector<int> candidates(int T, long long U, int sms) {
     };
     for (int k = 1; k <= 8; ++k) add(static_cast<long long>(k) * T);
     for (int e = 8; e >= 4; --e) add(static_cast<long long>(sms) * e / 8);
+    if (T > sms)
+        for (int d = sms; d >= 1; --d)
+            if (T % d == 0) {
+                add(d);
+                break;
+            }
     return c;
 }
 
