@@ -123,9 +123,10 @@ namespace {
 // Ties go to the grid without splits, then to whole multiples.  More tiles
 // than SMs: stream-K, one CTA per SM, unless whole tiles divide evenly over
 // a grid (the largest divisor of the tile count up to the SM count) whose
-// busiest CTA costs fewer units than stream-K's plus its split tail (W8A8
-// at 256 rows: 136 CTAs of two whole tiles ran 36.5 us against 41.1 us for
-// stream-K over 152).
+// busiest CTA costs fewer units than stream-K's plus its split and straddle
+// tails (W8A8 at 256 rows: 136 CTAs of two whole tiles ran 36.5 us against
+// 41.1 us for stream-K over 152; the BF16 lm_head shape, 256 tiles, 50.2
+// against 52.1 us on 128 CTAs).
 constexpr int kMaxPiecesPerTile = 8;
 constexpr long long kSplitCostUnits = 10;
 constexpr long long kStraddleCostUnits = 5;
@@ -191,9 +192,9 @@ Schedule choose_schedule(int kind, int M, int N, int K, int sms) {
         if (unit_bound && gc != g && cost_of(gc, kStraddleCostUnits) < best) g = gc;
     } else {
         if (g > s.U) g = s.U;
+        // with more tiles than SMs every stream-K piece straddles tiles
         const long long stream_cost =
-            ceil_div(s.U, g) + (splits(s.U, s.KU, static_cast<int>(g)) ? kSplitCostUnits : 0) +
-            (unit_bound ? kStraddleCostUnits : 0);
+            ceil_div(s.U, g) + (splits(s.U, s.KU, static_cast<int>(g)) ? kSplitCostUnits + kStraddleCostUnits : 0);
         for (long long d = sms; d >= 1; --d) {
             if (s.T % d != 0) continue;
             if (s.T / d * s.KU < stream_cost) g = d;
