@@ -357,10 +357,14 @@ qg_status qg_dequant_lut3(const void *Wq, const void *qmap, const void *scales,
  *   number); ctas == 0 removes it.  M in 1..32 (1..65536 for QG_KIND_W8A8).
  * qg_dispatch_get: the grid the next call of the shape launches on the
  *   current device (0 for invalid arguments).
+ * qg_dispatch_rule: the grid the built-in cost rule picks for the shape on
+ *   a device with `sms` SMs, whatever the table holds (host only, no CUDA
+ *   call; 0 for invalid arguments).
  * qg_dispatch_clear: removes every entry.
  */
 qg_status qg_dispatch_set(int kind, int M, int N, int K, int ctas);
 int qg_dispatch_get(int kind, int M, int N, int K);
+int qg_dispatch_rule(int kind, int M, int N, int K, int sms);
 void qg_dispatch_clear(void);
 
 /*

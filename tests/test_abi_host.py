@@ -279,3 +279,47 @@ def test_bf16_and_w8a8_tuner_argument_validation(qg):
              None) == 2
     assert qg.lib.qg_workspace_bytes_max_w8a8(0, 256) == 0
     assert qg.lib.qg_workspace_bytes_max_w8a8(64, 0) == 0
+
+
+# ------------------------------------------------------------------ dispatch rule (host only)
+# The built-in rule on a 152-SM GB300 against the grids the exactness-gated
+# tuner picked when it timed every candidate on the GPU (the bench's tuned
+# lines): the rule was set from those measurements and should keep matching.
+@pytest.mark.parametrize("kind,M,N,K,grid", [
+    (0, 16, 17408, 5120, 136), (0, 1, 17408, 5120, 136),        # gate/up: one CTA per tile
+    (0, 16, 5120, 17408, 120), (0, 32, 5120, 17408, 152),       # down: 3 per tile; stream-K at 32 rows
+    (0, 16, 6144, 5120, 144), (0, 16, 5120, 5120, 120), (0, 16, 1024, 5120, 64),
+    (1, 16, 28672, 8192, 152),                                  # LUT3: stream-K over 224 tiles
+    (2, 16, 32768, 5120, 128),                                  # BF16 lm_head: two whole tiles per CTA
+    (3, 64, 17408, 5120, 136), (3, 256, 17408, 5120, 136), (3, 1024, 17408, 5120, 152),
+])
+def test_dispatch_rule_matches_the_tuned_grids(qg, kind, M, N, K, grid):
+    assert qg.dispatch_rule(kind, M, N, K, 152) == grid
+
+
+def test_dispatch_rule_invariants(qg):
+    """Every grid is 1 .. min(SMs, work units); with more tiles than SMs a
+    grid below the SM count holds whole tiles only; with tiles <= SMs the
+    grid is one CTA per tile, a whole multiple of the tiles, or one CTA per
+    SM; invalid arguments give 0."""
+    for kind, Ms, kmul in ((0, (1, 16, 17, 32), 16), (1, (1, 16, 32), 128), (2, (1, 32), 8), (3, (33, 64, 65, 300, 4096), 16)):
+        for M in Ms:
+            for N in (128, 200, 1024, 5120, 17408, 32768, 65536):
+                for K in (kmul, 1024, 5120, 17408):
+                    if K % kmul:
+                        continue
+                    rows = (64 if M <= 64 else 128) if kind == 3 else None
+                    T = -(-N // 128) * (-(-M // rows) if rows else 1)
+                    KU = -(-K // 256) if kind == 3 else -(-K // 128)
+                    U = T * KU
+                    for sms in (1, 8, 76, 148, 152, 160):
+                        g = qg.dispatch_rule(kind, M, N, K, sms)
+                        assert 1 <= g <= min(sms, U), (kind, M, N, K, sms, g)
+                        if T > sms and g < sms:
+                            assert T % g == 0, (kind, M, N, K, sms, g)
+                        if T <= sms:
+                            assert g == min(sms, U) or g % T == 0, (kind, M, N, K, sms, g)
+    assert qg.dispatch_rule(0, 0, 128, 128, 152) == 0
+    assert qg.dispatch_rule(0, 33, 128, 128, 152) == 0
+    assert qg.dispatch_rule(0, 1, 128, 128, 0) == 0
+    assert qg.dispatch_rule(9, 1, 128, 128, 152) == 0

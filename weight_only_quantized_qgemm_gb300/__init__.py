@@ -37,7 +37,7 @@ __all__ = [
     "QgemmError", "LIB_PATH", "lib", "status_string", "workspace_bytes", "Workspace",
     "qgemm_fp8_block", "qgemm_fp8_block_multi", "qgemm_fp8_block_host", "Fp8Segment", "MAX_SEGMENTS", "qgemm_lut3", "pack_lut3", "unpack_lut3", "lut3_packed_bytes",
     "debug_fp8_split", "dequant_lut3", "last_device_status", "set_wait_timeout_ns",
-    "set_fault_injection", "set_weight_prefetch_overlap", "dispatch_set", "dispatch_get", "dispatch_clear",
+    "set_fault_injection", "set_weight_prefetch_overlap", "dispatch_set", "dispatch_get", "dispatch_rule", "dispatch_clear",
     "debug_schedule", "tune_fp8", "tune_lut3", "workspace_bytes_max", "qgemm_bf16", "KIND_BF16", "KIND_FP8_BLOCK", "KIND_LUT3", "STATUS",
     "quantize_act_e4m3", "qgemm_w8a8_block", "qgemm_w8a8", "KIND_W8A8", "MAX_M_W8A8",
     "tune_bf16", "tune_w8a8", "workspace_bytes_max_w8a8",
@@ -90,6 +90,7 @@ _SIGS = {
     "qg_debug_schedule": (_I, [_I, _I, _I, _I, _P, _P, _P, _I, _P]),
     "qg_dispatch_set": (_I, [_I, _I, _I, _I, _I]),
     "qg_dispatch_get": (_I, [_I, _I, _I, _I]),
+    "qg_dispatch_rule": (_I, [_I, _I, _I, _I, _I]),
     "qg_dispatch_clear": (None, []),
     "qg_workspace_bytes_max": (_S, [_I]),
     "qg_workspace_bytes_max_w8a8": (_S, [_I, _I]),
@@ -488,6 +489,13 @@ def dispatch_set(kind: int, M: int, N: int, K: int, ctas: int) -> None:
 def dispatch_get(kind: int, M: int, N: int, K: int) -> int:
     """The grid (CTA count) the next call of this shape launches."""
     return int(lib.qg_dispatch_get(kind, M, N, K))
+
+
+def dispatch_rule(kind: int, M: int, N: int, K: int, sms: int) -> int:
+    """The grid the built-in cost rule picks for this shape on a device with
+    `sms` SMs, ignoring the dispatch table (host only; 0 for invalid
+    arguments)."""
+    return int(lib.qg_dispatch_rule(kind, M, N, K, sms))
 
 
 def dispatch_clear() -> None:

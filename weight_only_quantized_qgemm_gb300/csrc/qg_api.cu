@@ -160,7 +160,8 @@ int table_lookup(int kind, int M, int N, int K) {
     return 0;
 }
 
-Schedule choose_schedule(int kind, int M, int N, int K, int sms) {
+// The schedule of a shape on `sms` SMs, with `forced` > 0 a dispatch-table grid.
+Schedule schedule_for(int kind, int M, int N, int K, int sms, int forced) {
     Schedule s;
     s.nmma = kind == QG_KIND_W8A8 ? w8a8_tile_rows(M) : M <= 16 ? 16 : 32;
     // W8A8 tiles are 128 weight rows x nmma activation rows, weight-tile-major
@@ -168,7 +169,6 @@ Schedule choose_schedule(int kind, int M, int N, int K, int sms) {
     // one unit = 128 rows x one 128-wide K block (W8A8: two blocks)
     s.KU = kind == QG_KIND_W8A8 ? (K + 255) / 256 : (K + 127) / 128;
     s.U = static_cast<long long>(s.T) * s.KU;
-    const int forced = table_lookup(kind, M, N, K);
     const bool unit_bound = kind == QG_KIND_W8A8 || (kind == QG_KIND_FP8_BLOCK && M > 16);
     long long g = sms;
     if (forced > 0) {
@@ -204,6 +204,10 @@ Schedule choose_schedule(int kind, int M, int N, int K, int sms) {
     s.G = static_cast<int>(g);
     s.max_ctas = sms > s.G ? sms : s.G;
     return s;
+}
+
+Schedule choose_schedule(int kind, int M, int N, int K, int sms) {
+    return schedule_for(kind, M, N, K, sms, table_lookup(kind, M, N, K));
 }
 
 // True when some tile's units are spread over more than one CTA.
@@ -852,6 +856,11 @@ int qg_dispatch_get(int kind, int M, int N, int K) {
     DeviceInfo* d = device_info();
     if (!d) return 0;
     return cached_schedule(kind, M, N, K, d->sms).s.G;
+}
+
+int qg_dispatch_rule(int kind, int M, int N, int K, int sms) {
+    if (max_m(kind) == 0 || M < 1 || M > max_m(kind) || N < 1 || K < 1 || sms < 1) return 0;
+    return schedule_for(kind, M, N, K, sms, 0).G;
 }
 
 void qg_dispatch_clear(void) {
