@@ -276,6 +276,9 @@ qg_status qg_quantize_act_e4m3(const void *X, int64_t ldx, uint8_t *Xq, int64_t 
  *   W, W_scale, Y, ldy       as for qgemm_fp8_block
  *   M, N, K  1 <= M <= 65536, N >= 1, K % 16 == 0
  *   workspace as for qgemm_fp8_block, with kind QG_KIND_W8A8.
+ * Y is written through TMA stores when it is 16-byte aligned and ldy and N
+ * are multiples of 8, by plain stores otherwise (same values; only elements
+ * of Y[0..M-1][0..N-1] are written either way).
  * Results match the strict-order FP32 fold within the header's comparison
  * rule.
  */
