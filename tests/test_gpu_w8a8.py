@@ -129,7 +129,7 @@ def test_w8a8_strided_and_padding_untouched():
 
 
 @pytest.mark.parametrize("M,N,y_pad,shift", [(70, 504, 8, 0), (130, 248, 24, 0), (33, 384, 0, 0),
-                                             (70, 500, 12, 0), (70, 504, 8, 1)])
+                                             (300, 200, 8, 0), (70, 500, 12, 0), (70, 504, 8, 1)])
 def test_w8a8_y_store_paths(M, N, y_pad, shift):
     """Y through the TMA store (Y 16-byte aligned, ldy and N multiples of 8:
     ragged last tiles clipped at N and at M, padding columns and the rows
